@@ -1,0 +1,201 @@
+"""Python binding of the GB300 FP32 SGEMM C ABI (include/b2g_sgemm.h).
+
+Argument marshalling only: every step of the GEMM runs in the CUDA library
+``libb2g_sgemm.so``; torch supplies device memory and the current stream.  The
+library must be built first (``dense_fp32_gemm_07_gb300.build.build()``); there
+is no fallback when it is missing.
+
+Low-level names mirror the C ABI one to one (``b2g_sgemm``, ``b2g_sgemm_ex``,
+``b2g_sgemm_with_plan``, ...) and take raw device pointers; ``sgemm`` is the
+tensor-level convenience: ``C <- alpha * op(A) @ op(B) + beta * C`` in place.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libb2g_sgemm.so")
+
+B2G_OK = 0
+B2G_ERR_INVALID_DIM = -1
+B2G_ERR_INVALID_LD = -2
+B2G_ERR_NULL = -3
+B2G_ERR_LAUNCH = -4
+B2G_ERR_DEVICE = -5
+B2G_ERR_UNSUPPORTED = -6
+B2G_ERR_INVALID_PLAN = -7
+B2G_ERR_TENSOR_MAP = -8
+B2G_ERR_CUDA = -9
+B2G_ERR_TIMEOUT = -10
+
+# every symbol include/b2g_sgemm.h declares
+EXPORTS = (
+    "b2g_sgemm", "b2g_sgemm_ex", "b2g_sgemm_with_plan", "b2g_sgemm_select_plan",
+    "b2g_plan_count", "b2g_plan_name", "b2g_plan_info", "b2g_status", "b2g_set_wait_limit_ns",
+    "b2g_debug_stop_after", "b2g_strerror", "b2g_version",
+)
+
+_lock = threading.Lock()
+_lib = None
+
+
+class B2GError(RuntimeError):
+    def __init__(self, code: int):
+        self.code = code
+        super().__init__(f"b2g error {code}: {b2g_strerror(code)}")
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is not built; run dense_fp32_gemm_07_gb300.build.build() "
+                "(or __graft_entry__.build()) first")
+        lib = ctypes.CDLL(LIB_PATH)
+        i, f, vp, u64 = ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_ulonglong
+        gemm = [i, i, i, f, vp, i, vp, i, f, vp, i, vp]
+        lib.b2g_sgemm.argtypes = gemm
+        lib.b2g_sgemm_ex.argtypes = [i, i] + gemm
+        lib.b2g_sgemm_with_plan.argtypes = [i, i, i] + gemm
+        lib.b2g_sgemm_select_plan.argtypes = [i, i, i, i, i, f, vp, i, vp, i, vp, i]
+        lib.b2g_plan_count.argtypes = []
+        lib.b2g_plan_name.argtypes = [i]
+        lib.b2g_plan_name.restype = ctypes.c_char_p
+        lib.b2g_plan_info.argtypes = [i, ctypes.POINTER(ctypes.c_int)]
+        lib.b2g_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint), i]
+        lib.b2g_set_wait_limit_ns.argtypes = [u64]
+        lib.b2g_debug_stop_after.argtypes = [i]
+        lib.b2g_strerror.argtypes = [i]
+        lib.b2g_strerror.restype = ctypes.c_char_p
+        lib.b2g_version.argtypes = []
+        lib.b2g_version.restype = ctypes.c_char_p
+        for name in EXPORTS:
+            if not hasattr(lib, name):
+                raise RuntimeError(f"{LIB_PATH} does not export {name}")
+        _lib = lib
+        return lib
+
+
+def library():
+    """The loaded ctypes library (raises when it has not been built)."""
+    return _load()
+
+
+# --- one-to-one wrappers of the C ABI -------------------------------------------
+
+def b2g_sgemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> int:
+    return _load().b2g_sgemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
+
+
+def b2g_sgemm_ex(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> int:
+    return _load().b2g_sgemm_ex(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                                stream)
+
+
+def b2g_sgemm_with_plan(plan, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                        stream=0) -> int:
+    return _load().b2g_sgemm_with_plan(plan, transA, transB, M, N, K, alpha, A, lda, B, ldb,
+                                       beta, C, ldc, stream)
+
+
+def b2g_sgemm_select_plan(transA, transB, M, N, K, alpha, A, lda, B, ldb, C, ldc) -> int:
+    return _load().b2g_sgemm_select_plan(transA, transB, M, N, K, alpha, A, lda, B, ldb, C, ldc)
+
+
+def b2g_plan_count() -> int:
+    return _load().b2g_plan_count()
+
+
+def b2g_plan_name(plan: int) -> Optional[str]:
+    r = _load().b2g_plan_name(plan)
+    return r.decode() if r is not None else None
+
+
+def b2g_plan_info(plan: int) -> dict:
+    buf = (ctypes.c_int * 9)()
+    rc = _load().b2g_plan_info(plan, buf)
+    if rc:
+        raise B2GError(rc)
+    keys = ("BM", "BN", "BK", "stages", "TN", "alayout", "feed", "threads", "smem_bytes")
+    return dict(zip(keys, list(buf)))
+
+
+def b2g_status(stream=0, clear: bool = True):
+    """(rc, flags): synchronises `stream` and reads the kernels' status word."""
+    flags = ctypes.c_uint(0)
+    rc = _load().b2g_status(stream, ctypes.byref(flags), int(clear))
+    return rc, flags.value
+
+
+def b2g_set_wait_limit_ns(ns: int) -> int:
+    return _load().b2g_set_wait_limit_ns(int(ns))
+
+
+def b2g_debug_stop_after(n: int) -> int:
+    return _load().b2g_debug_stop_after(int(n))
+
+
+def b2g_strerror(code: int) -> str:
+    return _load().b2g_strerror(code).decode()
+
+
+def b2g_version() -> str:
+    return _load().b2g_version().decode()
+
+
+# --- tensor-level convenience ----------------------------------------------------
+
+def _stream_handle(stream) -> int:
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(t, name):
+    import torch
+
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or t.dim() != 2:
+        raise TypeError(f"{name} must be a 2-D torch.float32 tensor")
+    if not t.is_cuda:
+        raise TypeError(f"{name} must be on a CUDA device")
+    if t.size(1) > 1 and t.stride(1) != 1:
+        raise ValueError(f"{name} must have unit column stride (row-major rows)")
+    return max(1, t.stride(0)) if t.size(0) > 1 else max(1, t.size(1))
+
+
+def sgemm(A, B, C, alpha: float = 1.0, beta: float = 0.0, transA: bool = False,
+          transB: bool = False, plan: Optional[int] = None, stream=None):
+    """C <- alpha * op(A) @ op(B) + beta * C on the current (or given) stream.
+
+    A, B, C are 2-D float32 CUDA tensors with unit column stride; their row
+    stride is the leading dimension.  op(A) is A.T when transA (A stored K x M),
+    likewise for B.  Returns C.  Raises B2GError on a library error code.
+    """
+    lda, ldb, ldc = _check(A, "A"), _check(B, "B"), _check(C, "C")
+    M, K = (A.size(1), A.size(0)) if transA else (A.size(0), A.size(1))
+    Kb, N = (B.size(1), B.size(0)) if transB else (B.size(0), B.size(1))
+    if Kb != K or tuple(C.shape) != (M, N):
+        raise ValueError(f"shape mismatch: op(A) {M}x{K}, op(B) {Kb}x{N}, C {tuple(C.shape)}")
+    s = _stream_handle(stream)
+    args = (M, N, K, float(alpha), A.data_ptr(), lda, B.data_ptr(), ldb, float(beta),
+            C.data_ptr(), ldc, s)
+    if plan is None:
+        rc = b2g_sgemm_ex(int(transA), int(transB), *args)
+    else:
+        rc = b2g_sgemm_with_plan(int(plan), int(transA), int(transB), *args)
+    if rc:
+        raise B2GError(rc)
+    return C
+
+
+def plans():
+    """Names of the compiled plans, by index."""
+    return [b2g_plan_name(i) for i in range(b2g_plan_count())]

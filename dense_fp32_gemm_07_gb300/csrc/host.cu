@@ -1,0 +1,351 @@
+// host.cu -- the C ABI (include/b2g_sgemm.h): argument checks, the quick
+// returns, plan choice from the tune table, bulk-tensor descriptors, launch.
+//
+// Quick returns follow the reference-BLAS convention (the pages are silent):
+// M == 0 or N == 0 launches nothing; K == 0 or alpha == 0 only scales C by beta
+// (beta == 0 writes zeros without reading C).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/b2g_sgemm.h"
+#include "sgemm_params.h"
+#include "tune_table.h"
+
+namespace b2g {
+
+// The device status word every kernel may flag (timeouts).  One per device
+// context; the host passes its address to each kernel.
+__device__ unsigned int g_status_word;
+
+// C = beta * C over an M x N window with leading dimension ldc (beta == 0 writes
+// zeros without reading C).  Used when the product term vanishes.
+__global__ void scale_c_kernel(int M, int N, float beta, float* __restrict__ C, long long ldc) {
+  const long long total = (long long)M * N;
+  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const long long i = idx / N, j = idx - i * N;
+    float* q = C + i * ldc + j;
+    *q = (beta == 0.f) ? 0.f : beta * *q;
+  }
+}
+
+namespace {
+
+struct DeviceState {
+  bool init = false;
+  int err = 0;
+  int sms = 0;
+  unsigned int* status = nullptr;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
+std::atomic<int> g_debug_stop{-1};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+bool g_encode_init = false;
+
+int device_state(DeviceState** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return B2G_ERR_DEVICE;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& d = g_dev[dev];
+  if (!d.init) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      return B2G_ERR_DEVICE;  // not cached: a later call may succeed
+    }
+    if (major != 10 || minor != 3) {
+      d.err = B2G_ERR_DEVICE;
+    } else if (cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_status_word) !=
+               cudaSuccess) {
+      d.err = B2G_ERR_CUDA;
+    }
+    d.init = true;
+  }
+  if (d.err) return d.err;
+  *out = &d;
+  return 0;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_encode_init) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    g_encode_init = true;
+  }
+  return g_encode;
+}
+
+int num_plans() { return kNumPlansTMA + kNumPlansGeneral; }
+
+const Plan* plan_at(int i) {
+  if (i < 0) return nullptr;
+  if (i < kNumPlansTMA) return &kPlansTMA[i];
+  i -= kNumPlansTMA;
+  if (i < kNumPlansGeneral) return &kPlansGeneral[i];
+  return nullptr;
+}
+
+int plan_index(const char* name) {
+  for (int i = 0; i < num_plans(); ++i)
+    if (std::strcmp(plan_at(i)->name, name) == 0) return i;
+  return -1;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Call {
+  int transA, transB, M, N, K;
+  float alpha, beta;
+  const float* A;
+  int lda;
+  const float* B;
+  int ldb;
+  float* C;
+  int ldc;
+};
+
+// 0 when the arguments are valid, else the B2G_ERR_* code.
+int validate(const Call& c) {
+  if (c.M < 0 || c.N < 0 || c.K < 0) return B2G_ERR_INVALID_DIM;
+  const int a_cols = c.transA ? c.M : c.K;
+  const int b_cols = c.transB ? c.K : c.N;
+  if (c.lda < (a_cols > 1 ? a_cols : 1) || c.ldb < (b_cols > 1 ? b_cols : 1) ||
+      c.ldc < (c.N > 1 ? c.N : 1))
+    return B2G_ERR_INVALID_LD;
+  if (c.M == 0 || c.N == 0) return 0;
+  if (c.C == nullptr) return B2G_ERR_NULL;
+  if (c.K > 0 && c.alpha != 0.f && (c.A == nullptr || c.B == nullptr)) return B2G_ERR_NULL;
+  return 0;
+}
+
+bool needs_gemm(const Call& c) { return c.M > 0 && c.N > 0 && c.K > 0 && c.alpha != 0.f; }
+
+int operand_class(const Call& c) {
+  const bool ab_aligned = aligned16(c.A) && aligned16(c.B) && c.lda % 4 == 0 && c.ldb % 4 == 0;
+  if (!ab_aligned || c.transB) return kClassGeneral;
+  if (c.transA) return kClassFastTransA;
+  return c.K % 4 == 0 ? kClassFast : kClassGeneral;
+}
+
+bool plan_accepts(const Plan& pl, const Call& c) {
+  if (pl.feed == kFeedCpAsync) return true;
+  const int cls = operand_class(c);
+  if (pl.alayout == kAKChunk) return cls == kClassFast;
+  return cls == kClassFastTransA;
+}
+
+int select_plan(const Call& c) {
+  const int cls = operand_class(c);
+  for (const TuneRule& r : kTuneTable) {
+    if (r.cls == cls && c.M >= r.m_min && c.M <= r.m_max && c.N >= r.n_min && c.N <= r.n_max) {
+      const int i = plan_index(r.plan);
+      if (i >= 0) return i;
+    }
+  }
+  return plan_index("gen_128x128x16_s4");
+}
+
+int encode_2d(CUtensorMap* m, const float* base, long long inner, long long outer,
+              long long row_stride_elems, int box_inner, int box_outer) {
+  auto enc = encoder();
+  if (!enc) return B2G_ERR_TENSOR_MAP;
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+  cuuint64_t strides[1] = {(cuuint64_t)row_stride_elems * 4};
+  cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : B2G_ERR_TENSOR_MAP;
+}
+
+// Row-major A (M x K, lda) seen as a 3-D tensor {4, M, K/4}: element (e, r, q) is
+// A[r][4q + e].  A box {4, BM, BK/4} lands in shared memory as [BK/4][BM][4].
+int encode_a_kchunk(CUtensorMap* m, const float* A, int M, int K, int lda, int BM, int BK) {
+  auto enc = encoder();
+  if (!enc) return B2G_ERR_TENSOR_MAP;
+  cuuint64_t dims[3] = {4, (cuuint64_t)M, (cuuint64_t)(K / 4)};
+  cuuint64_t strides[2] = {(cuuint64_t)lda * 4, 16};
+  cuuint32_t box[3] = {4, (cuuint32_t)BM, (cuuint32_t)(BK / 4)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(A), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : B2G_ERR_TENSOR_MAP;
+}
+
+int launch_scale(const Call& c, const DeviceState& d, cudaStream_t st) {
+  const long long total = (long long)c.M * c.N;
+  long long blocks = (total + 255) / 256;
+  const long long cap = (long long)d.sms * 8;
+  if (blocks > cap) blocks = cap;
+  void* args[] = {(void*)&c.M, (void*)&c.N, (void*)&c.beta, (void*)&c.C, nullptr};
+  long long ldc = c.ldc;
+  args[4] = &ldc;
+  cudaError_t e = cudaLaunchKernel(reinterpret_cast<const void*>(&scale_c_kernel),
+                                   dim3((unsigned)blocks), dim3(256), args, 0, st);
+  return e == cudaSuccess ? 0 : B2G_ERR_LAUNCH;
+}
+
+int run(const Call& c, int forced_plan, void* stream) {
+  int rc = validate(c);
+  if (rc) return rc;
+  if (c.M == 0 || c.N == 0) return 0;
+  if (forced_plan >= num_plans()) return B2G_ERR_INVALID_PLAN;
+  DeviceState* d = nullptr;
+  rc = device_state(&d);
+  if (rc) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (!needs_gemm(c)) return launch_scale(c, *d, st);
+
+  const int pi = forced_plan >= 0 ? forced_plan : select_plan(c);
+  const Plan* pl = plan_at(pi);
+  if (!pl) return B2G_ERR_INVALID_PLAN;
+  if (!plan_accepts(*pl, c)) return B2G_ERR_UNSUPPORTED;
+
+  SgemmParams p;
+  p.M = c.M, p.N = c.N, p.K = c.K;
+  p.alpha = c.alpha, p.beta = c.beta;
+  p.A = c.A, p.lda = c.lda, p.B = c.B, p.ldb = c.ldb, p.C = c.C, p.ldc = c.ldc;
+  p.transA = c.transA, p.transB = c.transB;
+  p.c_vec4 = aligned16(c.C) && c.ldc % 4 == 0;
+  p.tiles_m = (c.M + pl->BM - 1) / pl->BM;
+  p.tiles_n = (c.N + pl->BN - 1) / pl->BN;
+  p.group_m = 8;
+  p.k_tiles = (c.K + pl->BK - 1) / pl->BK;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+  p.debug_stop_ktile = g_debug_stop.load();
+  p.status = d->status;
+
+  CUtensorMap tmA, tmB;
+  const CUtensorMap* pA = nullptr;
+  const CUtensorMap* pB = nullptr;
+  if (pl->feed == kFeedTMA) {
+    if (pl->alayout == kAKChunk)
+      rc = encode_a_kchunk(&tmA, c.A, c.M, c.K, c.lda, pl->BM, pl->BK);
+    else
+      rc = encode_2d(&tmA, c.A, c.M, c.K, c.lda, pl->BM, pl->BK);  // A stored K x M
+    if (!rc) rc = encode_2d(&tmB, c.B, c.N, c.K, c.ldb, pl->BN, pl->BK);
+    if (rc) return rc;
+    pA = &tmA, pB = &tmB;
+  }
+  cudaError_t e = pl->launch(p, pA, pB, d->sms, st);
+  return e == cudaSuccess ? 0 : B2G_ERR_LAUNCH;
+}
+
+}  // namespace
+}  // namespace b2g
+
+using namespace b2g;
+
+extern "C" {
+
+int b2g_sgemm(int M, int N, int K, float alpha, const float* A, int lda, const float* B, int ldb,
+              float beta, float* C, int ldc, void* stream) {
+  return run(Call{0, 0, M, N, K, alpha, beta, A, lda, B, ldb, C, ldc}, -1, stream);
+}
+
+int b2g_sgemm_ex(int transA, int transB, int M, int N, int K, float alpha, const float* A, int lda,
+                 const float* B, int ldb, float beta, float* C, int ldc, void* stream) {
+  return run(Call{transA != 0, transB != 0, M, N, K, alpha, beta, A, lda, B, ldb, C, ldc}, -1,
+             stream);
+}
+
+int b2g_sgemm_with_plan(int plan, int transA, int transB, int M, int N, int K, float alpha,
+                        const float* A, int lda, const float* B, int ldb, float beta, float* C,
+                        int ldc, void* stream) {
+  if (plan < 0 || plan >= num_plans()) return B2G_ERR_INVALID_PLAN;
+  return run(Call{transA != 0, transB != 0, M, N, K, alpha, beta, A, lda, B, ldb, C, ldc}, plan,
+             stream);
+}
+
+int b2g_sgemm_select_plan(int transA, int transB, int M, int N, int K, float alpha, const float* A,
+                          int lda, const float* B, int ldb, const float* C, int ldc) {
+  Call c{transA != 0, transB != 0, M, N, K, alpha, 0.f, A, lda, B, ldb, const_cast<float*>(C), ldc};
+  const int rc = validate(c);
+  if (rc) return rc;
+  if (!needs_gemm(c)) return num_plans();
+  return select_plan(c);
+}
+
+int b2g_plan_count(void) { return num_plans(); }
+
+const char* b2g_plan_name(int plan) {
+  const Plan* p = plan_at(plan);
+  return p ? p->name : nullptr;
+}
+
+int b2g_plan_info(int plan, int* info) {
+  const Plan* p = plan_at(plan);
+  if (!p) return B2G_ERR_INVALID_PLAN;
+  if (!info) return B2G_ERR_NULL;
+  const int v[9] = {p->BM, p->BN, p->BK, p->stages, p->TN, p->alayout, p->feed, p->threads,
+                    p->smem_bytes};
+  for (int i = 0; i < 9; ++i) info[i] = v[i];
+  return 0;
+}
+
+int b2g_status(void* stream, unsigned int* flags, int clear) {
+  if (!flags) return B2G_ERR_NULL;
+  DeviceState* d = nullptr;
+  const int rc = device_state(&d);
+  if (rc) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  unsigned int v = 0;
+  if (cudaMemcpyAsync(&v, d->status, sizeof(v), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return B2G_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return B2G_ERR_CUDA;
+  if (clear && v) {
+    if (cudaMemsetAsync(d->status, 0, sizeof(unsigned int), st) != cudaSuccess) return B2G_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return B2G_ERR_CUDA;
+  }
+  *flags = v;
+  return v ? B2G_ERR_TIMEOUT : 0;
+}
+
+int b2g_set_wait_limit_ns(unsigned long long ns) {
+  if (ns == 0) return B2G_ERR_INVALID_DIM;
+  g_wait_limit_ns.store(ns);
+  return 0;
+}
+
+int b2g_debug_stop_after(int n) {
+  g_debug_stop.store(n < 0 ? -1 : n);
+  return 0;
+}
+
+const char* b2g_strerror(int code) {
+  switch (code) {
+    case B2G_OK: return "ok";
+    case B2G_ERR_INVALID_DIM: return "invalid dimension (M, N or K < 0)";
+    case B2G_ERR_INVALID_LD: return "invalid leading dimension";
+    case B2G_ERR_NULL: return "null pointer for an operand that must be read or written";
+    case B2G_ERR_LAUNCH: return "kernel launch failed";
+    case B2G_ERR_DEVICE: return "no usable sm_103 device is current";
+    case B2G_ERR_UNSUPPORTED: return "the requested plan cannot take these operands";
+    case B2G_ERR_INVALID_PLAN: return "plan index out of range";
+    case B2G_ERR_TENSOR_MAP: return "bulk-tensor descriptor rejected by the driver";
+    case B2G_ERR_CUDA: return "CUDA runtime call failed";
+    case B2G_ERR_TIMEOUT: return "a kernel's bounded wait ran out (see b2g_status flags)";
+    default: return "unknown error code";
+  }
+}
+
+const char* b2g_version(void) { return "b2g_sgemm 0.1 (sm_103a)"; }
+
+}  // extern "C"

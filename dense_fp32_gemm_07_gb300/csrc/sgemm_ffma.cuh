@@ -1,0 +1,346 @@
+// sgemm_ffma.cuh -- persistent, warp-specialised FP32 SGEMM on the CUDA cores.
+//
+//   C = alpha * op(A) * op(B) + beta * C      (row-major, FP32 FFMA throughout)
+//
+// The problem statement is the GEMM handbook's ("GEMM 优化之路", section
+// 问题定义与性能上限).  The design keeps what the pages' optimisation chain
+// establishes -- block tiling in shared memory (section v2), an 8x8 per-thread
+// register outer product (section v4), 128-bit fragment loads (section v5),
+// overlapped loading with several stages (section 接下来的优化方向: double
+// buffering / cp.async pipelining) and masked edges (练习 2) -- and re-builds it
+// around sm_103a's asynchronous machinery:
+//
+//  * one CTA per SM, persistent over output tiles (grouped along M for L2 reuse);
+//  * an S-stage shared-memory ring with `full`/`empty` mbarriers;
+//  * producer warp(s) fill the ring: either one elected thread issuing
+//    bulk-tensor (TMA) copies, or warps issuing 4-byte cp.async with zero fill
+//    for arbitrary alignment, leading dimensions and transposes;
+//  * consumer warps each own a 32 x (8*TN) warp tile, as 4 x 8 threads with an
+//    8 x TN register tile; per k they run 8*TN FFMAs from registers;
+//  * B is staged [BK][BN] and a quarter-warp's 16-byte loads cover 128
+//    contiguous bytes, so B fragment loads are free of bank conflicts;
+//  * A is staged either k-chunked ([BK/4][BM][4], written directly by a 3-D
+//    TMA view, one 16-byte load gives a row's next 4 k) or transposed
+//    ([BK][BM], one 16-byte load gives 4 rows at one k); both give 128-bit
+//    fragment loads without bank conflicts;
+//  * every mbarrier wait is bounded: on timeout a flag goes to the status word
+//    and the kernel leaves instead of hanging.
+//
+// Every output element is a k-ordered chain of FP32 FFMAs, so a given plan is
+// bitwise reproducible run to run.
+#pragma once
+#include <algorithm>
+#include <atomic>
+#include <cstring>
+
+#include "ptx.cuh"
+#include "sgemm_params.h"
+
+namespace b2g {
+
+template <int BM, int BN, int BK, int WM, int WN, int TN, int STAGES, int ALAY, int FEED,
+          int PWARPS>
+struct FfmaCfg {
+  static constexpr int TM = 8;
+  static constexpr int kConsumerWarps = WM * WN;
+  static constexpr int kConsumers = kConsumerWarps * 32;
+  static constexpr int kProducers = PWARPS * 32;
+  static constexpr int kThreads = kConsumers + kProducers;
+  static constexpr int kAStage = BM * BK;  // floats per stage
+  static constexpr int kBStage = BK * BN;
+  static constexpr int kStageBytes = (kAStage + kBStage) * 4;
+  static constexpr int kSmemBytes = STAGES * kStageBytes + 2 * STAGES * 8;
+  static_assert(BM == WM * 32, "a warp tile is 32 rows");
+  static_assert(BN == WN * 8 * TN, "a warp tile is 8*TN columns");
+  static_assert(TN % 4 == 0 && BK % 4 == 0, "16-byte fragments");
+  static_assert(BM <= 256 && BN <= 256, "bulk-tensor box dimensions are at most 256");
+  static_assert(FEED == kFeedTMA ? PWARPS == 1 : PWARPS >= 1, "producer warps");
+  static_assert(FEED == kFeedTMA || ALAY == kAKMajor, "4-byte feed writes the transposed layout");
+  static_assert(FEED == kFeedTMA || (BM * BK) % kProducers == 0, "A tile split evenly");
+  static_assert(FEED == kFeedTMA || (BK * BN) % kProducers == 0, "B tile split evenly");
+};
+
+// Output tile of linear index `tile`: tiles run down a group of `group_m` tile
+// rows before moving one tile column right, so CTAs that run together share A
+// row panels and B column panels in L2.
+__device__ __forceinline__ void tile_coords(const SgemmParams& p, int tile, int& tm, int& tn) {
+  const int per_group = p.group_m * p.tiles_n;
+  const int g = tile / per_group;
+  const int first_m = g * p.group_m;
+  const int gsize = min(p.tiles_m - first_m, p.group_m);
+  const int r = tile - g * per_group;
+  tm = first_m + r % gsize;
+  tn = r / gsize;
+}
+
+template <int BM, int BN, int BK, int WM, int WN, int TN, int STAGES, int ALAY, int FEED,
+          int PWARPS>
+__global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
+    sgemm_ffma_kernel(const __grid_constant__ SgemmParams p,
+                      const __grid_constant__ CUtensorMap tmA,
+                      const __grid_constant__ CUtensorMap tmB) {
+  using Cfg = FfmaCfg<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS>;
+  extern __shared__ __align__(1024) unsigned char smem[];
+  float* sA = reinterpret_cast<float*>(smem);
+  float* sB = sA + STAGES * Cfg::kAStage;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * Cfg::kBStage);
+  const uint32_t full0 = smem_addr(bars);
+  const uint32_t empty0 = smem_addr(bars + STAGES);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8 * s, FEED == kFeedTMA ? 1 : Cfg::kProducers);
+      mbar_init(empty0 + 8 * s, Cfg::kConsumerWarps);
+    }
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  __syncthreads();
+
+  const int total_tiles = p.tiles_m * p.tiles_n;
+
+  // ------------------------------------------------------------------ producer
+  if (warp >= Cfg::kConsumerWarps) {
+    int stage = 0;
+    uint32_t phase = 0;
+    int issued = 0;
+    if constexpr (FEED == kFeedTMA) {
+      if (lane != 0) return;
+      prefetch_tmap(&tmA);
+      prefetch_tmap(&tmB);
+      for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+        int tm, tn;
+        tile_coords(p, tile, tm, tn);
+        const int m0 = tm * BM, n0 = tn * BN;
+        for (int kt = 0; kt < p.k_tiles; ++kt) {
+          if (p.debug_stop_ktile >= 0 && issued >= p.debug_stop_ktile) goto drain_tma;
+          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, p.wait_limit_ns, p.status,
+                         kStatusTimeoutEmpty))
+            goto drain_tma;
+          const uint32_t fb = full0 + 8 * stage;
+          mbar_arrive_expect_tx(fb, Cfg::kStageBytes);
+          const uint32_t dA = smem_addr(sA + stage * Cfg::kAStage);
+          const uint32_t dB = smem_addr(sB + stage * Cfg::kBStage);
+          if constexpr (ALAY == kAKChunk)
+            tma_load_3d(dA, &tmA, 0, m0, kt * (BK / 4), fb);  // view {4, M, K/4}
+          else
+            tma_load_2d(dA, &tmA, m0, kt * BK, fb);  // A stored K x M
+          tma_load_2d(dB, &tmB, n0, kt * BK, fb);
+          ++issued;
+          if (++stage == STAGES) stage = 0, phase ^= 1u;
+        }
+      }
+    drain_tma:
+      // Leave only after every copy this thread started has landed.
+      for (int d = 0, pending = min(issued, STAGES); d < pending; ++d) {
+        if (--stage < 0) stage = STAGES - 1, phase ^= 1u;
+        if (!mbar_wait(full0 + 8 * stage, phase, p.wait_limit_ns, p.status, kStatusTimeoutDrain))
+          break;
+      }
+    } else {
+      const int pt = threadIdx.x - Cfg::kConsumers;
+      for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+        int tm, tn;
+        tile_coords(p, tile, tm, tn);
+        const int m0 = tm * BM, n0 = tn * BN;
+        for (int kt = 0; kt < p.k_tiles; ++kt) {
+          if (p.debug_stop_ktile >= 0 && issued >= p.debug_stop_ktile) goto drain_cp;
+          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, p.wait_limit_ns, p.status,
+                         kStatusTimeoutEmpty))
+            goto drain_cp;
+          const int k0 = kt * BK;
+          const uint32_t dA = smem_addr(sA + stage * Cfg::kAStage);
+          const uint32_t dB = smem_addr(sB + stage * Cfg::kBStage);
+          // A tile -> As[k][m]; consecutive threads take consecutive m, so the
+          // shared-memory writes hit consecutive banks.
+#pragma unroll 4
+          for (int it = 0; it < (BM * BK) / Cfg::kProducers; ++it) {
+            const int idx = it * Cfg::kProducers + pt;
+            const int r = idx % BM, k = idx / BM;
+            const int gr = m0 + r, gk = k0 + k;
+            const bool ok = gr < p.M && gk < p.K;
+            const long long off = ok ? (p.transA ? (long long)gk * p.lda + gr
+                                                 : (long long)gr * p.lda + gk)
+                                     : 0;
+            cp_async_4(dA + 4u * (k * BM + r), p.A + off, ok ? 4u : 0u);
+          }
+          // B tile -> Bs[k][n]
+#pragma unroll 4
+          for (int it = 0; it < (BK * BN) / Cfg::kProducers; ++it) {
+            const int idx = it * Cfg::kProducers + pt;
+            const int n = idx % BN, k = idx / BN;
+            const int gn = n0 + n, gk = k0 + k;
+            const bool ok = gn < p.N && gk < p.K;
+            const long long off = ok ? (p.transB ? (long long)gn * p.ldb + gk
+                                                 : (long long)gk * p.ldb + gn)
+                                     : 0;
+            cp_async_4(dB + 4u * (k * BN + n), p.B + off, ok ? 4u : 0u);
+          }
+          cp_async_arrive_noinc(full0 + 8 * stage);
+          ++issued;
+          if (++stage == STAGES) stage = 0, phase ^= 1u;
+        }
+      }
+    drain_cp:
+      cp_async_wait_all();
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------------ consumers
+  const int wm = warp % WM, wn = warp / WM;
+  const int tr = lane >> 3, tc = lane & 7;
+  // Thread rows: k-chunked A gives rows wm*32 + tr + 4i (the 4 thread rows of a
+  // warp read 4 consecutive 16-byte vectors); transposed A gives rows
+  // wm*32 + 4tr + (i & 3) + 16(i >> 2).  Thread columns:
+  // wn*8*TN + 4tc + 32(j >> 2) + (j & 3).
+  const int a_off = (ALAY == kAKChunk) ? (wm * 32 + tr) * 4 : wm * 32 + 4 * tr;
+  const int b_off = wn * (8 * TN) + 4 * tc;
+  int stage = 0;
+  uint32_t phase = 0;
+
+  for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+    int tm, tn;
+    tile_coords(p, tile, tm, tn);
+    float acc[8][TN];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
+
+    for (int kt = 0; kt < p.k_tiles; ++kt) {
+      if (!mbar_wait(full0 + 8 * stage, phase, p.wait_limit_ns, p.status, kStatusTimeoutFull))
+        return;  // the status word says why; the producer drains and leaves too
+      const float* As = sA + stage * Cfg::kAStage + a_off;
+      const float* Bs = sB + stage * Cfg::kBStage + b_off;
+      if constexpr (ALAY == kAKChunk) {
+#pragma unroll
+        for (int q = 0; q < BK / 4; ++q) {
+          float4 a4[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            a4[i] = *reinterpret_cast<const float4*>(As + q * BM * 4 + 16 * i);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            float b[TN];
+#pragma unroll
+            for (int j4 = 0; j4 < TN / 4; ++j4) {
+              const float4 v =
+                  *reinterpret_cast<const float4*>(Bs + (4 * q + kk) * BN + 32 * j4);
+              b[4 * j4 + 0] = v.x, b[4 * j4 + 1] = v.y, b[4 * j4 + 2] = v.z, b[4 * j4 + 3] = v.w;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float a = kk == 0 ? a4[i].x : kk == 1 ? a4[i].y : kk == 2 ? a4[i].z : a4[i].w;
+#pragma unroll
+              for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a, b[j], acc[i][j]);
+            }
+          }
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < BK; ++k) {
+          const float4 a0 = *reinterpret_cast<const float4*>(As + k * BM);
+          const float4 a1 = *reinterpret_cast<const float4*>(As + k * BM + 16);
+          const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+          float b[TN];
+#pragma unroll
+          for (int j4 = 0; j4 < TN / 4; ++j4) {
+            const float4 v = *reinterpret_cast<const float4*>(Bs + k * BN + 32 * j4);
+            b[4 * j4 + 0] = v.x, b[4 * j4 + 1] = v.y, b[4 * j4 + 2] = v.z, b[4 * j4 + 3] = v.w;
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * stage);
+      if (++stage == STAGES) stage = 0, phase ^= 1u;
+    }
+
+    // Epilogue: C = alpha*acc + beta*C, C read only when beta != 0, float4
+    // where the 4 columns are in range and C is 16-byte aligned.
+    const int m0 = tm * BM, n0 = tn * BN;
+    const float alpha = p.alpha, beta = p.beta;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = m0 + ((ALAY == kAKChunk) ? wm * 32 + tr + 4 * i
+                                            : wm * 32 + 4 * tr + (i & 3) + 16 * (i >> 2));
+      if (r >= p.M) continue;
+      float* crow = p.C + (long long)r * p.ldc;
+#pragma unroll
+      for (int j4 = 0; j4 < TN / 4; ++j4) {
+        const int c = n0 + b_off + 32 * j4;
+        const float* av = &acc[i][4 * j4];
+        if (p.c_vec4 && c + 3 < p.N) {
+          float4 o;
+          if (beta != 0.f) {
+            const float4 cv = *reinterpret_cast<const float4*>(crow + c);
+            o.x = fmaf(alpha, av[0], beta * cv.x);
+            o.y = fmaf(alpha, av[1], beta * cv.y);
+            o.z = fmaf(alpha, av[2], beta * cv.z);
+            o.w = fmaf(alpha, av[3], beta * cv.w);
+          } else {
+            o.x = alpha * av[0], o.y = alpha * av[1], o.z = alpha * av[2], o.w = alpha * av[3];
+          }
+          *reinterpret_cast<float4*>(crow + c) = o;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if (c + e < p.N) {
+              float* q = crow + c + e;
+              *q = (beta != 0.f) ? fmaf(alpha, av[e], beta * *q) : alpha * av[e];
+            }
+          }
+        }
+      }
+    }
+  }
+}
+
+template <int BM, int BN, int BK, int WM, int WN, int TN, int STAGES, int ALAY, int FEED,
+          int PWARPS>
+cudaError_t launch_ffma(const SgemmParams& p, const CUtensorMap* tmA, const CUtensorMap* tmB,
+                        int num_sms, cudaStream_t stream) {
+  using Cfg = FfmaCfg<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS>;
+  auto kern = sgemm_ffma_kernel<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS>;
+  // Per device, once: opt in to the dynamic shared memory size and record how
+  // many CTAs fit on one SM (the persistent grid is SMs x that).
+  static std::atomic<int> resident[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  int occ = resident[dev].load(std::memory_order_acquire);
+  if (occ == 0) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, Cfg::kThreads, Cfg::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    if (occ < 1) return cudaErrorInvalidConfiguration;
+    resident[dev].store(occ, std::memory_order_release);
+  }
+  const long long tiles = (long long)p.tiles_m * p.tiles_n;
+  const int grid = (int)std::min<long long>(tiles, (long long)num_sms * occ);
+  CUtensorMap none;
+  memset(&none, 0, sizeof(none));
+  SgemmParams pc = p;
+  CUtensorMap a = tmA ? *tmA : none, b = tmB ? *tmB : none;
+  void* args[] = {&pc, &a, &b};
+  return cudaLaunchKernel(reinterpret_cast<const void*>(kern), dim3(grid), dim3(Cfg::kThreads),
+                          args, Cfg::kSmemBytes, stream);
+}
+
+#define B2G_FFMA_PLAN(NAME, BM, BN, BK, WM, WN, TN, ST, ALAY, FEED, PW)                           \
+  Plan {                                                                                         \
+    NAME, BM, BN, BK, ST, TN, ALAY, FEED,                                                        \
+        FfmaCfg<BM, BN, BK, WM, WN, TN, ST, ALAY, FEED, PW>::kThreads,                           \
+        FfmaCfg<BM, BN, BK, WM, WN, TN, ST, ALAY, FEED, PW>::kSmemBytes,                         \
+        &launch_ffma<BM, BN, BK, WM, WN, TN, ST, ALAY, FEED, PW>                                 \
+  }
+
+}  // namespace b2g

@@ -1,0 +1,63 @@
+// sgemm_params.h -- what the host passes to every SGEMM kernel, and the plan
+// descriptor the tune table is made of.  Shared by the C-ABI layer and the
+// kernel translation units; holds no arithmetic.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace b2g {
+
+struct SgemmParams {
+  int M, N, K;
+  float alpha, beta;
+  const float* A;
+  long long lda;
+  const float* B;
+  long long ldb;
+  float* C;
+  long long ldc;
+  int transA;   // A stored K x M (op(A) = A^T); general feed only
+  int transB;   // B stored N x K (op(B) = B^T); general feed only
+  int c_vec4;   // C 16-byte aligned and ldc % 4 == 0: float4 epilogue allowed
+  int tiles_m, tiles_n, group_m, k_tiles;
+  unsigned long long wait_limit_ns;  // bound on every mbarrier wait
+  int debug_stop_ktile;              // < 0 normally; >= 0 stops the producer (timeout test)
+  unsigned int* status;              // device status word (timeout flags)
+};
+
+// How A is laid out in one shared-memory stage.
+enum ALayout : int {
+  kAKChunk = 0,  // [BK/4][BM][4]: a row's 4 consecutive k in one 16-byte vector
+  kAKMajor = 1,  // [BK][BM]: transposed, a column's m values contiguous
+};
+
+// How stages are filled.
+enum Feed : int {
+  kFeedTMA = 0,      // one elected thread issues bulk-tensor copies (aligned operands)
+  kFeedCpAsync = 1,  // producer warps issue 4-byte cp.async with zero fill (any layout)
+};
+
+constexpr int kMaxDevices = 64;
+
+// Launch one plan's kernel on `stream` with a persistent grid of at most
+// num_sms x (CTAs resident per SM) CTAs.  Returns the launch's CUDA error.
+using LaunchFn = cudaError_t (*)(const SgemmParams& p, const CUtensorMap* tmA,
+                                 const CUtensorMap* tmB, int num_sms, cudaStream_t stream);
+
+struct Plan {
+  const char* name;
+  int BM, BN, BK, stages, TN;
+  int alayout;  // ALayout
+  int feed;     // Feed
+  int threads;  // CTA size (consumer warps + producer warps)
+  int smem_bytes;
+  LaunchFn launch;
+};
+
+// Plans compiled in each kernel translation unit.
+extern const Plan kPlansTMA[];
+extern const int kNumPlansTMA;
+extern const Plan kPlansGeneral[];
+extern const int kNumPlansGeneral;
+
+}  // namespace b2g

@@ -1,0 +1,138 @@
+/*
+ * b2g_sgemm.h -- C ABI of the GB300 (sm_103a) FP32 SGEMM library.
+ *
+ * The operation (GEMM 优化之路 / CUDA 进阶手册, section 问题定义与性能上限):
+ *
+ *     C = alpha * op(A) * op(B) + beta * C
+ *
+ * with op(A) an M x K matrix, op(B) K x N and C M x N, all FP32 and ROW-MAJOR:
+ * element (i, k) of a stored matrix X with leading dimension ldX sits at
+ * X[i * ldX + k].  op(X) is X, or X transposed when the trans flag is set (the
+ * optimisation guide on gsyq.cn, section 6.4 step 8, lists A^T*B and A*B^T as
+ * the cases a complete GEMM handles).  Every product and sum is an FP32
+ * multiply-add (no reduced-precision arithmetic).
+ *
+ * Ownership and ordering
+ *   - A, B and C are DEVICE pointers owned by the caller; the library never
+ *     allocates, frees or keeps them.  C must not overlap A or B.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls are
+ *     asynchronous: they enqueue work on `stream` and return; the result is
+ *     ordered on that stream.  No call synchronises the host except
+ *     b2g_status().
+ *   - The calls are thread-safe.  Only sm_103 devices are supported.
+ *
+ * Return values: 0 on success, a negative B2G_ERR_* code otherwise.  Nothing is
+ * printed, nothing throws, nothing exits.  b2g_strerror() names a code.
+ */
+#ifndef B2G_SGEMM_H
+#define B2G_SGEMM_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define B2G_OK 0
+#define B2G_ERR_INVALID_DIM (-1)  /* M, N or K < 0 */
+#define B2G_ERR_INVALID_LD (-2)   /* a leading dimension smaller than its row width (min 1) */
+#define B2G_ERR_NULL (-3)         /* a pointer the call must dereference is NULL */
+#define B2G_ERR_LAUNCH (-4)       /* the kernel launch failed (cudaLaunchKernel's error) */
+#define B2G_ERR_DEVICE (-5)       /* no current device, or it is not sm_103 */
+#define B2G_ERR_UNSUPPORTED (-6)  /* the forced plan cannot run these operands */
+#define B2G_ERR_INVALID_PLAN (-7) /* plan index out of range */
+#define B2G_ERR_TENSOR_MAP (-8)   /* the driver refused a bulk-tensor descriptor */
+#define B2G_ERR_CUDA (-9)         /* another CUDA runtime call failed */
+#define B2G_ERR_TIMEOUT (-10)     /* b2g_status(): a kernel's bounded wait ran out */
+
+/*
+ * Row-major SGEMM, C = alpha*A*B + beta*C.
+ *   M, N, K  >= 0.  M == 0 or N == 0: nothing is launched, returns 0.
+ *   A        device, M x K, lda >= max(1, K).  Not read when K == 0 or alpha == 0.
+ *   B        device, K x N, ldb >= max(1, N).  Not read when K == 0 or alpha == 0.
+ *   C        device, M x N, ldc >= max(1, N).  Read only when beta != 0 (beta == 0
+ *            makes C write-only, so NaN/Inf already in C do not propagate).
+ *   stream   cudaStream_t or NULL.
+ * Any alignment and any leading dimension are accepted; 16-byte aligned
+ * operands with lda, ldb, ldc and K multiples of 4 take the bulk-tensor fed
+ * kernels, everything else the 4-byte-fed kernel.  The plan comes from the
+ * library's shape-keyed tune table.
+ */
+int b2g_sgemm(int M, int N, int K, float alpha, const float* A, int lda, const float* B, int ldb,
+              float beta, float* C, int ldc, void* stream);
+
+/*
+ * As b2g_sgemm with op() flags.  transA != 0: A is stored K x M (lda >= max(1, M))
+ * and op(A) = A^T.  transB != 0: B is stored N x K (ldb >= max(1, K)) and
+ * op(B) = B^T.  C is always M x N row-major.
+ */
+int b2g_sgemm_ex(int transA, int transB, int M, int N, int K, float alpha, const float* A, int lda,
+                 const float* B, int ldb, float beta, float* C, int ldc, void* stream);
+
+/*
+ * As b2g_sgemm_ex, but run plan `plan` (0 <= plan < b2g_plan_count()) instead of
+ * the tune table's choice.  Returns B2G_ERR_UNSUPPORTED when that plan cannot
+ * take these operands (alignment, op() flags).  For tests and tuning sweeps.
+ */
+int b2g_sgemm_with_plan(int plan, int transA, int transB, int M, int N, int K, float alpha,
+                        const float* A, int lda, const float* B, int ldb, float beta, float* C,
+                        int ldc, void* stream);
+
+/*
+ * The plan index the tune table picks for these arguments (nothing is
+ * launched), or a negative B2G_ERR_* code for invalid arguments.  Calls that
+ * need no GEMM kernel (K == 0 or alpha == 0: C = beta*C only; M == 0 or N == 0:
+ * nothing) return b2g_plan_count(), one past the last plan.
+ */
+int b2g_sgemm_select_plan(int transA, int transB, int M, int N, int K, float alpha, const float* A,
+                          int lda, const float* B, int ldb, const float* C, int ldc);
+
+/* Number of GEMM plans compiled into the library. */
+int b2g_plan_count(void);
+
+/* Name of plan `plan` ("tma_128x128x16_s6", ...), or NULL when out of range. */
+const char* b2g_plan_name(int plan);
+
+/*
+ * Plan parameters written to info[0..8]: BM, BN, BK, stages, TN (per-thread
+ * columns; rows are 8), A layout (0 = k-chunked, 1 = transposed), feed
+ * (0 = bulk-tensor, 1 = 4-byte cp.async), threads per CTA, dynamic shared bytes.
+ * Returns 0 or B2G_ERR_INVALID_PLAN / B2G_ERR_NULL.
+ */
+int b2g_plan_info(int plan, int* info);
+
+/*
+ * Read the device status word that kernels set when a bounded wait runs out.
+ * Synchronises `stream`, then stores the flags in *flags (0 = none; bit 0 a
+ * consumer timed out waiting for data, bit 1 a producer timed out waiting for
+ * a free stage, bit 2 a producer timed out waiting for its own copies, bit 3
+ * the tensor-core path timed out waiting for its MMAs).  clear != 0 resets the
+ * word.  Returns 0, B2G_ERR_TIMEOUT when a flag is set, or B2G_ERR_CUDA.
+ */
+int b2g_status(void* stream, unsigned int* flags, int clear);
+
+/*
+ * Upper bound, in nanoseconds of GPU wall time, on every mbarrier wait inside
+ * the kernels (default 2e9 = 2 s).  A wait that runs past it sets a status flag
+ * and its kernel returns early instead of hanging.  Returns 0, or
+ * B2G_ERR_INVALID_DIM for 0.
+ */
+int b2g_set_wait_limit_ns(unsigned long long ns);
+
+/*
+ * Failure-injection hook for tests of the bounded waits: with n >= 0 the
+ * producer of every subsequently launched GEMM kernel stops after issuing n
+ * stages, so the consumers' waits run out; n < 0 (the default) turns it off.
+ * Only meaningful on tiny problems with a short wait limit.  Returns 0.
+ */
+int b2g_debug_stop_after(int n);
+
+/* Static string for a B2G_* code. */
+const char* b2g_strerror(int code);
+
+/* Library version string. */
+const char* b2g_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* B2G_SGEMM_H */

@@ -139,7 +139,8 @@ def violations(got: np.ndarray, ref: np.ndarray, bound: np.ndarray) -> np.ndarra
     unless ``ref`` holds the same non-finite value.
     """
     got = np.asarray(got, dtype=np.float64)
-    err = np.abs(got - ref)
-    bad = ~(err <= bound)
-    same_nonfinite = ~np.isfinite(ref) & ((got == ref) | (np.isnan(got) & np.isnan(ref)))
+    with np.errstate(invalid="ignore"):
+        err = np.abs(got - ref)
+        bad = ~(err <= bound)
+        same_nonfinite = ~np.isfinite(ref) & ((got == ref) | (np.isnan(got) & np.isnan(ref)))
     return bad & ~same_nonfinite

@@ -1,0 +1,148 @@
+"""The C-ABI library loads, exports every symbol the header declares, and its
+host-side logic (argument checks, quick returns, plan choice) behaves as the
+header states.  None of these calls reaches a kernel, so they run without a GPU.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "b2g_sgemm.h")
+
+
+@pytest.fixture(scope="module")
+def b2g():
+    from dense_fp32_gemm_07_gb300 import build
+
+    build.build()
+    import dense_fp32_gemm_07_gb300 as pkg
+
+    pkg.library()
+    return pkg
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(b2g_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(b2g):
+    names = declared_functions()
+    assert len(names) >= 12
+    lib = ctypes.CDLL(b2g.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(b2g.EXPORTS) == names
+
+
+def test_error_codes_match_header(b2g):
+    text = open(HEADER).read()
+    for name, val in re.findall(r"#define (B2G_\w+) \(?(-?\d+)\)?", text):
+        assert getattr(b2g, name) == int(val), name
+        assert b2g.b2g_strerror(int(val)) != "unknown error code"
+
+
+def test_version_and_plans(b2g):
+    assert "sm_103a" in b2g.b2g_version()
+    names = b2g.plans()
+    assert len(names) == b2g.b2g_plan_count() >= 4 and len(set(names)) == len(names)
+    for i, n in enumerate(names):
+        info = b2g.b2g_plan_info(i)
+        assert info["BM"] > 0 and info["BN"] > 0 and info["BK"] % 4 == 0
+        assert info["threads"] % 32 == 0 and info["smem_bytes"] <= 227 * 1024
+        assert n.startswith(("tma", "gen"))
+    assert b2g.b2g_plan_name(len(names)) is None
+    with pytest.raises(b2g.B2GError):
+        b2g.b2g_plan_info(-1)
+
+
+FAKE = 0x100000  # a 16-byte aligned address; never dereferenced by these calls
+
+
+@pytest.mark.parametrize("args,code", [
+    ((-1, 4, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 4), -1),
+    ((4, -1, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 4), -1),
+    ((4, 4, -1, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 4), -1),
+    ((4, 4, 8, 1.0, FAKE, 7, FAKE, 4, 0.0, FAKE, 4), -2),   # lda < K
+    ((4, 4, 8, 1.0, FAKE, 8, FAKE, 3, 0.0, FAKE, 4), -2),   # ldb < N
+    ((4, 4, 8, 1.0, FAKE, 8, FAKE, 4, 0.0, FAKE, 3), -2),   # ldc < N
+    ((4, 4, 0, 1.0, FAKE, 0, FAKE, 4, 0.0, FAKE, 4), -2),   # lda >= max(1, K)
+    ((4, 4, 8, 1.0, FAKE, 8, FAKE, 4, 0.0, None, 4), -3),   # C null
+    ((4, 4, 8, 1.0, None, 8, FAKE, 4, 0.0, FAKE, 4), -3),   # A null and read
+    ((4, 4, 8, 1.0, FAKE, 8, None, 4, 0.0, FAKE, 4), -3),   # B null and read
+])
+def test_invalid_arguments(b2g, args, code):
+    assert b2g.b2g_sgemm(*args, 0) == code
+    assert b2g.b2g_sgemm_select_plan(0, 0, *args[:8], args[9], args[10]) == code
+
+
+def test_quick_returns_touch_nothing(b2g):
+    # M == 0 or N == 0: valid, nothing launched (so no device needed)
+    assert b2g.b2g_sgemm(0, 4, 4, 1.0, None, 4, None, 4, 0.0, None, 4, 0) == 0
+    assert b2g.b2g_sgemm(4, 0, 4, 1.0, None, 4, None, 1, 0.0, None, 1, 0) == 0
+    n = b2g.b2g_plan_count()
+    # alpha == 0 or K == 0: A and B not needed, beta-scale only
+    assert b2g.b2g_sgemm_select_plan(0, 0, 4, 4, 8, 0.0, None, 8, None, 4, FAKE, 4) == n
+    assert b2g.b2g_sgemm_select_plan(0, 0, 4, 4, 0, 1.0, None, 1, None, 4, FAKE, 4) == n
+
+
+def test_transposed_leading_dims(b2g):
+    # transA: A stored K x M -> lda >= M ; transB: B stored N x K -> ldb >= K
+    assert b2g.b2g_sgemm_select_plan(1, 0, 16, 8, 4, 1.0, FAKE, 15, FAKE, 8, FAKE, 8) == -2
+    assert b2g.b2g_sgemm_select_plan(1, 0, 16, 8, 4, 1.0, FAKE, 16, FAKE, 8, FAKE, 8) >= 0
+    assert b2g.b2g_sgemm_select_plan(0, 1, 16, 8, 4, 1.0, FAKE, 4, FAKE, 3, FAKE, 8) == -2
+    assert b2g.b2g_sgemm_select_plan(0, 1, 16, 8, 4, 1.0, FAKE, 4, FAKE, 4, FAKE, 8) >= 0
+
+
+def _plan(b2g, *a):
+    return b2g.b2g_plan_name(b2g.b2g_sgemm_select_plan(*a))
+
+
+def test_tune_table_classes(b2g):
+    # aligned, ld % 4 == 0, K % 4 == 0 -> bulk-tensor plans
+    assert _plan(b2g, 0, 0, 4096, 4096, 4096, 1.0, FAKE, 4096, FAKE, 4096, FAKE, 4096).startswith("tma_")
+    assert _plan(b2g, 0, 0, 16, 4096, 4096, 1.0, FAKE, 4096, FAKE, 4096, FAKE, 4096).startswith("tma_")
+    # odd leading dimension -> 4-byte feed
+    assert _plan(b2g, 0, 0, 1000, 1025, 777, 0.75, FAKE, 777, FAKE, 1025, FAKE, 1025).startswith("gen_")
+    # misaligned base pointer -> 4-byte feed
+    assert _plan(b2g, 0, 0, 512, 512, 512, 1.0, FAKE + 4, 512, FAKE, 512, FAKE, 512).startswith("gen_")
+    # K not a multiple of 4 -> 4-byte feed
+    assert _plan(b2g, 0, 0, 512, 512, 510, 1.0, FAKE, 512, FAKE, 512, FAKE, 512).startswith("gen_")
+    # op(A) = A^T aligned -> transposed-layout bulk-tensor plan; op(B) = B^T -> 4-byte feed
+    assert _plan(b2g, 1, 0, 512, 512, 512, 1.0, FAKE, 512, FAKE, 512, FAKE, 512).startswith("tmaT_")
+    assert _plan(b2g, 0, 1, 512, 512, 512, 1.0, FAKE, 512, FAKE, 512, FAKE, 512).startswith("gen_")
+
+
+def test_forced_plan_range(b2g):
+    n = b2g.b2g_plan_count()
+    args = (0, 0, 4, 4, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 4, 0)
+    assert b2g.b2g_sgemm_with_plan(n, *args) == -7
+    assert b2g.b2g_sgemm_with_plan(-1, *args) == -7
+
+
+def test_wait_limit_and_debug_hook(b2g):
+    assert b2g.b2g_set_wait_limit_ns(0) == -1
+    assert b2g.b2g_set_wait_limit_ns(2_000_000_000) == 0
+    assert b2g.b2g_debug_stop_after(-5) == 0
+
+
+def test_no_gpu_means_loud_failure(b2g):
+    """Without a usable sm_103 device a real call fails with a code; nothing
+    falls back to the CPU."""
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    rc = b2g.b2g_sgemm(4, 4, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 4, 0)
+    assert rc == b2g.B2G_ERR_DEVICE
+
+
+def test_tensor_api_rejects_cpu_tensors(b2g):
+    import torch
+
+    a = torch.zeros(4, 4)
+    with pytest.raises(TypeError):
+        b2g.sgemm(a, a, a)
