@@ -145,7 +145,7 @@ int operand_class(const Call& c) {
 bool plan_accepts(const Plan& pl, const Call& c) {
   if (pl.feed == kFeedCpAsync) return true;
   const int cls = operand_class(c);
-  if (pl.alayout == kAKChunk) return cls == kClassFast;
+  if (pl.feed == kFeedTMATrans || pl.alayout == kAKChunk) return cls == kClassFast;
   return cls == kClassFastTransA;
 }
 
@@ -235,8 +235,8 @@ int run(const Call& c, int forced_plan, void* stream) {
   CUtensorMap tmA, tmB;
   const CUtensorMap* pA = nullptr;
   const CUtensorMap* pB = nullptr;
-  if (pl->feed == kFeedTMA) {
-    if (pl->alayout == kAKChunk)
+  if (pl->feed != kFeedCpAsync) {
+    if (pl->feed != kFeedTMA || pl->alayout == kAKChunk)
       rc = encode_a_kchunk(&tmA, c.A, c.M, c.K, c.lda, pl->BM, pl->BK);
     else
       rc = encode_2d(&tmA, c.A, c.M, c.K, c.lda, pl->BM, pl->BK);  // A stored K x M

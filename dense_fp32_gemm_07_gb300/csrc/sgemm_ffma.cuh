@@ -39,7 +39,7 @@
 namespace b2g {
 
 template <int BM, int BN, int BK, int WM, int WN, int TN, int STAGES, int ALAY, int FEED,
-          int PWARPS>
+          int PWARPS, int ORD = 0>
 struct FfmaCfg {
   static constexpr int TM = 8;
   static constexpr int kConsumerWarps = WM * WN;
@@ -48,17 +48,58 @@ struct FfmaCfg {
   static constexpr int kThreads = kConsumers + kProducers;
   static constexpr int kAStage = BM * BK;  // floats per stage
   static constexpr int kBStage = BK * BN;
-  static constexpr int kStageBytes = (kAStage + kBStage) * 4;
-  static constexpr int kSmemBytes = STAGES * kStageBytes + 2 * STAGES * 8;
+  static constexpr bool kStaged = FEED == kFeedTMATrans;
+  static constexpr int kStaging = kStaged ? BM * BK : 0;  // k-chunked A copy
+  static constexpr int kStageBytes = (kAStage + kBStage) * 4;  // bytes one stage's copies land
+  static constexpr int kBarriers = kStaged ? 3 : 2;
+  static constexpr int kSmemBytes =
+      STAGES * (kAStage + kBStage + kStaging) * 4 + kBarriers * STAGES * 8;
   static_assert(BM == WM * 32, "a warp tile is 32 rows");
   static_assert(BN == WN * 8 * TN, "a warp tile is 8*TN columns");
   static_assert(TN % 4 == 0 && BK % 4 == 0, "16-byte fragments");
   static_assert(BM <= 256 && BN <= 256, "bulk-tensor box dimensions are at most 256");
-  static_assert(FEED == kFeedTMA ? PWARPS == 1 : PWARPS >= 1, "producer warps");
+  static_assert(FEED == kFeedCpAsync ? PWARPS >= 1 : PWARPS == 1, "producer warps");
   static_assert(FEED == kFeedTMA || ALAY == kAKMajor, "4-byte feed writes the transposed layout");
+  static_assert(FEED != kFeedTMATrans || (BM * BK / 4) % (kConsumers) == 0,
+                "the rewrite of one A stage splits evenly over the consumer threads");
+  // The consumer warps rewrite stage t + kAhead while they compute stage t.  A
+  // warp can run at most kAhead stages ahead of the slowest one (it needs every
+  // warp's share of its stage), so the slot it rewrites is free when
+  // STAGES > 2 * kAhead.
+  static constexpr int kAhead = (STAGES - 1) / 2;
+  static_assert(FEED != kFeedTMATrans || kAhead >= 1, "transposing feed needs >= 3 stages");
   static_assert(FEED == kFeedTMA || (BM * BK) % kProducers == 0, "A tile split evenly");
   static_assert(FEED == kFeedTMA || (BK * BN) % kProducers == 0, "B tile split evenly");
 };
+
+// One k step of the register outer product, acc[i][j] += a[i] * b[j], as FP32
+// FFMAs.  ORD picks the issue order (0: row by row, 1: column by column,
+// 2: rows with alternating column direction); every order performs the same
+// FFMAs on the same accumulators, so results are identical, but the order
+// changes which operand consecutive FFMAs share.
+template <int ORD, int TN>
+__device__ __forceinline__ void outer_product(float (&acc)[8][TN], const float (&a)[8],
+                                              const float (&b)[TN]) {
+  if constexpr (ORD == 1) {
+#pragma unroll
+    for (int j = 0; j < TN; ++j)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+  } else if constexpr (ORD == 2) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int jj = 0; jj < TN; ++jj) {
+        const int j = (i & 1) ? TN - 1 - jj : jj;
+        acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+      }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+  }
+}
 
 // Output tile of linear index `tile`: tiles run down a group of `group_m` tile
 // rows before moving one tile column right, so CTAs that run together share A
@@ -74,25 +115,30 @@ __device__ __forceinline__ void tile_coords(const SgemmParams& p, int tile, int&
 }
 
 template <int BM, int BN, int BK, int WM, int WN, int TN, int STAGES, int ALAY, int FEED,
-          int PWARPS>
+          int PWARPS, int ORD>
 __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
     sgemm_ffma_kernel(const __grid_constant__ SgemmParams p,
                       const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB) {
-  using Cfg = FfmaCfg<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS>;
+  using Cfg = FfmaCfg<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS, ORD>;
   extern __shared__ __align__(1024) unsigned char smem[];
   float* sA = reinterpret_cast<float*>(smem);
   float* sB = sA + STAGES * Cfg::kAStage;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * Cfg::kBStage);
+  float* sAst = sB + STAGES * Cfg::kBStage;  // staging (transposing feed only)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sAst + STAGES * Cfg::kStaging);
   const uint32_t full0 = smem_addr(bars);
   const uint32_t empty0 = smem_addr(bars + STAGES);
+  const uint32_t tfull0 = smem_addr(bars + 2 * STAGES);  // transposing feed: copies landed
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full0 + 8 * s, FEED == kFeedTMA ? 1 : Cfg::kProducers);
+      mbar_init(full0 + 8 * s, FEED == kFeedTMA         ? 1
+                               : FEED == kFeedTMATrans ? Cfg::kConsumers
+                                                       : Cfg::kProducers);
       mbar_init(empty0 + 8 * s, Cfg::kConsumerWarps);
+      if constexpr (Cfg::kStaged) mbar_init(tfull0 + 8 * s, 1);
     }
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -102,11 +148,12 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
   const int total_tiles = p.tiles_m * p.tiles_n;
 
   // ------------------------------------------------------------------ producer
-  if (warp >= Cfg::kConsumerWarps) {
+  // Producer warps come first (warps 0 .. PWARPS-1), consumers after them.
+  if (warp < PWARPS) {
     int stage = 0;
     uint32_t phase = 0;
     int issued = 0;
-    if constexpr (FEED == kFeedTMA) {
+    if constexpr (FEED == kFeedTMA || FEED == kFeedTMATrans) {
       if (lane != 0) return;
       prefetch_tmap(&tmA);
       prefetch_tmap(&tmB);
@@ -119,11 +166,13 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, p.wait_limit_ns, p.status,
                          kStatusTimeoutEmpty))
             goto drain_tma;
-          const uint32_t fb = full0 + 8 * stage;
+          // the transposing feed lands A in the staging slot and signals `tfull`
+          const uint32_t fb = (FEED == kFeedTMATrans ? tfull0 : full0) + 8 * stage;
           mbar_arrive_expect_tx(fb, Cfg::kStageBytes);
-          const uint32_t dA = smem_addr(sA + stage * Cfg::kAStage);
+          const uint32_t dA = smem_addr(FEED == kFeedTMATrans ? sAst + stage * Cfg::kStaging
+                                                              : sA + stage * Cfg::kAStage);
           const uint32_t dB = smem_addr(sB + stage * Cfg::kBStage);
-          if constexpr (ALAY == kAKChunk)
+          if constexpr (ALAY == kAKChunk || FEED == kFeedTMATrans)
             tma_load_3d(dA, &tmA, 0, m0, kt * (BK / 4), fb);  // view {4, M, K/4}
           else
             tma_load_2d(dA, &tmA, m0, kt * BK, fb);  // A stored K x M
@@ -136,11 +185,12 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
       // Leave only after every copy this thread started has landed.
       for (int d = 0, pending = min(issued, STAGES); d < pending; ++d) {
         if (--stage < 0) stage = STAGES - 1, phase ^= 1u;
-        if (!mbar_wait(full0 + 8 * stage, phase, p.wait_limit_ns, p.status, kStatusTimeoutDrain))
+        if (!mbar_wait((FEED == kFeedTMATrans ? tfull0 : full0) + 8 * stage, phase,
+                       p.wait_limit_ns, p.status, kStatusTimeoutDrain))
           break;
       }
     } else {
-      const int pt = threadIdx.x - Cfg::kConsumers;
+      const int pt = threadIdx.x;
       for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
         int tm, tn;
         tile_coords(p, tile, tm, tn);
@@ -190,7 +240,8 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
   }
 
   // ------------------------------------------------------------------ consumers
-  const int wm = warp % WM, wn = warp / WM;
+  const int cw = warp - PWARPS;  // consumer warp index
+  const int wm = cw % WM, wn = cw / WM;
   const int tr = lane >> 3, tc = lane & 7;
   // Thread rows: k-chunked A gives rows wm*32 + tr + 4i (the 4 thread rows of a
   // warp read 4 consecutive 16-byte vectors); transposed A gives rows
@@ -200,6 +251,56 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
   const int b_off = wn * (8 * TN) + 4 * tc;
   int stage = 0;
   uint32_t phase = 0;
+
+  // Transposing feed: the consumer warps rewrite stage u = t + kAhead from the
+  // k-chunked staging copy [BK/4][BM][4] to [BK][BM] while they compute stage
+  // t; each warp takes an equal share.  Every 16-byte read and every 4-byte
+  // write covers 32 consecutive m, so neither side has bank conflicts.  The
+  // reads are issued before the stage's FFMAs and the writes after them, so
+  // their latency hides under the arithmetic.
+  constexpr int kXPer = Cfg::kStaged ? (BM * BK / 4) / Cfg::kConsumers : 1;
+  long long xt = 0;  // next stage to rewrite
+  long long total_stages = 0;
+  if constexpr (Cfg::kStaged) {
+    const int my_tiles =
+        blockIdx.x < total_tiles ? (total_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    total_stages = (long long)my_tiles * p.k_tiles;
+  }
+  float4 xv[kXPer];
+  auto x_load = [&](long long u) -> bool {  // wait for stage u's copies, read my share
+    const int slot = (int)(u % STAGES);
+    const uint32_t ph = (uint32_t)((u / STAGES) & 1);
+    if (!mbar_wait(tfull0 + 8 * slot, ph, p.wait_limit_ns, p.status, kStatusTimeoutFull))
+      return false;
+    const float* st = sAst + slot * Cfg::kStaging;
+#pragma unroll
+    for (int it = 0; it < kXPer; ++it) {
+      const int idx = (it * Cfg::kConsumerWarps + cw) * 32 + lane;
+      const int q = idx / BM, m = idx % BM;
+      xv[it] = *reinterpret_cast<const float4*>(st + (q * BM + m) * 4);
+    }
+    return true;
+  };
+  auto x_store = [&](long long u) {  // write my share transposed, then count it in
+    const int slot = (int)(u % STAGES);
+    float* dst = sA + slot * Cfg::kAStage;
+#pragma unroll
+    for (int it = 0; it < kXPer; ++it) {
+      const int idx = (it * Cfg::kConsumerWarps + cw) * 32 + lane;
+      const int q = idx / BM, m = idx % BM;
+      dst[(4 * q + 0) * BM + m] = xv[it].x;
+      dst[(4 * q + 1) * BM + m] = xv[it].y;
+      dst[(4 * q + 2) * BM + m] = xv[it].z;
+      dst[(4 * q + 3) * BM + m] = xv[it].w;
+    }
+    mbar_arrive(full0 + 8 * slot);
+  };
+  if constexpr (Cfg::kStaged) {
+    for (; xt < total_stages && xt < Cfg::kAhead; ++xt) {
+      if (!x_load(xt)) return;
+      x_store(xt);
+    }
+  }
 
   for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
     int tm, tn;
@@ -211,6 +312,13 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
       for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
 
     for (int kt = 0; kt < p.k_tiles; ++kt) {
+      bool x_now = false;
+      if constexpr (Cfg::kStaged) {
+        if (xt < total_stages) {
+          if (!x_load(xt)) return;
+          x_now = true;
+        }
+      }
       if (!mbar_wait(full0 + 8 * stage, phase, p.wait_limit_ns, p.status, kStatusTimeoutFull))
         return;  // the status word says why; the producer drains and leaves too
       const float* As = sA + stage * Cfg::kAStage + a_off;
@@ -231,12 +339,11 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
                   *reinterpret_cast<const float4*>(Bs + (4 * q + kk) * BN + 32 * j4);
               b[4 * j4 + 0] = v.x, b[4 * j4 + 1] = v.y, b[4 * j4 + 2] = v.z, b[4 * j4 + 3] = v.w;
             }
+            float a[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float a = kk == 0 ? a4[i].x : kk == 1 ? a4[i].y : kk == 2 ? a4[i].z : a4[i].w;
-#pragma unroll
-              for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a, b[j], acc[i][j]);
-            }
+            for (int i = 0; i < 8; ++i)
+              a[i] = kk == 0 ? a4[i].x : kk == 1 ? a4[i].y : kk == 2 ? a4[i].z : a4[i].w;
+            outer_product<ORD, TN>(acc, a, b);
           }
         }
       } else {
@@ -251,10 +358,13 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
             const float4 v = *reinterpret_cast<const float4*>(Bs + k * BN + 32 * j4);
             b[4 * j4 + 0] = v.x, b[4 * j4 + 1] = v.y, b[4 * j4 + 2] = v.z, b[4 * j4 + 3] = v.w;
           }
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-#pragma unroll
-            for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+          outer_product<ORD, TN>(acc, a, b);
+        }
+      }
+      if constexpr (Cfg::kStaged) {
+        if (x_now) {
+          x_store(xt);
+          ++xt;
         }
       }
       __syncwarp();
@@ -303,11 +413,11 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
 }
 
 template <int BM, int BN, int BK, int WM, int WN, int TN, int STAGES, int ALAY, int FEED,
-          int PWARPS>
+          int PWARPS, int ORD>
 cudaError_t launch_ffma(const SgemmParams& p, const CUtensorMap* tmA, const CUtensorMap* tmB,
                         int num_sms, cudaStream_t stream) {
-  using Cfg = FfmaCfg<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS>;
-  auto kern = sgemm_ffma_kernel<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS>;
+  using Cfg = FfmaCfg<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS, ORD>;
+  auto kern = sgemm_ffma_kernel<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS, ORD>;
   // Per device, once: opt in to the dynamic shared memory size and record how
   // many CTAs fit on one SM (the persistent grid is SMs x that).
   static std::atomic<int> resident[kMaxDevices];
@@ -335,12 +445,12 @@ cudaError_t launch_ffma(const SgemmParams& p, const CUtensorMap* tmA, const CUte
                           args, Cfg::kSmemBytes, stream);
 }
 
-#define B2G_FFMA_PLAN(NAME, BM, BN, BK, WM, WN, TN, ST, ALAY, FEED, PW)                           \
+#define B2G_FFMA_PLAN(NAME, BM, BN, BK, WM, WN, TN, ST, ALAY, FEED, PW, ORD)                      \
   Plan {                                                                                         \
     NAME, BM, BN, BK, ST, TN, ALAY, FEED,                                                        \
-        FfmaCfg<BM, BN, BK, WM, WN, TN, ST, ALAY, FEED, PW>::kThreads,                           \
-        FfmaCfg<BM, BN, BK, WM, WN, TN, ST, ALAY, FEED, PW>::kSmemBytes,                         \
-        &launch_ffma<BM, BN, BK, WM, WN, TN, ST, ALAY, FEED, PW>                                 \
+        FfmaCfg<BM, BN, BK, WM, WN, TN, ST, ALAY, FEED, PW, ORD>::kThreads,                      \
+        FfmaCfg<BM, BN, BK, WM, WN, TN, ST, ALAY, FEED, PW, ORD>::kSmemBytes,                    \
+        &launch_ffma<BM, BN, BK, WM, WN, TN, ST, ALAY, FEED, PW, ORD>                            \
   }
 
 }  // namespace b2g

@@ -35,6 +35,8 @@ enum ALayout : int {
 enum Feed : int {
   kFeedTMA = 0,      // one elected thread issues bulk-tensor copies (aligned operands)
   kFeedCpAsync = 1,  // producer warps issue 4-byte cp.async with zero fill (any layout)
+  kFeedTMATrans = 2,  // bulk-tensor copies; A lands k-chunked in a staging slot and the
+                      // consumer warps rewrite it transposed ([BK][BM]) a few stages ahead
 };
 
 constexpr int kMaxDevices = 64;
