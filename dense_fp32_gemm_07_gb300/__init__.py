@@ -34,6 +34,7 @@ B2G_ERR_TIMEOUT = -10
 # every symbol include/b2g_sgemm.h declares
 EXPORTS = (
     "b2g_sgemm", "b2g_sgemm_ex", "b2g_sgemm_with_plan", "b2g_sgemm_select_plan",
+    "b2g_sgemm_ws", "b2g_sgemm_workspace_size", "b2g_release_workspaces",
     "b2g_plan_count", "b2g_plan_name", "b2g_plan_info", "b2g_status", "b2g_set_wait_limit_ns",
     "b2g_debug_stop_after", "b2g_strerror", "b2g_version",
 )
@@ -64,6 +65,11 @@ def _load():
         lib.b2g_sgemm_ex.argtypes = [i, i] + gemm
         lib.b2g_sgemm_with_plan.argtypes = [i, i, i] + gemm
         lib.b2g_sgemm_select_plan.argtypes = [i, i, i, i, i, f, vp, i, vp, i, vp, i]
+        lib.b2g_sgemm_ws.argtypes = [i, i, i, i, i, f, vp, i, vp, i, f, vp, i, vp, ctypes.c_size_t,
+                                     vp]
+        lib.b2g_sgemm_workspace_size.argtypes = [i, i, i, i, i, f, vp, i, vp, i, vp, i,
+                                                 ctypes.POINTER(ctypes.c_size_t)]
+        lib.b2g_release_workspaces.argtypes = []
         lib.b2g_plan_count.argtypes = []
         lib.b2g_plan_name.argtypes = [i]
         lib.b2g_plan_name.restype = ctypes.c_char_p
@@ -106,6 +112,24 @@ def b2g_sgemm_with_plan(plan, transA, transB, M, N, K, alpha, A, lda, B, ldb, be
 
 def b2g_sgemm_select_plan(transA, transB, M, N, K, alpha, A, lda, B, ldb, C, ldc) -> int:
     return _load().b2g_sgemm_select_plan(transA, transB, M, N, K, alpha, A, lda, B, ldb, C, ldc)
+
+
+def b2g_sgemm_ws(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, workspace,
+                 workspace_bytes, stream=0) -> int:
+    return _load().b2g_sgemm_ws(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                                workspace, workspace_bytes, stream)
+
+
+def b2g_sgemm_workspace_size(transA, transB, M, N, K, alpha, A, lda, B, ldb, C, ldc):
+    """(rc, bytes) for the tune table's plan."""
+    n = ctypes.c_size_t(0)
+    rc = _load().b2g_sgemm_workspace_size(transA, transB, M, N, K, alpha, A, lda, B, ldb, C, ldc,
+                                          ctypes.byref(n))
+    return rc, n.value
+
+
+def b2g_release_workspaces() -> int:
+    return _load().b2g_release_workspaces()
 
 
 def b2g_plan_count() -> int:

@@ -15,6 +15,7 @@
 
 #include "../../include/b2g_sgemm.h"
 #include "sgemm_params.h"
+#include "transpose.h"
 #include "tune_table.h"
 
 namespace b2g {
@@ -90,6 +91,62 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return g_encode;
 }
 
+// Library-owned workspace, one per device, for calls that do not bring their
+// own.  Its users on different streams are ordered through an event recorded
+// after each use, so a stream never overwrites a buffer another stream may
+// still read.  It is allocated (stream-ordered) on first need and grown when a
+// larger call comes; it is never used while the stream is being captured.
+struct AutoWorkspace {
+  std::mutex mu;
+  void* ptr = nullptr;
+  size_t bytes = 0;
+  cudaEvent_t done = nullptr;
+  bool used = false;
+};
+AutoWorkspace g_ws[kMaxDevices];
+
+// Lock the device's workspace and make it at least `bytes` long, ordered on
+// `st`; returns nullptr (lock released) when it cannot be had.  On success the
+// caller enqueues its work and then calls ws_release().
+void* ws_acquire(int dev, cudaStream_t st, size_t bytes) {
+  AutoWorkspace& w = g_ws[dev];
+  w.mu.lock();
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+    w.mu.unlock();
+    return nullptr;
+  }
+  if (!w.done && cudaEventCreateWithFlags(&w.done, cudaEventDisableTiming) != cudaSuccess) {
+    w.done = nullptr;
+    w.mu.unlock();
+    return nullptr;
+  }
+  if (w.used && cudaStreamWaitEvent(st, w.done, 0) != cudaSuccess) {
+    w.mu.unlock();
+    return nullptr;
+  }
+  if (bytes > w.bytes) {
+    const size_t grain = size_t(2) << 20;
+    const size_t want = (bytes + grain - 1) / grain * grain;
+    void* np = nullptr;
+    if (cudaMallocAsync(&np, want, st) != cudaSuccess) {
+      cudaGetLastError();
+      w.mu.unlock();
+      return nullptr;
+    }
+    if (w.ptr) cudaFreeAsync(w.ptr, st);
+    w.ptr = np;
+    w.bytes = want;
+  }
+  return w.ptr;
+}
+
+void ws_release(int dev, cudaStream_t st) {
+  AutoWorkspace& w = g_ws[dev];
+  if (cudaEventRecord(w.done, st) == cudaSuccess) w.used = true;
+  w.mu.unlock();
+}
+
 int num_plans() { return kNumPlansTMA + kNumPlansGeneral; }
 
 const Plan* plan_at(int i) {
@@ -145,20 +202,37 @@ int operand_class(const Call& c) {
 bool plan_accepts(const Plan& pl, const Call& c) {
   if (pl.feed == kFeedCpAsync) return true;
   const int cls = operand_class(c);
+  if (pl.pretranspose) return cls == kClassFast;
   if (pl.feed == kFeedTMATrans || pl.alayout == kAKChunk) return cls == kClassFast;
   return cls == kClassFastTransA;
 }
 
-int select_plan(const Call& c) {
+// The tune table's plan; `fallback` receives the plan to use when the chosen
+// one needs a workspace that cannot be had (the same plan when it needs none).
+int select_plan(const Call& c, int* fallback = nullptr) {
   const int cls = operand_class(c);
+  const double mnk = (double)c.M * c.N * c.K;
   for (const TuneRule& r : kTuneTable) {
-    if (r.cls == cls && c.M >= r.m_min && c.M <= r.m_max && c.N >= r.n_min && c.N <= r.n_max) {
+    if (r.cls == cls && c.M >= r.m_min && c.M <= r.m_max && c.N >= r.n_min && c.N <= r.n_max &&
+        mnk >= r.mnk_min) {
       const int i = plan_index(r.plan);
-      if (i >= 0) return i;
+      if (i >= 0) {
+        if (fallback) {
+          const int f = r.fallback ? plan_index(r.fallback) : i;
+          *fallback = f >= 0 ? f : i;
+        }
+        return i;
+      }
     }
   }
-  return plan_index("gen_128x128x16_s4");
+  const int g = plan_index("gen_128x128x16_s4");
+  if (fallback) *fallback = g;
+  return g;
 }
+
+long long pre_ld(int M) { return ((long long)M + 3) / 4 * 4; }
+
+size_t pre_bytes(const Call& c) { return (size_t)c.K * (size_t)pre_ld(c.M) * sizeof(float); }
 
 int encode_2d(CUtensorMap* m, const float* base, long long inner, long long outer,
               long long row_stride_elems, int box_inner, int box_outer) {
@@ -202,7 +276,13 @@ int launch_scale(const Call& c, const DeviceState& d, cudaStream_t st) {
   return e == cudaSuccess ? 0 : B2G_ERR_LAUNCH;
 }
 
-int run(const Call& c, int forced_plan, void* stream) {
+// Launch one GEMM.  `user_ws` (may be null) is a caller-provided workspace of
+// `user_ws_bytes`; without one, plans that need a workspace take the device's
+// library-owned one, and fall back to a plan that needs none when it cannot be
+// had.  A forced plan that needs a workspace fails with B2G_ERR_UNSUPPORTED
+// when none can be had.
+int run(const Call& c, int forced_plan, void* stream, void* user_ws = nullptr,
+        size_t user_ws_bytes = 0, bool allow_auto_ws = true) {
   int rc = validate(c);
   if (rc) return rc;
   if (c.M == 0 || c.N == 0) return 0;
@@ -213,10 +293,31 @@ int run(const Call& c, int forced_plan, void* stream) {
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (!needs_gemm(c)) return launch_scale(c, *d, st);
 
-  const int pi = forced_plan >= 0 ? forced_plan : select_plan(c);
+  int fallback = -1;
+  int pi = forced_plan >= 0 ? forced_plan : select_plan(c, &fallback);
   const Plan* pl = plan_at(pi);
   if (!pl) return B2G_ERR_INVALID_PLAN;
   if (!plan_accepts(*pl, c)) return B2G_ERR_UNSUPPORTED;
+
+  int dev = 0;
+  cudaGetDevice(&dev);
+  float* ws = nullptr;
+  bool auto_ws = false;
+  if (pl->pretranspose) {
+    const size_t need = pre_bytes(c);
+    if (user_ws && user_ws_bytes >= need && aligned16(user_ws)) {
+      ws = static_cast<float*>(user_ws);
+    } else if (allow_auto_ws) {
+      ws = static_cast<float*>(ws_acquire(dev, st, need));
+      auto_ws = ws != nullptr;
+    }
+    if (!ws) {
+      if (forced_plan >= 0 || fallback < 0) return B2G_ERR_UNSUPPORTED;
+      pi = fallback;
+      pl = plan_at(pi);
+      if (!pl || !plan_accepts(*pl, c) || pl->pretranspose) return B2G_ERR_UNSUPPORTED;
+    }
+  }
 
   SgemmParams p;
   p.M = c.M, p.N = c.N, p.K = c.K;
@@ -232,19 +333,27 @@ int run(const Call& c, int forced_plan, void* stream) {
   p.debug_stop_ktile = g_debug_stop.load();
   p.status = d->status;
 
+  cudaError_t e = cudaSuccess;
+  if (ws) {  // At = A^T, then the kernel reads A stored K x M
+    const long long ldat = pre_ld(c.M);
+    e = launch_transpose_a(c.A, c.M, c.K, c.lda, ws, ldat, st);
+    p.A = ws, p.lda = ldat, p.transA = 1;
+  }
+
   CUtensorMap tmA, tmB;
   const CUtensorMap* pA = nullptr;
   const CUtensorMap* pB = nullptr;
-  if (pl->feed != kFeedCpAsync) {
+  if (e == cudaSuccess && pl->feed != kFeedCpAsync) {
     if (pl->feed != kFeedTMA || pl->alayout == kAKChunk)
-      rc = encode_a_kchunk(&tmA, c.A, c.M, c.K, c.lda, pl->BM, pl->BK);
+      rc = encode_a_kchunk(&tmA, p.A, c.M, c.K, (int)p.lda, pl->BM, pl->BK);
     else
-      rc = encode_2d(&tmA, c.A, c.M, c.K, c.lda, pl->BM, pl->BK);  // A stored K x M
+      rc = encode_2d(&tmA, p.A, c.M, c.K, p.lda, pl->BM, pl->BK);  // A stored K x M
     if (!rc) rc = encode_2d(&tmB, c.B, c.N, c.K, c.ldb, pl->BN, pl->BK);
-    if (rc) return rc;
     pA = &tmA, pB = &tmB;
   }
-  cudaError_t e = pl->launch(p, pA, pB, d->sms, st);
+  if (e == cudaSuccess && !rc) e = pl->launch(p, pA, pB, d->sms, st);
+  if (auto_ws) ws_release(dev, st);
+  if (rc) return rc;
   return e == cudaSuccess ? 0 : B2G_ERR_LAUNCH;
 }
 
@@ -272,6 +381,49 @@ int b2g_sgemm_with_plan(int plan, int transA, int transB, int M, int N, int K, f
   if (plan < 0 || plan >= num_plans()) return B2G_ERR_INVALID_PLAN;
   return run(Call{transA != 0, transB != 0, M, N, K, alpha, beta, A, lda, B, ldb, C, ldc}, plan,
              stream);
+}
+
+int b2g_sgemm_ws(int transA, int transB, int M, int N, int K, float alpha, const float* A, int lda,
+                 const float* B, int ldb, float beta, float* C, int ldc, void* workspace,
+                 size_t workspace_bytes, void* stream) {
+  return run(Call{transA != 0, transB != 0, M, N, K, alpha, beta, A, lda, B, ldb, C, ldc}, -1,
+             stream, workspace, workspace_bytes, false);
+}
+
+int b2g_sgemm_workspace_size(int transA, int transB, int M, int N, int K, float alpha,
+                             const float* A, int lda, const float* B, int ldb, const float* C,
+                             int ldc, size_t* bytes) {
+  if (!bytes) return B2G_ERR_NULL;
+  Call c{transA != 0, transB != 0, M, N, K, alpha, 0.f, A, lda, B, ldb, const_cast<float*>(C), ldc};
+  const int rc = validate(c);
+  if (rc) return rc;
+  *bytes = 0;
+  if (needs_gemm(c)) {
+    const Plan* pl = plan_at(select_plan(c));
+    if (pl && pl->pretranspose) *bytes = pre_bytes(c);
+  }
+  return 0;
+}
+
+int b2g_release_workspaces(void) {
+  int rc = 0;
+  for (int dev = 0; dev < kMaxDevices; ++dev) {
+    AutoWorkspace& w = g_ws[dev];
+    std::lock_guard<std::mutex> lk(w.mu);
+    if (!w.ptr) continue;
+    int cur = 0;
+    cudaGetDevice(&cur);
+    if (cudaSetDevice(dev) != cudaSuccess) {
+      rc = B2G_ERR_CUDA;
+      continue;
+    }
+    if (w.done) cudaEventSynchronize(w.done);
+    if (cudaFree(w.ptr) != cudaSuccess) rc = B2G_ERR_CUDA;
+    w.ptr = nullptr;
+    w.bytes = 0;
+    cudaSetDevice(cur);
+  }
+  return rc;
 }
 
 int b2g_sgemm_select_plan(int transA, int transB, int M, int N, int K, float alpha, const float* A,

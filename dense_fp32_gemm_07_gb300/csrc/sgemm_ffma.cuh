@@ -46,30 +46,23 @@ struct FfmaCfg {
   static constexpr int kConsumers = kConsumerWarps * 32;
   static constexpr int kProducers = PWARPS * 32;
   static constexpr int kThreads = kConsumers + kProducers;
-  static constexpr int kAStage = BM * BK;  // floats per stage
-  static constexpr int kBStage = BK * BN;
+  // Staged feed: A lands k-chunked in a staging slot and each consumer warp
+  // rewrites the 32 rows it owns, transposed, into a private double buffer.
   static constexpr bool kStaged = FEED == kFeedTMATrans;
-  static constexpr int kStaging = kStaged ? BM * BK : 0;  // k-chunked A copy
-  static constexpr int kStageBytes = (kAStage + kBStage) * 4;  // bytes one stage's copies land
-  static constexpr int kBarriers = kStaged ? 3 : 2;
+  static constexpr int kAStage = kStaged ? 0 : BM * BK;  // floats per stage, shared A
+  static constexpr int kBStage = BK * BN;
+  static constexpr int kStaging = kStaged ? BM * BK : 0;                 // k-chunked A copy
+  static constexpr int kPrivate = kStaged ? kConsumerWarps * 2 * BK * 32 : 0;  // per-warp A
+  static constexpr int kARow = kStaged ? 32 : BM;  // row stride of the transposed A a warp reads
+  static constexpr int kStageBytes = (BM * BK + kBStage) * 4;  // bytes one stage's copies land
   static constexpr int kSmemBytes =
-      STAGES * (kAStage + kBStage + kStaging) * 4 + kBarriers * STAGES * 8;
+      (STAGES * (kAStage + kBStage + kStaging) + kPrivate) * 4 + 2 * STAGES * 8;
   static_assert(BM == WM * 32, "a warp tile is 32 rows");
   static_assert(BN == WN * 8 * TN, "a warp tile is 8*TN columns");
   static_assert(TN % 4 == 0 && BK % 4 == 0, "16-byte fragments");
   static_assert(BM <= 256 && BN <= 256, "bulk-tensor box dimensions are at most 256");
   static_assert(FEED == kFeedCpAsync ? PWARPS >= 1 : PWARPS == 1, "producer warps");
   static_assert(FEED == kFeedTMA || ALAY == kAKMajor, "4-byte feed writes the transposed layout");
-  static_assert(FEED != kFeedTMATrans || (BM * BK / 4) % (kConsumers) == 0,
-                "the rewrite of one A stage splits evenly over the consumer threads");
-  // The consumer warps rewrite stage t + kAhead while they compute stage t.  A
-  // warp can run at most kAhead stages ahead of the slowest one (it needs every
-  // warp's share of its stage), so the slot it rewrites is free when
-  // STAGES > 2 * kAhead.
-  static constexpr int kAhead = (STAGES - 1) / 2;
-  static_assert(FEED != kFeedTMATrans || kAhead >= 1, "transposing feed needs >= 3 stages");
-  static_assert(FEED == kFeedTMA || (BM * BK) % kProducers == 0, "A tile split evenly");
-  static_assert(FEED == kFeedTMA || (BK * BN) % kProducers == 0, "B tile split evenly");
 };
 
 // One k step of the register outer product, acc[i][j] += a[i] * b[j], as FP32
@@ -124,21 +117,18 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
   extern __shared__ __align__(1024) unsigned char smem[];
   float* sA = reinterpret_cast<float*>(smem);
   float* sB = sA + STAGES * Cfg::kAStage;
-  float* sAst = sB + STAGES * Cfg::kBStage;  // staging (transposing feed only)
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sAst + STAGES * Cfg::kStaging);
+  float* sAst = sB + STAGES * Cfg::kBStage;     // staging (staged feed only)
+  float* sAp = sAst + STAGES * Cfg::kStaging;   // per-warp A buffers (staged feed only)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sAp + Cfg::kPrivate);
   const uint32_t full0 = smem_addr(bars);
   const uint32_t empty0 = smem_addr(bars + STAGES);
-  const uint32_t tfull0 = smem_addr(bars + 2 * STAGES);  // transposing feed: copies landed
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full0 + 8 * s, FEED == kFeedTMA         ? 1
-                               : FEED == kFeedTMATrans ? Cfg::kConsumers
-                                                       : Cfg::kProducers);
+      mbar_init(full0 + 8 * s, FEED == kFeedCpAsync ? Cfg::kProducers : 1);
       mbar_init(empty0 + 8 * s, Cfg::kConsumerWarps);
-      if constexpr (Cfg::kStaged) mbar_init(tfull0 + 8 * s, 1);
     }
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -166,8 +156,8 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, p.wait_limit_ns, p.status,
                          kStatusTimeoutEmpty))
             goto drain_tma;
-          // the transposing feed lands A in the staging slot and signals `tfull`
-          const uint32_t fb = (FEED == kFeedTMATrans ? tfull0 : full0) + 8 * stage;
+          // the staged feed lands A in the staging slot
+          const uint32_t fb = full0 + 8 * stage;
           mbar_arrive_expect_tx(fb, Cfg::kStageBytes);
           const uint32_t dA = smem_addr(FEED == kFeedTMATrans ? sAst + stage * Cfg::kStaging
                                                               : sA + stage * Cfg::kAStage);
@@ -185,8 +175,7 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
       // Leave only after every copy this thread started has landed.
       for (int d = 0, pending = min(issued, STAGES); d < pending; ++d) {
         if (--stage < 0) stage = STAGES - 1, phase ^= 1u;
-        if (!mbar_wait((FEED == kFeedTMATrans ? tfull0 : full0) + 8 * stage, phase,
-                       p.wait_limit_ns, p.status, kStatusTimeoutDrain))
+        if (!mbar_wait(full0 + 8 * stage, phase, p.wait_limit_ns, p.status, kStatusTimeoutDrain))
           break;
       }
     } else {
@@ -252,53 +241,39 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
   int stage = 0;
   uint32_t phase = 0;
 
-  // Transposing feed: the consumer warps rewrite stage u = t + kAhead from the
-  // k-chunked staging copy [BK/4][BM][4] to [BK][BM] while they compute stage
-  // t; each warp takes an equal share.  Every 16-byte read and every 4-byte
-  // write covers 32 consecutive m, so neither side has bank conflicts.  The
-  // reads are issued before the stage's FFMAs and the writes after them, so
-  // their latency hides under the arithmetic.
-  constexpr int kXPer = Cfg::kStaged ? (BM * BK / 4) / Cfg::kConsumers : 1;
-  long long xt = 0;  // next stage to rewrite
-  long long total_stages = 0;
+  // Staged feed: before computing stage t each warp reads its 32 rows of stage
+  // t+1 from the k-chunked staging copy (one 16-byte load per 4 k, 32
+  // consecutive rows per warp load), and after computing stage t writes them
+  // transposed, [BK][32], into its other private buffer (32 consecutive rows per
+  // warp store).  Neither side has bank conflicts, the latency hides under the
+  // FFMAs, and no warp waits for another.
+  long long t_all = 0, total_stages = 0;
+  float4 xv[Cfg::kStaged ? BK / 4 : 1];
+  float* priv = sAp + cw * 2 * BK * 32;
+  auto x_load = [&](int slot) {
+    const float* st = sAst + slot * Cfg::kStaging + (wm * 32 + lane) * 4;
+#pragma unroll
+    for (int q = 0; q < BK / 4; ++q) xv[q] = *reinterpret_cast<const float4*>(st + q * BM * 4);
+  };
+  auto x_store = [&](int buf) {
+    float* d = priv + buf * BK * 32 + lane;
+#pragma unroll
+    for (int q = 0; q < BK / 4; ++q) {
+      d[(4 * q + 0) * 32] = xv[q].x;
+      d[(4 * q + 1) * 32] = xv[q].y;
+      d[(4 * q + 2) * 32] = xv[q].z;
+      d[(4 * q + 3) * 32] = xv[q].w;
+    }
+  };
   if constexpr (Cfg::kStaged) {
     const int my_tiles =
         blockIdx.x < total_tiles ? (total_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
     total_stages = (long long)my_tiles * p.k_tiles;
-  }
-  float4 xv[kXPer];
-  auto x_load = [&](long long u) -> bool {  // wait for stage u's copies, read my share
-    const int slot = (int)(u % STAGES);
-    const uint32_t ph = (uint32_t)((u / STAGES) & 1);
-    if (!mbar_wait(tfull0 + 8 * slot, ph, p.wait_limit_ns, p.status, kStatusTimeoutFull))
-      return false;
-    const float* st = sAst + slot * Cfg::kStaging;
-#pragma unroll
-    for (int it = 0; it < kXPer; ++it) {
-      const int idx = (it * Cfg::kConsumerWarps + cw) * 32 + lane;
-      const int q = idx / BM, m = idx % BM;
-      xv[it] = *reinterpret_cast<const float4*>(st + (q * BM + m) * 4);
-    }
-    return true;
-  };
-  auto x_store = [&](long long u) {  // write my share transposed, then count it in
-    const int slot = (int)(u % STAGES);
-    float* dst = sA + slot * Cfg::kAStage;
-#pragma unroll
-    for (int it = 0; it < kXPer; ++it) {
-      const int idx = (it * Cfg::kConsumerWarps + cw) * 32 + lane;
-      const int q = idx / BM, m = idx % BM;
-      dst[(4 * q + 0) * BM + m] = xv[it].x;
-      dst[(4 * q + 1) * BM + m] = xv[it].y;
-      dst[(4 * q + 2) * BM + m] = xv[it].z;
-      dst[(4 * q + 3) * BM + m] = xv[it].w;
-    }
-    mbar_arrive(full0 + 8 * slot);
-  };
-  if constexpr (Cfg::kStaged) {
-    for (; xt < total_stages && xt < Cfg::kAhead; ++xt) {
-      if (!x_load(xt)) return;
-      x_store(xt);
+    if (total_stages > 0) {
+      if (!mbar_wait(full0, 0, p.wait_limit_ns, p.status, kStatusTimeoutFull)) return;
+      x_load(0);
+      x_store(0);
+      __syncwarp();
     }
   }
 
@@ -312,16 +287,23 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
       for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
 
     for (int kt = 0; kt < p.k_tiles; ++kt) {
-      bool x_now = false;
+      const float* As;
+      bool next = false;
       if constexpr (Cfg::kStaged) {
-        if (xt < total_stages) {
-          if (!x_load(xt)) return;
-          x_now = true;
+        next = t_all + 1 < total_stages;
+        if (next) {
+          const int ns = stage + 1 == STAGES ? 0 : stage + 1;
+          const uint32_t np = stage + 1 == STAGES ? phase ^ 1u : phase;
+          if (!mbar_wait(full0 + 8 * ns, np, p.wait_limit_ns, p.status, kStatusTimeoutFull))
+            return;
+          x_load(ns);
         }
+        As = priv + (int)(t_all & 1) * BK * 32 + 4 * tr;
+      } else {
+        if (!mbar_wait(full0 + 8 * stage, phase, p.wait_limit_ns, p.status, kStatusTimeoutFull))
+          return;  // the status word says why; the producer drains and leaves too
+        As = sA + stage * Cfg::kAStage + a_off;
       }
-      if (!mbar_wait(full0 + 8 * stage, phase, p.wait_limit_ns, p.status, kStatusTimeoutFull))
-        return;  // the status word says why; the producer drains and leaves too
-      const float* As = sA + stage * Cfg::kAStage + a_off;
       const float* Bs = sB + stage * Cfg::kBStage + b_off;
       if constexpr (ALAY == kAKChunk) {
 #pragma unroll
@@ -349,8 +331,8 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
       } else {
 #pragma unroll
         for (int k = 0; k < BK; ++k) {
-          const float4 a0 = *reinterpret_cast<const float4*>(As + k * BM);
-          const float4 a1 = *reinterpret_cast<const float4*>(As + k * BM + 16);
+          const float4 a0 = *reinterpret_cast<const float4*>(As + k * Cfg::kARow);
+          const float4 a1 = *reinterpret_cast<const float4*>(As + k * Cfg::kARow + 16);
           const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
           float b[TN];
 #pragma unroll
@@ -362,14 +344,12 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
         }
       }
       if constexpr (Cfg::kStaged) {
-        if (x_now) {
-          x_store(xt);
-          ++xt;
-        }
+        if (next) x_store((int)((t_all + 1) & 1));
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8 * stage);
       if (++stage == STAGES) stage = 0, phase ^= 1u;
+      ++t_all;
     }
 
     // Epilogue: C = alpha*acc + beta*C, C read only when beta != 0, float4
@@ -450,7 +430,16 @@ cudaError_t launch_ffma(const SgemmParams& p, const CUtensorMap* tmA, const CUte
     NAME, BM, BN, BK, ST, TN, ALAY, FEED,                                                        \
         FfmaCfg<BM, BN, BK, WM, WN, TN, ST, ALAY, FEED, PW, ORD>::kThreads,                      \
         FfmaCfg<BM, BN, BK, WM, WN, TN, ST, ALAY, FEED, PW, ORD>::kSmemBytes,                    \
-        &launch_ffma<BM, BN, BK, WM, WN, TN, ST, ALAY, FEED, PW, ORD>                            \
+        &launch_ffma<BM, BN, BK, WM, WN, TN, ST, ALAY, FEED, PW, ORD>, 0                         \
+  }
+
+// The same kernel behind a transpose of row-major A into a workspace.
+#define B2G_FFMA_PLAN_PRE(NAME, BM, BN, BK, WM, WN, TN, ST, PW, ORD)                              \
+  Plan {                                                                                         \
+    NAME, BM, BN, BK, ST, TN, kAKMajor, kFeedTMA,                                                \
+        FfmaCfg<BM, BN, BK, WM, WN, TN, ST, kAKMajor, kFeedTMA, PW, ORD>::kThreads,              \
+        FfmaCfg<BM, BN, BK, WM, WN, TN, ST, kAKMajor, kFeedTMA, PW, ORD>::kSmemBytes,            \
+        &launch_ffma<BM, BN, BK, WM, WN, TN, ST, kAKMajor, kFeedTMA, PW, ORD>, 1                 \
   }
 
 }  // namespace b2g

@@ -54,6 +54,8 @@ struct Plan {
   int threads;  // CTA size (consumer warps + producer warps)
   int smem_bytes;
   LaunchFn launch;
+  int pretranspose;  // 1: row-major A is first transposed into a workspace, then this
+                     // plan's kernel (which reads A stored K x M) runs on it
 };
 
 // Plans compiled in each kernel translation unit.

@@ -1,0 +1,65 @@
+// transpose.cu -- At = A^T for the pre-transposed GEMM plans.
+//
+// The FFMA kernels run fastest when A reaches shared memory as [k][m] rows
+// (a thread's eight m values in two 16-byte vectors).  Row-major A has k
+// contiguous instead, so the pre-transposed plans first write At (K x ldat,
+// row-major, ldat = M rounded up to 4) into a workspace with this HBM-bound
+// kernel: 64 x 64 tiles, 16-byte loads of A rows, a [64 k][64 m] shared tile
+// written by 32 consecutive m per warp store (no bank conflicts), and 16-byte
+// stores of At rows.  Requires A 16-byte aligned with lda % 4 == 0 and
+// K % 4 == 0 (the callers check); M is arbitrary.  Columns M .. ldat-1 of At
+// are padding and receive zeros.
+#include <cuda_runtime.h>
+
+#include "transpose.h"
+
+namespace b2g {
+
+constexpr int kTT = 64;  // tile edge (m and k)
+
+__global__ void __launch_bounds__(256) transpose_a_kernel(const float* __restrict__ A, int M,
+                                                          int K, long long lda,
+                                                          float* __restrict__ At,
+                                                          long long ldat) {
+  __shared__ __align__(16) float tile[kTT][kTT];  // [k][m]
+  const int m0 = blockIdx.x * kTT, k0 = blockIdx.y * kTT;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // load: warp w takes 4-k chunks c = w, w+8; lanes take 32 consecutive rows
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int m = m0 + h * 32 + lane;
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+      const int c = warp + 8 * cc;  // 0..15
+      const int k = k0 + 4 * c;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (m < M && k < K) v = *reinterpret_cast<const float4*>(A + (long long)m * lda + k);
+      tile[4 * c + 0][h * 32 + lane] = v.x;
+      tile[4 * c + 1][h * 32 + lane] = v.y;
+      tile[4 * c + 2][h * 32 + lane] = v.z;
+      tile[4 * c + 3][h * 32 + lane] = v.w;
+    }
+  }
+  __syncthreads();
+  // store: 16 threads cover one At row segment of 64 m as 16-byte vectors
+  const int t = threadIdx.x & 15, r = threadIdx.x >> 4;  // r = 0..15
+#pragma unroll
+  for (int rr = 0; rr < kTT / 16; ++rr) {
+    const int kl = r + 16 * rr;
+    const int k = k0 + kl, m = m0 + 4 * t;
+    if (k < K && m < ldat) {
+      const float4 v = *reinterpret_cast<const float4*>(&tile[kl][4 * t]);
+      *reinterpret_cast<float4*>(At + (long long)k * ldat + m) = v;
+    }
+  }
+}
+
+cudaError_t launch_transpose_a(const float* A, int M, int K, long long lda, float* At,
+                               long long ldat, cudaStream_t stream) {
+  const dim3 grid((unsigned)((M + kTT - 1) / kTT), (unsigned)((K + kTT - 1) / kTT));
+  void* args[] = {(void*)&A, (void*)&M, (void*)&K, (void*)&lda, (void*)&At, (void*)&ldat};
+  return cudaLaunchKernel(reinterpret_cast<const void*>(&transpose_a_kernel), grid, dim3(256),
+                          args, 0, stream);
+}
+
+}  // namespace b2g

@@ -1,0 +1,13 @@
+// transpose.h -- launcher of the A -> A^T workspace kernel (transpose.cu).
+#pragma once
+#include <cuda_runtime.h>
+
+namespace b2g {
+
+// At[k][m] = A[m][k] for m < M, k < K; columns M .. ldat-1 of At get zeros.
+// A: 16-byte aligned, lda % 4 == 0, K % 4 == 0.  At: 16-byte aligned,
+// ldat % 4 == 0, ldat >= M, K x ldat floats.
+cudaError_t launch_transpose_a(const float* A, int M, int K, long long lda, float* At,
+                               long long ldat, cudaStream_t stream);
+
+}  // namespace b2g

@@ -16,21 +16,24 @@ struct TuneRule {
   int cls;
   int m_min, m_max;  // inclusive bounds on M
   int n_min, n_max;  // inclusive bounds on N
+  double mnk_min;    // smallest M*N*K the rule applies to
   const char* plan;
+  const char* fallback;  // plan used when `plan` needs a workspace that cannot be had
 };
 
 constexpr int kInf = 0x7fffffff;
 
-// Measured on GB300 (152 SMs); see the bench sweep notes in the design document.
+// Chosen from per-plan timings on GB300 (152 SMs) over the square sweep
+// (128^3 .. 8192^3), the 8192x11008x4096 and 16x4096x4096 shapes and the
+// ragged 1000x1025x777 shape.
 const TuneRule kTuneTable[] = {
-    {kClassFast, 0, 48, 0, kInf, "tma_32x64x32_s6"},
-    {kClassFast, 49, 127, 0, kInf, "tma_64x128x16_s6"},
-    {kClassFast, 128, kInf, 0, 127, "tma_64x128x16_s6"},
-    {kClassFast, 128, kInf, 128, kInf, "tma_128x128x16_s6"},
-    {kClassFastTransA, 0, kInf, 0, kInf, "tmaT_128x128x16_s6"},
-    {kClassGeneral, 0, 96, 0, kInf, "gen_64x64x16_s4"},
-    {kClassGeneral, 97, kInf, 0, 96, "gen_64x64x16_s4"},
-    {kClassGeneral, 97, kInf, 97, kInf, "gen_128x128x16_s4"},
+    {kClassFast, 0, 48, 0, kInf, 0, "tma_64x128x16_s6_o2", nullptr},
+    {kClassFast, 49, kInf, 0, kInf, 1.0e9, "pre_64x128x16_s6", "tma_64x128x16_s6_o2"},
+    {kClassFast, 49, kInf, 0, kInf, 0, "tma_64x128x16_s6_o2", nullptr},
+    {kClassFastTransA, 0, kInf, 0, kInf, 0, "tmaT_64x128x16_s6", nullptr},
+    {kClassGeneral, 0, 96, 0, kInf, 0, "gen_64x64x16_s4", nullptr},
+    {kClassGeneral, 97, kInf, 0, 96, 0, "gen_64x64x16_s4", nullptr},
+    {kClassGeneral, 97, kInf, 97, kInf, 0, "gen_128x128x16_s4", nullptr},
 };
 
 }  // namespace b2g

@@ -27,6 +27,8 @@
 #ifndef B2G_SGEMM_H
 #define B2G_SGEMM_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -55,6 +57,16 @@ extern "C" {
  * operands with lda, ldb, ldc and K multiples of 4 take the bulk-tensor fed
  * kernels, everything else the 4-byte-fed kernel.  The plan comes from the
  * library's shape-keyed tune table.
+ *
+ * Workspace: for large aligned problems the fastest plan first writes A^T
+ * (K x round_up(M, 4) floats) into a workspace.  This entry point uses a
+ * library-owned workspace, one per device, allocated stream-ordered
+ * (cudaMallocAsync) the first time a call needs it and grown when a later call
+ * needs more; calls on different streams that share it are ordered by an event
+ * the library records after each use.  While `stream` is being captured into a
+ * CUDA graph, or when the allocation fails, the call takes a plan that needs no
+ * workspace instead.  b2g_sgemm_ws lets the caller supply the workspace and
+ * never allocates; b2g_release_workspaces frees the library-owned ones.
  */
 int b2g_sgemm(int M, int N, int K, float alpha, const float* A, int lda, const float* B, int ldb,
               float beta, float* C, int ldc, void* stream);
@@ -68,9 +80,37 @@ int b2g_sgemm_ex(int transA, int transB, int M, int N, int K, float alpha, const
                  const float* B, int ldb, float beta, float* C, int ldc, void* stream);
 
 /*
+ * As b2g_sgemm_ex with a caller-owned device workspace of workspace_bytes
+ * (16-byte aligned).  Never allocates.  When the workspace is NULL or smaller
+ * than b2g_sgemm_workspace_size reports, a plan that needs none runs instead
+ * (slower, same result bound).  The caller orders reuse of the workspace
+ * across streams.
+ */
+int b2g_sgemm_ws(int transA, int transB, int M, int N, int K, float alpha, const float* A, int lda,
+                 const float* B, int ldb, float beta, float* C, int ldc, void* workspace,
+                 size_t workspace_bytes, void* stream);
+
+/*
+ * Workspace bytes the tune table's plan wants for these arguments (0 when it
+ * needs none), stored in *bytes.  Returns 0, a B2G_ERR_* code for invalid
+ * arguments, or B2G_ERR_NULL when bytes is NULL.  Launches nothing.
+ */
+int b2g_sgemm_workspace_size(int transA, int transB, int M, int N, int K, float alpha,
+                             const float* A, int lda, const float* B, int ldb, const float* C,
+                             int ldc, size_t* bytes);
+
+/*
+ * Free the library-owned workspaces of all devices, after waiting for the
+ * work that used them.  Later calls allocate again when needed.  Returns 0 or
+ * B2G_ERR_CUDA.
+ */
+int b2g_release_workspaces(void);
+
+/*
  * As b2g_sgemm_ex, but run plan `plan` (0 <= plan < b2g_plan_count()) instead of
  * the tune table's choice.  Returns B2G_ERR_UNSUPPORTED when that plan cannot
- * take these operands (alignment, op() flags).  For tests and tuning sweeps.
+ * take these operands (alignment, op() flags) or needs a workspace that cannot
+ * be had (it uses the library-owned one).  For tests and tuning sweeps.
  */
 int b2g_sgemm_with_plan(int plan, int transA, int transB, int M, int N, int K, float alpha,
                         const float* A, int lda, const float* B, int ldb, float beta, float* C,

@@ -53,7 +53,7 @@ def test_version_and_plans(b2g):
         info = b2g.b2g_plan_info(i)
         assert info["BM"] > 0 and info["BN"] > 0 and info["BK"] % 4 == 0
         assert info["threads"] % 32 == 0 and info["smem_bytes"] <= 227 * 1024
-        assert n.startswith(("tma", "gen"))
+        assert n.startswith(("tma", "gen", "pre"))
     assert b2g.b2g_plan_name(len(names)) is None
     with pytest.raises(b2g.B2GError):
         b2g.b2g_plan_info(-1)
@@ -102,9 +102,10 @@ def _plan(b2g, *a):
 
 
 def test_tune_table_classes(b2g):
-    # aligned, ld % 4 == 0, K % 4 == 0 -> bulk-tensor plans
-    assert _plan(b2g, 0, 0, 4096, 4096, 4096, 1.0, FAKE, 4096, FAKE, 4096, FAKE, 4096).startswith("tma_")
+    # aligned, ld % 4 == 0, K % 4 == 0 -> bulk-tensor plans; large ones pre-transpose A
+    assert _plan(b2g, 0, 0, 4096, 4096, 4096, 1.0, FAKE, 4096, FAKE, 4096, FAKE, 4096).startswith("pre_")
     assert _plan(b2g, 0, 0, 16, 4096, 4096, 1.0, FAKE, 4096, FAKE, 4096, FAKE, 4096).startswith("tma_")
+    assert _plan(b2g, 0, 0, 64, 64, 64, 1.0, FAKE, 64, FAKE, 64, FAKE, 64).startswith("tma_")
     # odd leading dimension -> 4-byte feed
     assert _plan(b2g, 0, 0, 1000, 1025, 777, 0.75, FAKE, 777, FAKE, 1025, FAKE, 1025).startswith("gen_")
     # misaligned base pointer -> 4-byte feed
@@ -114,6 +115,20 @@ def test_tune_table_classes(b2g):
     # op(A) = A^T aligned -> transposed-layout bulk-tensor plan; op(B) = B^T -> 4-byte feed
     assert _plan(b2g, 1, 0, 512, 512, 512, 1.0, FAKE, 512, FAKE, 512, FAKE, 512).startswith("tmaT_")
     assert _plan(b2g, 0, 1, 512, 512, 512, 1.0, FAKE, 512, FAKE, 512, FAKE, 512).startswith("gen_")
+
+
+def test_workspace_size_query(b2g):
+    rc, n = b2g.b2g_sgemm_workspace_size(0, 0, 4096, 4096, 4096, 1.0, FAKE, 4096, FAKE, 4096,
+                                         FAKE, 4096)
+    assert rc == 0 and n == 4096 * 4096 * 4  # A^T, K x round_up(M, 4) floats
+    rc, n = b2g.b2g_sgemm_workspace_size(0, 0, 1001, 4096, 4096, 1.0, FAKE, 4096, FAKE, 4096,
+                                         FAKE, 4096)
+    assert rc == 0 and n == 4096 * 1004 * 4
+    rc, n = b2g.b2g_sgemm_workspace_size(0, 0, 64, 64, 64, 1.0, FAKE, 64, FAKE, 64, FAKE, 64)
+    assert rc == 0 and n == 0
+    rc, n = b2g.b2g_sgemm_workspace_size(0, 0, 64, 64, 64, 1.0, FAKE, 63, FAKE, 64, FAKE, 64)
+    assert rc == -2
+    assert b2g.b2g_release_workspaces() == 0  # nothing allocated yet: no CUDA call needed
 
 
 def test_forced_plan_range(b2g):
