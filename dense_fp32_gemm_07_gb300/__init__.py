@@ -30,11 +30,12 @@ B2G_ERR_INVALID_PLAN = -7
 B2G_ERR_TENSOR_MAP = -8
 B2G_ERR_CUDA = -9
 B2G_ERR_TIMEOUT = -10
+B2G_ERR_SCRATCH_LIMIT = -11
 
 # every symbol include/b2g_sgemm.h declares
 EXPORTS = (
     "b2g_sgemm", "b2g_sgemm_ex", "b2g_sgemm_with_plan", "b2g_sgemm_select_plan",
-    "b2g_sgemm_ws", "b2g_sgemm_workspace_size", "b2g_release_workspaces",
+    "b2g_sgemm_ws", "b2g_sgemm_workspace_size", "b2g_release_workspaces", "b2g_sgemm_noalloc",
     "b2g_plan_count", "b2g_plan_name", "b2g_plan_info", "b2g_status", "b2g_set_wait_limit_ns",
     "b2g_debug_stop_after", "b2g_strerror", "b2g_version",
 )
@@ -70,6 +71,7 @@ def _load():
         lib.b2g_sgemm_workspace_size.argtypes = [i, i, i, i, i, f, vp, i, vp, i, vp, i,
                                                  ctypes.POINTER(ctypes.c_size_t)]
         lib.b2g_release_workspaces.argtypes = []
+        lib.b2g_sgemm_noalloc.argtypes = gemm
         lib.b2g_plan_count.argtypes = []
         lib.b2g_plan_name.argtypes = [i]
         lib.b2g_plan_name.restype = ctypes.c_char_p
@@ -130,6 +132,12 @@ def b2g_sgemm_workspace_size(transA, transB, M, N, K, alpha, A, lda, B, ldb, C, 
 
 def b2g_release_workspaces() -> int:
     return _load().b2g_release_workspaces()
+
+
+def b2g_sgemm_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> int:
+    """The SGEMM for callers that cannot let the library allocate device memory
+    (its scratch is a fixed per-device array; see include/b2g_sgemm.h)."""
+    return _load().b2g_sgemm_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
 
 
 def b2g_plan_count() -> int:

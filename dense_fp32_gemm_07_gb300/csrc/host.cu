@@ -494,6 +494,8 @@ const char* b2g_strerror(int code) {
     case B2G_ERR_TENSOR_MAP: return "bulk-tensor descriptor rejected by the driver";
     case B2G_ERR_CUDA: return "CUDA runtime call failed";
     case B2G_ERR_TIMEOUT: return "a kernel's bounded wait ran out (see b2g_status flags)";
+    case B2G_ERR_SCRATCH_LIMIT:
+      return "the call needs more scratch than b2g_sgemm_noalloc's fixed array holds";
     default: return "unknown error code";
   }
 }

@@ -44,6 +44,7 @@ extern "C" {
 #define B2G_ERR_TENSOR_MAP (-8)   /* the driver refused a bulk-tensor descriptor */
 #define B2G_ERR_CUDA (-9)         /* another CUDA runtime call failed */
 #define B2G_ERR_TIMEOUT (-10)     /* b2g_status(): a kernel's bounded wait ran out */
+#define B2G_ERR_SCRATCH_LIMIT (-11) /* b2g_sgemm_noalloc: more scratch than its fixed array */
 
 /*
  * Row-major SGEMM, C = alpha*A*B + beta*C.
@@ -105,6 +106,29 @@ int b2g_sgemm_workspace_size(int transA, int transB, int M, int N, int K, float 
  * B2G_ERR_CUDA.
  */
 int b2g_release_workspaces(void);
+
+/*
+ * Row-major SGEMM (same arguments and result bound as b2g_sgemm) for callers
+ * that must not have the library allocate device memory -- for instance an
+ * application whose allocator reserved device memory at start-up and forbids
+ * later cudaMalloc / cudaMallocAsync calls.  It never allocates: its scratch
+ * (A^T for the plans that transpose A first) is a fixed 64 MiB array that every
+ * device loading the library holds until the process exits.
+ *   - Calls whose scratch need, K x round_up(M, 4) floats for those plans,
+ *     exceeds 64 MiB (16,777,216 floats) are rejected with
+ *     B2G_ERR_SCRATCH_LIMIT and launch nothing; use b2g_sgemm_ws with your own
+ *     buffer for them.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before capturing any stream.
+ *   - The array is shared by every call on a device and keeps the last call's
+ *     contents; each call rewrites all of the scratch it reads, so nothing
+ *     needs clearing, but calls that overlap on the GPU (different streams with
+ *     no ordering between them) race on it.
+ * No counterpart on the pages: it serves callers, not the method.
+ */
+int b2g_sgemm_noalloc(int M, int N, int K, float alpha, const float* A, int lda, const float* B,
+                      int ldb, float beta, float* C, int ldc, void* stream);
 
 /*
  * As b2g_sgemm_ex, but run plan `plan` (0 <= plan < b2g_plan_count()) instead of
