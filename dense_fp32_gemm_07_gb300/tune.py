@@ -1,0 +1,82 @@
+"""Per-plan timing sweep behind the shape-keyed tune table (csrc/tune_table.h).
+
+    python -m dense_fp32_gemm_07_gb300.tune [--once] MxNxK[xALPHAxBETA] ...
+
+Times every compiled plan that accepts the operands on each shape (CUDA events
+on the launching stream, after warm-up, operands uniform[-1, 1) made by
+torch), prints TFLOP/s per plan and marks the one the table picks.  Plans
+that read A stored K x M (tmaT_*) get a transposed copy of A.  With --once
+every plan runs exactly one launch per shape and nothing is timed: that is the
+form to run under ncu to compare plans' counters.
+"""
+from __future__ import annotations
+
+import argparse
+import sys
+
+import dense_fp32_gemm_07_gb300 as b2g
+
+
+def parse_shape(s: str):
+    f = s.split("x")
+    M, N, K = int(f[0]), int(f[1]), int(f[2])
+    alpha = float(f[3]) if len(f) > 3 else 1.0
+    beta = float(f[4]) if len(f) > 4 else 0.0
+    return M, N, K, alpha, beta
+
+
+def sweep(shapes, once=False, out=sys.stdout):
+    import torch
+
+    from dense_fp32_gemm_07_gb300 import build
+
+    build.build()
+    names = b2g.plans()
+    for M, N, K, alpha, beta in shapes:
+        A = torch.rand(M, K, device="cuda") * 2 - 1
+        B = torch.rand(K, N, device="cuda") * 2 - 1
+        C = torch.rand(M, N, device="cuda") * 2 - 1
+        At = A.t().contiguous()
+        flops = 2.0 * M * N * K
+        iters = max(3, min(50, int(2e11 / flops)))
+        sel = b2g.b2g_sgemm_select_plan(0, 0, M, N, K, alpha, A.data_ptr(), K, B.data_ptr(), N,
+                                        C.data_ptr(), N)
+        for pi, name in enumerate(names):
+            trans = name.startswith("tmaT")
+
+            def call():
+                b2g.sgemm(At if trans else A, B, C, alpha, beta, transA=trans, plan=pi)
+
+            try:
+                call()
+            except b2g.B2GError:
+                continue  # the plan cannot take these operands
+            torch.cuda.synchronize()
+            if once:
+                print(f"{M}x{N}x{K} {name}", file=out, flush=True)
+                continue
+            for _ in range(2):
+                call()
+            ev0 = torch.cuda.Event(enable_timing=True)
+            ev1 = torch.cuda.Event(enable_timing=True)
+            ev0.record()
+            for _ in range(iters):
+                call()
+            ev1.record()
+            torch.cuda.synchronize()
+            ms = ev0.elapsed_time(ev1) / iters
+            mark = "  <- table" if pi == sel else ""
+            print(f"{M}x{N}x{K} {name:26s} {ms:9.4f} ms {flops / ms / 1e9:8.2f} TFLOP/s{mark}",
+                  file=out, flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("shapes", nargs="*", default=["4096x4096x4096x1x0.5"])
+    ap.add_argument("--once", action="store_true")
+    args = ap.parse_args()
+    sweep([parse_shape(s) for s in args.shapes], once=args.once)
+
+
+if __name__ == "__main__":
+    main()
