@@ -214,7 +214,7 @@ int select_plan(const Call& c, int* fallback = nullptr) {
   const double mnk = (double)c.M * c.N * c.K;
   for (const TuneRule& r : kTuneTable) {
     if (r.cls == cls && c.M >= r.m_min && c.M <= r.m_max && c.N >= r.n_min && c.N <= r.n_max &&
-        mnk >= r.mnk_min) {
+        mnk >= r.mnk_min && mnk < r.mnk_max) {
       const int i = plan_index(r.plan);
       if (i >= 0) {
         if (fallback) {

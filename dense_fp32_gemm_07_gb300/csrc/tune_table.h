@@ -19,6 +19,7 @@ struct TuneRule {
   double mnk_min;    // smallest M*N*K the rule applies to
   const char* plan;
   const char* fallback;  // plan used when `plan` needs a workspace that cannot be had
+  double mnk_max = 1e300;  // the rule applies while M*N*K < mnk_max
 };
 
 constexpr int kInf = 0x7fffffff;
@@ -27,13 +28,21 @@ constexpr int kInf = 0x7fffffff;
 // (128^3 .. 8192^3), the 8192x11008x4096 and 16x4096x4096 shapes and the
 // ragged 1000x1025x777 shape.
 const TuneRule kTuneTable[] = {
-    {kClassFast, 0, 48, 0, kInf, 0, "tma_64x128x16_s6_o2", nullptr},
-    {kClassFast, 49, kInf, 0, kInf, 1.0e9, "pre_64x128x16_s6", "tma_64x128x16_s6_o2"},
-    {kClassFast, 49, kInf, 0, kInf, 0, "tma_64x128x16_s6_o2", nullptr},
-    {kClassFastTransA, 0, kInf, 0, kInf, 0, "tmaT_64x128x16_s6", nullptr},
-    {kClassGeneral, 0, 96, 0, kInf, 0, "gen_64x64x16_s4", nullptr},
-    {kClassGeneral, 97, kInf, 0, 96, 0, "gen_64x64x16_s4", nullptr},
-    {kClassGeneral, 97, kInf, 97, kInf, 0, "gen_128x128x16_s4", nullptr},
+    // skinny M: too few row tiles to fill 152 SMs with any plan here (split-K
+    // would be the remedy); the k-chunked plan needs no workspace
+    {kClassFast, 0, 48, 0, kInf, 0, "tma_64x128x16_s6_o1", nullptr},
+    // up to ~1.3e9 multiply-adds the transpose costs more than it saves
+    {kClassFast, 49, kInf, 0, kInf, 0, "tma_64x128x16_s6_o2", nullptr, 2.0e9},
+    // 2048^3-class: 128x128 tiles fill the SMs better than 64x128
+    {kClassFast, 49, kInf, 0, kInf, 2.0e9, "pre_128x128x16_s6_o1", "tmaX_128x128x16_s6_o2", 2.5e10},
+    // 4096^3 and 8192x11008x4096
+    {kClassFast, 49, kInf, 0, kInf, 2.5e10, "pre_64x128x16_s6", "tmaX_128x128x16_s6_o2", 4.0e11},
+    // 8192^3 and larger
+    {kClassFast, 49, kInf, 0, kInf, 4.0e11, "pre_128x128x16_s6_o1", "tmaX_128x128x16_s6_o2"},
+    {kClassFastTransA, 0, kInf, 0, kInf, 0, "tmaT_64x128x16_s6", nullptr, 2.5e10},
+    {kClassFastTransA, 0, kInf, 0, kInf, 2.5e10, "tmaT_64x128x16_s6", nullptr, 4.0e11},
+    {kClassFastTransA, 0, kInf, 0, kInf, 4.0e11, "tmaT_128x128x16_s6_o1", nullptr},
+    {kClassGeneral, 0, kInf, 0, kInf, 0, "gen_64x64x16_s4", nullptr},
 };
 
 }  // namespace b2g

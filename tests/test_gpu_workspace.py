@@ -25,7 +25,7 @@ def _inputs(seed, M, N, K):
 
 
 # M*N*K at or above the size where the tune table pre-transposes A
-SHAPE = (1030, 1100, 1024)
+SHAPE = (1030, 1500, 1400)
 
 
 def test_table_picks_pretranspose(tb):

@@ -39,7 +39,7 @@ def _run(torch, fn, A, B, C, alpha, beta):
 def test_noalloc_matches_regular_entry_point_twice(tb):
     torch, b2g = tb
     lib = b2g.library()  # the C ABI through ctypes
-    M, N, K = 1030, 1100, 1024  # large enough that the plan uses the scratch
+    M, N, K = 1030, 1500, 1400  # large enough that the plan uses the scratch
     rc, need = b2g.b2g_sgemm_workspace_size(0, 0, M, N, K, 1.0, 1 << 20, K, 1 << 20, N,
                                             1 << 20, N)
     assert rc == 0 and 0 < need <= 64 << 20
