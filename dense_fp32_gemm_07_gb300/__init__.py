@@ -36,6 +36,7 @@ B2G_ERR_SCRATCH_LIMIT = -11
 EXPORTS = (
     "b2g_sgemm", "b2g_sgemm_ex", "b2g_sgemm_with_plan", "b2g_sgemm_select_plan",
     "b2g_sgemm_ws", "b2g_sgemm_workspace_size", "b2g_release_workspaces", "b2g_sgemm_noalloc",
+    "b2g_sgemm_3xtf32",
     "b2g_plan_count", "b2g_plan_name", "b2g_plan_info", "b2g_status", "b2g_set_wait_limit_ns",
     "b2g_debug_stop_after", "b2g_strerror", "b2g_version",
 )
@@ -72,6 +73,7 @@ def _load():
                                                  ctypes.POINTER(ctypes.c_size_t)]
         lib.b2g_release_workspaces.argtypes = []
         lib.b2g_sgemm_noalloc.argtypes = gemm
+        lib.b2g_sgemm_3xtf32.argtypes = gemm
         lib.b2g_plan_count.argtypes = []
         lib.b2g_plan_name.argtypes = [i]
         lib.b2g_plan_name.restype = ctypes.c_char_p
@@ -138,6 +140,25 @@ def b2g_sgemm_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) ->
     """The SGEMM for callers that cannot let the library allocate device memory
     (its scratch is a fixed per-device array; see include/b2g_sgemm.h)."""
     return _load().b2g_sgemm_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
+
+
+def b2g_sgemm_3xtf32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> int:
+    return _load().b2g_sgemm_3xtf32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
+
+
+def sgemm_3xtf32(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):
+    """C <- alpha * A @ B + beta * C on the tensor cores (3xTF32 split); see
+    b2g_sgemm_3xtf32 in include/b2g_sgemm.h."""
+    lda, ldb, ldc = _check(A, "A"), _check(B, "B"), _check(C, "C")
+    M, K = A.shape
+    Kb, N = B.shape
+    if Kb != K or tuple(C.shape) != (M, N):
+        raise ValueError("shape mismatch")
+    rc = b2g_sgemm_3xtf32(M, N, K, float(alpha), A.data_ptr(), lda, B.data_ptr(), ldb,
+                          float(beta), C.data_ptr(), ldc, _stream_handle(stream))
+    if rc:
+        raise B2GError(rc)
+    return C
 
 
 def b2g_plan_count() -> int:

@@ -15,6 +15,7 @@
 
 #include "../../include/b2g_sgemm.h"
 #include "sgemm_params.h"
+#include "tf32x3.h"
 #include "transpose.h"
 #include "tune_table.h"
 
@@ -248,6 +249,23 @@ int encode_2d(CUtensorMap* m, const float* base, long long inner, long long oute
   return r == CUDA_SUCCESS ? 0 : B2G_ERR_TENSOR_MAP;
 }
 
+// 2-D row-major tensor {inner, outer} with boxes of 32 x box_outer FP32
+// elements (128 bytes) landing with the 128-byte swizzle: the K-major operand
+// layout the tensor cores read.
+int encode_2d_sw128(CUtensorMap* m, const float* base, long long inner, long long outer,
+                    long long row_stride_elems, int box_outer) {
+  auto enc = encoder();
+  if (!enc) return B2G_ERR_TENSOR_MAP;
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+  cuuint64_t strides[1] = {(cuuint64_t)row_stride_elems * 4};
+  cuuint32_t box[2] = {32, (cuuint32_t)box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : B2G_ERR_TENSOR_MAP;
+}
+
 // Row-major A (M x K, lda) seen as a 3-D tensor {4, M, K/4}: element (e, r, q) is
 // A[r][4q + e].  A box {4, BM, BK/4} lands in shared memory as [BK/4][BM][4].
 int encode_a_kchunk(CUtensorMap* m, const float* A, int M, int K, int lda, int BM, int BK) {
@@ -357,6 +375,60 @@ int run(const Call& c, int forced_plan, void* stream, void* user_ws = nullptr,
   return e == cudaSuccess ? 0 : B2G_ERR_LAUNCH;
 }
 
+// The 3xTF32 tensor-core path: split the operands into a workspace, then the
+// tcgen05 kernel.  Row-major, no op() flags; A 16-byte aligned with lda and K
+// multiples of 4 (B is read element by element by its split kernel).
+size_t tf32x3_bytes(const Call& c) {
+  return 2 * ((size_t)c.M * c.K + (size_t)c.N * c.K) * sizeof(float);
+}
+
+int run_tf32x3(const Call& c, void* stream) {
+  int rc = validate(c);
+  if (rc) return rc;
+  if (c.M == 0 || c.N == 0) return 0;
+  DeviceState* d = nullptr;
+  rc = device_state(&d);
+  if (rc) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (!needs_gemm(c)) return launch_scale(c, *d, st);
+  if (c.transA || c.transB || !aligned16(c.A) || c.lda % 4 || c.K % 4) return B2G_ERR_UNSUPPORTED;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  float* ws = static_cast<float*>(ws_acquire(dev, st, tf32x3_bytes(c)));
+  if (!ws) return B2G_ERR_UNSUPPORTED;  // capturing, or the workspace cannot be had
+  float* Ahi = ws;
+  float* Alo = Ahi + (size_t)c.M * c.K;
+  float* Bhi = Alo + (size_t)c.M * c.K;
+  float* Blo = Bhi + (size_t)c.N * c.K;
+  cudaError_t e = launch_split_a(c.A, c.M, c.K, c.lda, Ahi, Alo, d->sms, st);
+  if (e == cudaSuccess) e = launch_split_bt(c.B, c.K, c.N, c.ldb, Bhi, Blo, st);
+  CUtensorMap maps[4];
+  if (e == cudaSuccess) {
+    rc = encode_2d_sw128(&maps[0], Ahi, c.K, c.M, c.K, kTcBM);
+    if (!rc) rc = encode_2d_sw128(&maps[1], Alo, c.K, c.M, c.K, kTcBM);
+    if (!rc) rc = encode_2d_sw128(&maps[2], Bhi, c.K, c.N, c.K, kTcBN);
+    if (!rc) rc = encode_2d_sw128(&maps[3], Blo, c.K, c.N, c.K, kTcBN);
+  }
+  if (e == cudaSuccess && !rc) {
+    Tf32x3Params p;
+    p.M = c.M, p.N = c.N, p.K = c.K;
+    p.alpha = c.alpha, p.beta = c.beta;
+    p.C = c.C, p.ldc = c.ldc;
+    p.c_vec4 = aligned16(c.C) && c.ldc % 4 == 0;
+    p.tiles_m = (c.M + kTcBM - 1) / kTcBM;
+    p.tiles_n = (c.N + kTcBN - 1) / kTcBN;
+    p.group_m = 8;
+    p.k_tiles = (c.K + kTcBK - 1) / kTcBK;
+    p.wait_limit_ns = g_wait_limit_ns.load();
+    p.debug_stop_ktile = g_debug_stop.load();
+    p.status = d->status;
+    e = launch_tf32x3(p, maps, d->sms, st);
+  }
+  ws_release(dev, st);
+  if (rc) return rc;
+  return e == cudaSuccess ? 0 : B2G_ERR_LAUNCH;
+}
+
 }  // namespace
 }  // namespace b2g
 
@@ -381,6 +453,11 @@ int b2g_sgemm_with_plan(int plan, int transA, int transB, int M, int N, int K, f
   if (plan < 0 || plan >= num_plans()) return B2G_ERR_INVALID_PLAN;
   return run(Call{transA != 0, transB != 0, M, N, K, alpha, beta, A, lda, B, ldb, C, ldc}, plan,
              stream);
+}
+
+int b2g_sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int lda, const float* B,
+                     int ldb, float beta, float* C, int ldc, void* stream) {
+  return run_tf32x3(Call{0, 0, M, N, K, alpha, beta, A, lda, B, ldb, C, ldc}, stream);
 }
 
 int b2g_sgemm_ws(int transA, int transB, int M, int N, int K, float alpha, const float* A, int lda,

@@ -1,0 +1,358 @@
+// tf32x3.cu -- row-major SGEMM on the 5th-generation tensor cores with the
+// 3xTF32 split, reported apart from the FP32 FFMA path.
+//
+// The handbook ("GEMM 优化之路", section 接下来的优化方向, 使用 Tensor Core)
+// points out that tensor cores run the same tiled GEMM with the innermost step
+// replaced by matrix instructions, and that TF32 keeps FP32 inputs but only a
+// 10-bit mantissa.  Three TF32 products recover FP32 accuracy: every operand x
+// is split into hi = x rounded to TF32 and lo = x - hi (exact in FP32, at most
+// 2^-11 |x|), and
+//     A*B ~= A_lo*B_hi + A_hi*B_lo + A_hi*B_hi
+// (the dropped A_lo*B_lo term and the TF32 rounding of lo are below 2^-21 of
+// |a||b| per product), accumulated in FP32 in tensor memory.
+//
+// Stages:
+//  1. split kernels (HBM bound): A -> A_hi, A_lo (M x K, row-major = K-major);
+//     B -> B_hi^T, B_lo^T (N x K, transposed so that B is K-major too);
+//  2. a persistent tcgen05 kernel: one lane issues bulk-tensor copies of the
+//     four 128 x 32 tiles per stage (128-byte swizzle), one lane issues the
+//     three tcgen05.mma kind::tf32 per K step into a double-buffered 128 x 128
+//     FP32 accumulator in tensor memory, four warps read finished accumulators
+//     back (tcgen05.ld) and apply C = alpha*acc + beta*C.
+// Every wait is bounded; on a timeout the kernel flags the status word, waits
+// (bounded) for the work it started, frees its tensor memory and returns.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstring>
+
+#include "ptx.cuh"
+#include "sgemm_params.h"
+#include "tf32x3.h"
+
+namespace b2g {
+
+// ----------------------------------------------------------------- the split
+
+// hi = x rounded to the nearest TF32 value (ties away from zero); lo = x - hi,
+// exact.  Non-finite x passes through in hi with lo = 0; a finite x whose
+// rounding would overflow is truncated instead.
+__device__ __forceinline__ void tf32_split(float x, float& hi, float& lo) {
+  if (!isfinite(x)) {
+    hi = x;
+    lo = 0.f;
+    return;
+  }
+  const uint32_t u = __float_as_uint(x);
+  float h = __uint_as_float((u + 0x1000u) & 0xFFFFE000u);
+  if (!isfinite(h)) h = __uint_as_float(u & 0xFFFFE000u);
+  hi = h;
+  lo = x - h;
+}
+
+// A (M x K, lda) -> Ahi, Alo (M x K, leading dimension K).  16-byte vectors:
+// A 16-byte aligned, lda and K multiples of 4.
+__global__ void __launch_bounds__(256) split_a_kernel(const float* __restrict__ A, int M, int K,
+                                                      long long lda, float* __restrict__ Ahi,
+                                                      float* __restrict__ Alo) {
+  const long long kv = K / 4;
+  const long long total = (long long)M * kv;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long r = i / kv, c = (i - r * kv) * 4;
+    const float4 v = *reinterpret_cast<const float4*>(A + r * lda + c);
+    float4 h, l;
+    tf32_split(v.x, h.x, l.x);
+    tf32_split(v.y, h.y, l.y);
+    tf32_split(v.z, h.z, l.z);
+    tf32_split(v.w, h.w, l.w);
+    *reinterpret_cast<float4*>(Ahi + r * K + c) = h;
+    *reinterpret_cast<float4*>(Alo + r * K + c) = l;
+  }
+}
+
+// B (K x N, ldb) -> Bhi^T, Blo^T (N x K, leading dimension K) in 64 x 64
+// tiles: coalesced reads of B rows, 16-byte writes of the transposed rows.  The
+// scalar shared-memory writes of the [n][k] tile (rows padded to 68 floats so
+// the 16-byte reads stay aligned) are 4-way bank conflicted, which the
+// HBM-bound kernel does not notice.  K % 4 == 0; N arbitrary.
+__global__ void __launch_bounds__(256) split_bt_kernel(const float* __restrict__ B, int K, int N,
+                                                       long long ldb, float* __restrict__ Bhi,
+                                                       float* __restrict__ Blo) {
+  __shared__ __align__(16) float tile[64][68];  // [n][k], rows padded to keep 16-byte reads aligned
+  const int k0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // load: warp w takes rows k = k0 + w + 8j; lanes take 32 consecutive n (twice)
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int kl = warp + 8 * j, k = k0 + kl;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int nl = h * 32 + lane, n = n0 + nl;
+      tile[nl][kl] = (k < K && n < N) ? B[(long long)k * ldb + n] : 0.f;
+    }
+  }
+  __syncthreads();
+  // store: 16 threads per transposed row (64 k as 16 vectors), 16 rows per pass
+  const int t = threadIdx.x & 15, r = threadIdx.x >> 4;
+#pragma unroll
+  for (int rr = 0; rr < 4; ++rr) {
+    const int nl = r + 16 * rr, n = n0 + nl, k = k0 + 4 * t;
+    if (n < N && k < K) {
+      const float4 v = *reinterpret_cast<const float4*>(&tile[nl][4 * t]);
+      float4 h, l;
+      tf32_split(v.x, h.x, l.x);
+      tf32_split(v.y, h.y, l.y);
+      tf32_split(v.z, h.z, l.z);
+      tf32_split(v.w, h.w, l.w);
+      *reinterpret_cast<float4*>(Bhi + (long long)n * K + k) = h;
+      *reinterpret_cast<float4*>(Blo + (long long)n * K + k) = l;
+    }
+  }
+}
+
+// ------------------------------------------------------------- the tensor-core GEMM
+
+constexpr int kTcThreads = 192;  // warp 0 copies, warp 1 MMA, warps 2-5 epilogue
+constexpr uint32_t kTcTileBytes = kTcBM * kTcBK * 4;    // one 128 x 32 FP32 tile: 16 KB
+constexpr uint32_t kTcStageBytes = 4 * kTcTileBytes;    // A_hi, A_lo, B_hi^T, B_lo^T
+constexpr uint32_t kTcTmemCols = 2 * kTcBN;             // two FP32 accumulators
+constexpr int kTcNumBars = 2 * kTcStages + 5;
+constexpr int kTcSmemBytes = kTcStages * kTcStageBytes + 1024 + kTcNumBars * 8 + 16;
+
+__device__ __forceinline__ void tc_tile_coords(const Tf32x3Params& p, int tile, int& tm, int& tn) {
+  const int per_group = p.group_m * p.tiles_n;
+  const int g = tile / per_group;
+  const int first_m = g * p.group_m;
+  const int gsize = min(p.tiles_m - first_m, p.group_m);
+  const int r = tile - g * per_group;
+  tm = first_m + r % gsize;
+  tn = r / gsize;
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    sgemm_tf32x3_kernel(const __grid_constant__ Tf32x3Params p,
+                        const __grid_constant__ CUtensorMap mAhi,
+                        const __grid_constant__ CUtensorMap mAlo,
+                        const __grid_constant__ CUtensorMap mBhi,
+                        const __grid_constant__ CUtensorMap mBlo) {
+  extern __shared__ unsigned char smem_raw[];
+  // the 128-byte swizzle atoms need 1024-byte aligned tiles
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  unsigned char* gbase = smem_raw + (base - raw);
+  const uint32_t bars = base + kTcStages * kTcStageBytes;
+  auto full = [&](int s) { return bars + 8u * s; };
+  auto empty = [&](int s) { return bars + 8u * (kTcStages + s); };
+  auto tfull = [&](int a) { return bars + 8u * (2 * kTcStages + a); };
+  auto tempty = [&](int a) { return bars + 8u * (2 * kTcStages + 2 + a); };
+  const uint32_t drain = bars + 8u * (2 * kTcStages + 4);
+  uint32_t* tmem_slot =
+      reinterpret_cast<uint32_t*>(gbase + kTcStages * kTcStageBytes + kTcNumBars * 8);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kTcStages; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull(a), 1);
+      mbar_init(tempty(a), 4);  // one arrival per epilogue warp
+    }
+    mbar_init(drain, 1);
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tmem_slot), kTcTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const int total_tiles = p.tiles_m * p.tiles_n;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- copy issuer
+    if (lane == 0) {
+      prefetch_tmap(&mAhi);
+      prefetch_tmap(&mAlo);
+      prefetch_tmap(&mBhi);
+      prefetch_tmap(&mBlo);
+      int s = 0, issued = 0;
+      uint32_t ph = 0;
+      for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+        int tm, tn;
+        tc_tile_coords(p, tile, tm, tn);
+        const int m0 = tm * kTcBM, n0 = tn * kTcBN;
+        for (int kt = 0; kt < p.k_tiles; ++kt) {
+          if (p.debug_stop_ktile >= 0 && issued >= p.debug_stop_ktile) goto copies_done;
+          if (!mbar_wait(empty(s), ph ^ 1u, p.wait_limit_ns, p.status, kStatusTimeoutEmpty))
+            goto copies_done;
+          const uint32_t st = base + s * kTcStageBytes;
+          mbar_arrive_expect_tx(full(s), kTcStageBytes);
+          tma_load_2d(st, &mAhi, kt * kTcBK, m0, full(s));
+          tma_load_2d(st + kTcTileBytes, &mAlo, kt * kTcBK, m0, full(s));
+          tma_load_2d(st + 2 * kTcTileBytes, &mBhi, kt * kTcBK, n0, full(s));
+          tma_load_2d(st + 3 * kTcTileBytes, &mBlo, kt * kTcBK, n0, full(s));
+          ++issued;
+          if (++s == kTcStages) s = 0, ph ^= 1u;
+        }
+      }
+    copies_done:
+      // leave only after every copy started here has landed
+      for (int d = 0, pending = min(issued, kTcStages); d < pending; ++d) {
+        if (--s < 0) s = kTcStages - 1, ph ^= 1u;
+        if (!mbar_wait(full(s), ph, p.wait_limit_ns, p.status, kStatusTimeoutDrain)) break;
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_tf32(kTcBM, kTcBN);
+      int s = 0, a = 0;
+      uint32_t ph = 0, aph = 0;
+      for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+        if (!mbar_wait(tempty(a), aph ^ 1u, p.wait_limit_ns, p.status, kStatusTimeoutTmem))
+          goto mma_done;
+        tc_fence_after_sync();
+        const uint32_t d = tmem + (uint32_t)(a * kTcBN);
+        for (int kt = 0; kt < p.k_tiles; ++kt) {
+          if (!mbar_wait(full(s), ph, p.wait_limit_ns, p.status, kStatusTimeoutFull)) goto mma_done;
+          tc_fence_after_sync();
+          const uint32_t st = base + s * kTcStageBytes;
+#pragma unroll
+          for (int kk = 0; kk < kTcBK / 8; ++kk) {  // 8 TF32 = 32 bytes per K step
+            const uint32_t off = kk * 32u;
+            const uint64_t ahi = smem_desc_sw128_kmajor(st + off);
+            const uint64_t alo = smem_desc_sw128_kmajor(st + kTcTileBytes + off);
+            const uint64_t bhi = smem_desc_sw128_kmajor(st + 2 * kTcTileBytes + off);
+            const uint64_t blo = smem_desc_sw128_kmajor(st + 3 * kTcTileBytes + off);
+            mma_tf32(d, alo, bhi, idesc, (kt > 0 || kk > 0) ? 1u : 0u);
+            mma_tf32(d, ahi, blo, idesc, 1u);
+            mma_tf32(d, ahi, bhi, idesc, 1u);
+          }
+          mma_commit(empty(s));  // the stage is free once these MMAs have read it
+          if (++s == kTcStages) s = 0, ph ^= 1u;
+        }
+        mma_commit(tfull(a));  // the accumulator is final once every MMA is done
+        if (++a == 2) a = 0, aph ^= 1u;
+      }
+    mma_done:
+      // leave only after every MMA issued here has completed
+      mma_commit(drain);
+      mbar_wait(drain, 0, p.wait_limit_ns, p.status, kStatusTimeoutTmem);
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int q = warp & 3;  // tensor-memory lanes 32q .. 32q+31 belong to this warp
+    int a = 0;
+    uint32_t aph = 0;
+    const float alpha = p.alpha, beta = p.beta;
+    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+      int tm, tn;
+      tc_tile_coords(p, tile, tm, tn);
+      if (!mbar_wait(tfull(a), aph, p.wait_limit_ns, p.status, kStatusTimeoutTmem)) break;
+      tc_fence_after_sync();
+      const int r = tm * kTcBM + 32 * q + lane;
+      float* crow = p.C + (long long)r * p.ldc;
+#pragma unroll 1
+      for (int c = 0; c < kTcBN / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(a * kTcBN + 32 * c), v);
+        tmem_ld_wait();
+        if (r < p.M) {
+          const int n = tn * kTcBN + 32 * c;
+          if (p.c_vec4 && n + 31 < p.N) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+              float4 o;
+              const float a0 = __uint_as_float(v[j]), a1 = __uint_as_float(v[j + 1]);
+              const float a2 = __uint_as_float(v[j + 2]), a3 = __uint_as_float(v[j + 3]);
+              if (beta != 0.f) {
+                const float4 cv = *reinterpret_cast<const float4*>(crow + n + j);
+                o = make_float4(fmaf(alpha, a0, beta * cv.x), fmaf(alpha, a1, beta * cv.y),
+                                fmaf(alpha, a2, beta * cv.z), fmaf(alpha, a3, beta * cv.w));
+              } else {
+                o = make_float4(alpha * a0, alpha * a1, alpha * a2, alpha * a3);
+              }
+              *reinterpret_cast<float4*>(crow + n + j) = o;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if (n + j < p.N) {
+                float* qp = crow + n + j;
+                const float acc = __uint_as_float(v[j]);
+                *qp = (beta != 0.f) ? fmaf(alpha, acc, beta * *qp) : alpha * acc;
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty(a));
+      if (++a == 2) a = 0, aph ^= 1u;
+    }
+  }
+
+  // teardown: every role is done with tensor memory; warp 1 frees it
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTcTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------- launchers
+
+cudaError_t launch_split_a(const float* A, int M, int K, long long lda, float* Ahi, float* Alo,
+                           int num_sms, cudaStream_t stream) {
+  const long long total = (long long)M * (K / 4);
+  long long blocks = (total + 255) / 256;
+  const long long cap = (long long)num_sms * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  void* args[] = {(void*)&A, (void*)&M, (void*)&K, (void*)&lda, (void*)&Ahi, (void*)&Alo};
+  return cudaLaunchKernel(reinterpret_cast<const void*>(&split_a_kernel), dim3((unsigned)blocks),
+                          dim3(256), args, 0, stream);
+}
+
+cudaError_t launch_split_bt(const float* B, int K, int N, long long ldb, float* Bhi, float* Blo,
+                            cudaStream_t stream) {
+  const dim3 grid((unsigned)((N + 63) / 64), (unsigned)((K + 63) / 64));
+  void* args[] = {(void*)&B, (void*)&K, (void*)&N, (void*)&ldb, (void*)&Bhi, (void*)&Blo};
+  return cudaLaunchKernel(reinterpret_cast<const void*>(&split_bt_kernel), grid, dim3(256), args,
+                          0, stream);
+}
+
+cudaError_t launch_tf32x3(const Tf32x3Params& p, const CUtensorMap* maps, int num_sms,
+                          cudaStream_t stream) {
+  static std::atomic<int> configured[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!configured[dev].load(std::memory_order_acquire)) {
+    e = cudaFuncSetAttribute(sgemm_tf32x3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kTcSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured[dev].store(1, std::memory_order_release);
+  }
+  const long long tiles = (long long)p.tiles_m * p.tiles_n;
+  const int grid = (int)(tiles < num_sms ? tiles : num_sms);
+  Tf32x3Params pc = p;
+  CUtensorMap m0 = maps[0], m1 = maps[1], m2 = maps[2], m3 = maps[3];
+  void* args[] = {&pc, &m0, &m1, &m2, &m3};
+  return cudaLaunchKernel(reinterpret_cast<const void*>(&sgemm_tf32x3_kernel), dim3(grid),
+                          dim3(kTcThreads), args, kTcSmemBytes, stream);
+}
+
+}  // namespace b2g

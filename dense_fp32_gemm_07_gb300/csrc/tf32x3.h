@@ -1,0 +1,35 @@
+// tf32x3.h -- launchers of the 3xTF32 tensor-core SGEMM (tf32x3.cu).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace b2g {
+
+struct Tf32x3Params {
+  int M, N, K;
+  float alpha, beta;
+  float* C;
+  long long ldc;
+  int c_vec4;  // C 16-byte aligned and ldc % 4 == 0
+  int tiles_m, tiles_n, group_m, k_tiles;
+  unsigned long long wait_limit_ns;
+  int debug_stop_ktile;  // < 0 normally; >= 0 stops the copy issuer (timeout test)
+  unsigned int* status;
+};
+
+// Tile shape of the tensor-core kernel.
+constexpr int kTcBM = 128, kTcBN = 128, kTcBK = 32, kTcStages = 3;
+
+// A -> Ahi, Alo (M x K, ld K); B -> Bhi^T, Blo^T (N x K, ld K).  A, B 16-byte
+// aligned, lda % 4 == 0, K % 4 == 0.
+cudaError_t launch_split_a(const float* A, int M, int K, long long lda, float* Ahi, float* Alo,
+                           int num_sms, cudaStream_t stream);
+cudaError_t launch_split_bt(const float* B, int K, int N, long long ldb, float* Bhi, float* Blo,
+                            cudaStream_t stream);
+
+// The GEMM on the split operands.  maps: Ahi, Alo, Bhi^T, Blo^T as 2-D tensors
+// {K, rows} with 128-byte swizzle and boxes {32, 128}.
+cudaError_t launch_tf32x3(const Tf32x3Params& p, const CUtensorMap* maps, int num_sms,
+                          cudaStream_t stream);
+
+}  // namespace b2g

@@ -189,6 +189,25 @@ int b2g_set_wait_limit_ns(unsigned long long ns);
  */
 int b2g_debug_stop_after(int n);
 
+/*
+ * Row-major SGEMM on the 5th-generation tensor cores with the 3xTF32 split --
+ * a separate path from the FFMA entry points above, reported apart.  TF32 keeps
+ * a 10-bit mantissa (the handbook, section 接下来的优化方向, 使用 Tensor Core);
+ * each operand x is split into hi = x rounded to TF32 and lo = x - hi (exact in
+ * FP32), and alpha*(A_lo*B_hi + A_hi*B_lo + A_hi*B_hi) + beta*C is accumulated
+ * in FP32 (tcgen05.mma kind::tf32, accumulator in tensor memory).  The dropped
+ * A_lo*B_lo term and the rounding of lo are below 2^-21 |a||b| per product, so
+ * results stay inside the same elementwise bound the FFMA path is tested
+ * against for the shapes the tests cover.
+ *   Same arguments as b2g_sgemm.  Requires A 16-byte aligned and lda, K
+ *   multiples of 4 (else B2G_ERR_UNSUPPORTED); B and C may have any alignment.  Needs a workspace of
+ *   2*(M*K + N*K) floats for the split operands, taken from the library-owned
+ *   per-device workspace (see b2g_sgemm); while `stream` is being captured, or
+ *   when that workspace cannot be had, it returns B2G_ERR_UNSUPPORTED.
+ */
+int b2g_sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int lda, const float* B,
+                     int ldb, float beta, float* C, int ldc, void* stream);
+
 /* Static string for a B2G_* code. */
 const char* b2g_strerror(int code);
 

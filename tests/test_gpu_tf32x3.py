@@ -1,0 +1,132 @@
+"""The 3xTF32 tensor-core path (b2g_sgemm_3xtf32) against the oracle, within
+the same elementwise FP32 bound as the FFMA path."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from gpu_helpers import check, env, sample_entries
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tb():
+    return env()
+
+
+def run3(torch, b2g, A, B, C, alpha, beta):
+    M, K = A.shape
+    N = B.shape[1]
+    dA, dB, dC = (torch.from_numpy(np.ascontiguousarray(x)).cuda() for x in (A, B, C))
+    s = torch.cuda.current_stream().cuda_stream
+    rc = b2g.b2g_sgemm_3xtf32(M, N, K, alpha, dA.data_ptr(), K, dB.data_ptr(), N, beta,
+                              dC.data_ptr(), N, s)
+    torch.cuda.synchronize()
+    return rc, (dC.cpu().numpy() if rc == 0 else None)
+
+
+@pytest.mark.parametrize("shape", [(128, 128, 32), (128, 128, 64), (256, 128, 32), (128, 256, 96),
+                                   (1, 1, 4), (5, 7, 8), (37, 45, 52), (130, 257, 68),
+                                   (300, 200, 1024)])
+def test_shapes_within_bound(tb, shape):
+    torch, b2g = tb
+    M, N, K = shape
+    rng = np.random.default_rng(M + 3 * N + 7 * K)
+    A = rng.uniform(-1, 1, size=(M, K)).astype(np.float32)
+    B = rng.uniform(-1, 1, size=(K, N)).astype(np.float32)
+    C = rng.uniform(-1, 1, size=(M, N)).astype(np.float32)
+    ref, bound, _ = oracle.sgemm(A, B, C, 0.75, -1.25)
+    rc, got = run3(torch, b2g, A, B, C, 0.75, -1.25)
+    assert rc == 0, b2g.b2g_strerror(rc)
+    check(got, ref, bound, f"3xtf32 {shape}")
+
+
+def test_small_integers_bit_exact(tb):
+    """Integers up to 2^10 are TF32 values (lo = 0) and every partial sum stays
+    below 2^24, so the tensor-core result must be exact."""
+    torch, b2g = tb
+    rng = np.random.default_rng(5)
+    M, N, K = 200, 160, 512
+    A = rng.integers(-3, 4, size=(M, K)).astype(np.float32)
+    B = rng.integers(-3, 4, size=(K, N)).astype(np.float32)
+    C = rng.integers(-3, 4, size=(M, N)).astype(np.float32)
+    ref, _, _ = oracle.sgemm(A, B, C, 2.0, -1.0)
+    rc, got = run3(torch, b2g, A, B, C, 2.0, -1.0)
+    assert rc == 0
+    assert np.array_equal(got.astype(np.float64), ref)
+
+
+@pytest.mark.parametrize("name", ["square512", "sweep128", "sweep1024", "skinny16x4096x4096"])
+def test_workloads_full(tb, name):
+    torch, b2g = tb
+    w = workloads.WORKLOADS[name]
+    A, B, C = w.make()
+    ref, bound, _ = oracle.sgemm(A, B, C, w.alpha, w.beta)
+    rc, got = run3(torch, b2g, A, B, C, w.alpha, w.beta)
+    assert rc == 0
+    check(got, ref, bound, name)
+
+
+@pytest.mark.parametrize("name", ["square4096", "mlp8192x11008x4096"])
+def test_workloads_sampled(tb, name):
+    torch, b2g = tb
+    w = workloads.WORKLOADS[name]
+    A, B, C = w.make()
+    dA, dB, dC = (torch.from_numpy(x).cuda() for x in (A, B, C))
+    b2g.sgemm_3xtf32(dA, dB, dC, w.alpha, w.beta)
+    torch.cuda.synchronize()
+    rows, cols = sample_entries(w.M, w.N, seed=w.seed)
+    got = dC[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()].cpu().numpy()
+    ref, bound, _ = oracle.sgemm_entries(A, B, C, w.alpha, w.beta, rows, cols)
+    check(got, ref, bound, name)
+
+
+def test_unsupported_operands(tb):
+    torch, b2g = tb
+    w = workloads.WORKLOADS["ragged1000x1025x777"]  # lda = 777: not a multiple of 4
+    A, B, C = (torch.from_numpy(x).cuda() for x in w.make())
+    s = torch.cuda.current_stream().cuda_stream
+    rc = b2g.b2g_sgemm_3xtf32(w.M, w.N, w.K, w.alpha, A.data_ptr(), 777, B.data_ptr(), 1025,
+                              w.beta, C.data_ptr(), 1025, s)
+    assert rc == b2g.B2G_ERR_UNSUPPORTED
+
+
+def test_nonfinite_and_beta_zero(tb):
+    torch, b2g = tb
+    rng = np.random.default_rng(9)
+    A = rng.uniform(-1, 1, size=(130, 64)).astype(np.float32)
+    B = rng.uniform(-1, 1, size=(64, 140)).astype(np.float32)
+    A[100, 0] = np.nan
+    C = np.full((130, 140), np.nan, np.float32)  # beta == 0: C must not be read
+    ref, bound, _ = oracle.sgemm(A, B, C, 1.0, 0.0)
+    rc, got = run3(torch, b2g, A, B, C, 1.0, 0.0)
+    assert rc == 0
+    check(got, ref, bound, "nonfinite")
+    assert np.isnan(got[100]).all() and np.isfinite(np.delete(got, 100, axis=0)).all()
+
+
+def test_wait_runs_out_and_context_survives(tb):
+    torch, b2g = tb
+    rng = np.random.default_rng(0)
+    A = rng.uniform(-1, 1, size=(128, 128)).astype(np.float32)
+    B = rng.uniform(-1, 1, size=(128, 128)).astype(np.float32)
+    C = np.zeros((128, 128), np.float32)
+    s = torch.cuda.current_stream().cuda_stream
+    b2g.b2g_status(s, clear=True)
+    try:
+        b2g.b2g_set_wait_limit_ns(20_000_000)
+        b2g.b2g_debug_stop_after(1)  # 128 / 32 = 4 stages needed, 1 issued
+        rc, _ = run3(torch, b2g, A, B, C, 1.0, 0.0)
+        assert rc == 0
+        rc, flags = b2g.b2g_status(s, clear=True)
+        assert rc == b2g.B2G_ERR_TIMEOUT and flags, f"{flags:#x}"
+    finally:
+        b2g.b2g_debug_stop_after(-1)
+        b2g.b2g_set_wait_limit_ns(2_000_000_000)
+    ref, bound, _ = oracle.sgemm(A, B, C, 1.0, 0.0)
+    rc, got = run3(torch, b2g, A, B, C, 1.0, 0.0)
+    assert rc == 0
+    check(got, ref, bound, "after timeout")
