@@ -148,13 +148,15 @@ void ws_release(int dev, cudaStream_t st) {
   w.mu.unlock();
 }
 
-int num_plans() { return kNumPlansTMA + kNumPlansGeneral; }
+int num_plans() { return kNumPlansTMA + kNumPlansGeneral + kNumPlansSkinny; }
 
 const Plan* plan_at(int i) {
   if (i < 0) return nullptr;
   if (i < kNumPlansTMA) return &kPlansTMA[i];
   i -= kNumPlansTMA;
   if (i < kNumPlansGeneral) return &kPlansGeneral[i];
+  i -= kNumPlansGeneral;
+  if (i < kNumPlansSkinny) return &kPlansSkinny[i];
   return nullptr;
 }
 
@@ -203,6 +205,7 @@ int operand_class(const Call& c) {
 bool plan_accepts(const Plan& pl, const Call& c) {
   if (pl.feed == kFeedCpAsync) return true;
   const int cls = operand_class(c);
+  if (pl.feed == kFeedSkinny) return cls == kClassFast && c.M <= pl.BM && c.N % 4 == 0;
   if (pl.pretranspose) return cls == kClassFast;
   if (pl.feed == kFeedTMATrans || pl.alayout == kAKChunk) return cls == kClassFast;
   return cls == kClassFastTransA;
@@ -217,7 +220,7 @@ int select_plan(const Call& c, int* fallback = nullptr) {
     if (r.cls == cls && c.M >= r.m_min && c.M <= r.m_max && c.N >= r.n_min && c.N <= r.n_max &&
         mnk >= r.mnk_min && mnk < r.mnk_max) {
       const int i = plan_index(r.plan);
-      if (i >= 0) {
+      if (i >= 0 && plan_accepts(*plan_at(i), c)) {
         if (fallback) {
           const int f = r.fallback ? plan_index(r.fallback) : i;
           *fallback = f >= 0 ? f : i;
@@ -233,7 +236,47 @@ int select_plan(const Call& c, int* fallback = nullptr) {
 
 long long pre_ld(int M) { return ((long long)M + 3) / 4 * 4; }
 
-size_t pre_bytes(const Call& c) { return (size_t)c.K * (size_t)pre_ld(c.M) * sizeof(float); }
+// SMs and resident CTAs per SM of plan `pl` on the current device (152 and 4
+// when no device answers, as on a machine without a GPU).
+void skinny_capacity(const Plan& pl, int* sms, int* occ) {
+  *sms = 152, *occ = 4;
+  DeviceState* d = nullptr;
+  if (device_state(&d) == 0) {
+    *sms = d->sms;
+    const int o = pl.occupancy ? pl.occupancy() : 0;
+    if (o > 0) *occ = o;
+  }
+}
+
+// Split-K factor of the skinny plans: as many k splits per 128-column slab as
+// fill every resident CTA slot once (one wave), at least 64 k per split; *kc
+// receives the k extent of one split (a multiple of 16).
+int skinny_splits(const Plan& pl, const Call& c, int* kc) {
+  int sms = 0, occ = 0;
+  skinny_capacity(pl, &sms, &occ);
+  const long long slabs = (c.N + 127) / 128;
+  long long S = (long long)sms * occ / slabs;
+  const long long smax = c.K / 64 > 1 ? c.K / 64 : 1;
+  if (S > smax) S = smax;
+  if (S < 1) S = 1;
+  long long k = (c.K + S - 1) / S;
+  k = (k + 15) / 16 * 16;
+  *kc = (int)k;
+  return (int)((c.K + k - 1) / k);
+}
+
+// Workspace bytes plan `pl` wants for this call (0 when it needs none).
+size_t plan_work_bytes(const Plan& pl, const Call& c) {
+  if (pl.pretranspose) return (size_t)c.K * (size_t)pre_ld(c.M) * sizeof(float);
+  if (pl.feed == kFeedSkinny) {
+    int kc = 0;
+    const int S = skinny_splits(pl, c, &kc);
+    return S > 1 ? (size_t)S * c.M * c.N * sizeof(float) : 0;
+  }
+  return 0;
+}
+
+
 
 int encode_2d(CUtensorMap* m, const float* base, long long inner, long long outer,
               long long row_stride_elems, int box_inner, int box_outer) {
@@ -321,20 +364,21 @@ int run(const Call& c, int forced_plan, void* stream, void* user_ws = nullptr,
   cudaGetDevice(&dev);
   float* ws = nullptr;
   bool auto_ws = false;
-  if (pl->pretranspose) {
-    const size_t need = pre_bytes(c);
+  const size_t need = plan_work_bytes(*pl, c);
+  if (need) {
     if (user_ws && user_ws_bytes >= need && aligned16(user_ws)) {
       ws = static_cast<float*>(user_ws);
     } else if (allow_auto_ws) {
       ws = static_cast<float*>(ws_acquire(dev, st, need));
       auto_ws = ws != nullptr;
     }
-    if (!ws) {
+    if (!ws && pl->pretranspose) {
       if (forced_plan >= 0 || fallback < 0) return B2G_ERR_UNSUPPORTED;
       pi = fallback;
       pl = plan_at(pi);
       if (!pl || !plan_accepts(*pl, c) || pl->pretranspose) return B2G_ERR_UNSUPPORTED;
     }
+    // a skinny plan without a workspace runs unsplit
   }
 
   SgemmParams p;
@@ -350,9 +394,14 @@ int run(const Call& c, int forced_plan, void* stream, void* user_ws = nullptr,
   p.wait_limit_ns = g_wait_limit_ns.load();
   p.debug_stop_ktile = g_debug_stop.load();
   p.status = d->status;
+  p.work = nullptr, p.splits = 1, p.kc = c.K;
+  if (pl->feed == kFeedSkinny && ws) {
+    p.splits = skinny_splits(*pl, c, &p.kc);
+    p.work = ws;
+  }
 
   cudaError_t e = cudaSuccess;
-  if (ws) {  // At = A^T, then the kernel reads A stored K x M
+  if (ws && pl->pretranspose) {  // At = A^T, then the kernel reads A stored K x M
     const long long ldat = pre_ld(c.M);
     e = launch_transpose_a(c.A, c.M, c.K, c.lda, ws, ldat, st);
     p.A = ws, p.lda = ldat, p.transA = 1;
@@ -361,7 +410,7 @@ int run(const Call& c, int forced_plan, void* stream, void* user_ws = nullptr,
   CUtensorMap tmA, tmB;
   const CUtensorMap* pA = nullptr;
   const CUtensorMap* pB = nullptr;
-  if (e == cudaSuccess && pl->feed != kFeedCpAsync) {
+  if (e == cudaSuccess && pl->feed != kFeedCpAsync && pl->feed != kFeedSkinny) {
     if (pl->feed != kFeedTMA || pl->alayout == kAKChunk)
       rc = encode_a_kchunk(&tmA, p.A, c.M, c.K, (int)p.lda, pl->BM, pl->BK);
     else
@@ -477,7 +526,7 @@ int b2g_sgemm_workspace_size(int transA, int transB, int M, int N, int K, float 
   *bytes = 0;
   if (needs_gemm(c)) {
     const Plan* pl = plan_at(select_plan(c));
-    if (pl && pl->pretranspose) *bytes = pre_bytes(c);
+    if (pl) *bytes = plan_work_bytes(*pl, c);
   }
   return 0;
 }

@@ -430,7 +430,7 @@ cudaError_t launch_ffma(const SgemmParams& p, const CUtensorMap* tmA, const CUte
     NAME, BM, BN, BK, ST, TN, ALAY, FEED,                                                        \
         FfmaCfg<BM, BN, BK, WM, WN, TN, ST, ALAY, FEED, PW, ORD>::kThreads,                      \
         FfmaCfg<BM, BN, BK, WM, WN, TN, ST, ALAY, FEED, PW, ORD>::kSmemBytes,                    \
-        &launch_ffma<BM, BN, BK, WM, WN, TN, ST, ALAY, FEED, PW, ORD>, 0                         \
+        &launch_ffma<BM, BN, BK, WM, WN, TN, ST, ALAY, FEED, PW, ORD>, 0, nullptr                \
   }
 
 // The same kernel behind a transpose of row-major A into a workspace.
@@ -439,7 +439,7 @@ cudaError_t launch_ffma(const SgemmParams& p, const CUtensorMap* tmA, const CUte
     NAME, BM, BN, BK, ST, TN, kAKMajor, kFeedTMA,                                                \
         FfmaCfg<BM, BN, BK, WM, WN, TN, ST, kAKMajor, kFeedTMA, PW, ORD>::kThreads,              \
         FfmaCfg<BM, BN, BK, WM, WN, TN, ST, kAKMajor, kFeedTMA, PW, ORD>::kSmemBytes,            \
-        &launch_ffma<BM, BN, BK, WM, WN, TN, ST, kAKMajor, kFeedTMA, PW, ORD>, 1                 \
+        &launch_ffma<BM, BN, BK, WM, WN, TN, ST, kAKMajor, kFeedTMA, PW, ORD>, 1, nullptr        \
   }
 
 }  // namespace b2g

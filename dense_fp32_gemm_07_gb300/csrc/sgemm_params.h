@@ -23,6 +23,9 @@ struct SgemmParams {
   unsigned long long wait_limit_ns;  // bound on every mbarrier wait
   int debug_stop_ktile;              // < 0 normally; >= 0 stops the producer (timeout test)
   unsigned int* status;              // device status word (timeout flags)
+  float* work;                       // split-K partial sums (skinny plans), or null
+  int splits;                        // split-K factor (skinny plans); 1 = no split
+  int kc;                            // k extent of one split (skinny plans)
 };
 
 // How A is laid out in one shared-memory stage.
@@ -37,6 +40,7 @@ enum Feed : int {
   kFeedCpAsync = 1,  // producer warps issue 4-byte cp.async with zero fill (any layout)
   kFeedTMATrans = 2,  // bulk-tensor copies; A lands k-chunked in a staging slot and the
                       // consumer warps rewrite it transposed ([BK][BM]) a few stages ahead
+  kFeedSkinny = 3,    // skinny-M split-K kernel: B streamed from global, A staged per k slab
 };
 
 constexpr int kMaxDevices = 64;
@@ -56,7 +60,15 @@ struct Plan {
   LaunchFn launch;
   int pretranspose;  // 1: row-major A is first transposed into a workspace, then this
                      // plan's kernel (which reads A stored K x M) runs on it
+  int (*occupancy)();  // CTAs of this plan resident per SM on the current device (0 on
+                       // failure); set for plans whose host side sizes a split by it
 };
+
+// Skinny-M plans (M <= BM), compiled in skinny.cu.
+extern const Plan kPlansSkinny[];
+extern const int kNumPlansSkinny;
+// C = alpha * sum_s P[s] + beta * C over the M x N window (split-K reduction).
+cudaError_t launch_splitk_reduce(const SgemmParams& p, cudaStream_t stream, int num_sms);
 
 // Plans compiled in each kernel translation unit.
 extern const Plan kPlansTMA[];

@@ -28,8 +28,11 @@ constexpr int kInf = 0x7fffffff;
 // (128^3 .. 8192^3), the 8192x11008x4096 and 16x4096x4096 shapes and the
 // ragged 1000x1025x777 shape.
 const TuneRule kTuneTable[] = {
-    // skinny M: too few row tiles to fill 152 SMs with any plan here (split-K
-    // would be the remedy); the k-chunked plan needs no workspace
+    // skinny M: split-K over B streamed from global memory (N % 4 == 0)
+    {kClassFast, 0, 8, 0, kInf, 0, "skinny_m8", nullptr},
+    {kClassFast, 9, 16, 0, kInf, 0, "skinny_m16", nullptr},
+    {kClassFast, 17, 32, 0, kInf, 0, "skinny_m32", nullptr},
+    // other small M: too few row tiles to fill 152 SMs with the tiled plans
     {kClassFast, 0, 48, 0, kInf, 0, "tma_64x128x16_s6_o1", nullptr},
     // up to ~1.3e9 multiply-adds the transpose costs more than it saves
     {kClassFast, 49, kInf, 0, kInf, 0, "tma_64x128x16_s6_o2", nullptr, 2.0e9},

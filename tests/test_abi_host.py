@@ -53,7 +53,7 @@ def test_version_and_plans(b2g):
         info = b2g.b2g_plan_info(i)
         assert info["BM"] > 0 and info["BN"] > 0 and info["BK"] % 4 == 0
         assert info["threads"] % 32 == 0 and info["smem_bytes"] <= 227 * 1024
-        assert n.startswith(("tma", "gen", "pre"))
+        assert n.startswith(("tma", "gen", "pre", "skinny"))
     assert b2g.b2g_plan_name(len(names)) is None
     with pytest.raises(b2g.B2GError):
         b2g.b2g_plan_info(-1)
@@ -104,7 +104,10 @@ def _plan(b2g, *a):
 def test_tune_table_classes(b2g):
     # aligned, ld % 4 == 0, K % 4 == 0 -> bulk-tensor plans; large ones pre-transpose A
     assert _plan(b2g, 0, 0, 4096, 4096, 4096, 1.0, FAKE, 4096, FAKE, 4096, FAKE, 4096).startswith("pre_")
-    assert _plan(b2g, 0, 0, 16, 4096, 4096, 1.0, FAKE, 4096, FAKE, 4096, FAKE, 4096).startswith("tma_")
+    assert _plan(b2g, 0, 0, 16, 4096, 4096, 1.0, FAKE, 4096, FAKE, 4096, FAKE, 4096) == "skinny_m16"
+    assert _plan(b2g, 0, 0, 32, 4096, 4096, 1.0, FAKE, 4096, FAKE, 4096, FAKE, 4096) == "skinny_m32"
+    # skinny M with N % 4 != 0 takes a tiled plan
+    assert _plan(b2g, 0, 0, 16, 4095, 4096, 1.0, FAKE, 4096, FAKE, 4096, FAKE, 4096).startswith("tma_")
     assert _plan(b2g, 0, 0, 64, 64, 64, 1.0, FAKE, 64, FAKE, 64, FAKE, 64).startswith("tma_")
     # odd leading dimension -> 4-byte feed
     assert _plan(b2g, 0, 0, 1000, 1025, 777, 0.75, FAKE, 777, FAKE, 1025, FAKE, 1025).startswith("gen_")
@@ -126,6 +129,10 @@ def test_workspace_size_query(b2g):
     assert rc == 0 and n == 4096 * 1004 * 4
     rc, n = b2g.b2g_sgemm_workspace_size(0, 0, 64, 64, 64, 1.0, FAKE, 64, FAKE, 64, FAKE, 64)
     assert rc == 0 and n == 0
+    # skinny: split-K partial sums, S x M x N floats for some S > 1
+    rc, n = b2g.b2g_sgemm_workspace_size(0, 0, 16, 4096, 4096, 1.0, FAKE, 4096, FAKE, 4096,
+                                         FAKE, 4096)
+    assert rc == 0 and n > 0 and n % (16 * 4096 * 4) == 0
     rc, n = b2g.b2g_sgemm_workspace_size(0, 0, 64, 64, 64, 1.0, FAKE, 63, FAKE, 64, FAKE, 64)
     assert rc == -2
     assert b2g.b2g_release_workspaces() == 0  # nothing allocated yet: no CUDA call needed
