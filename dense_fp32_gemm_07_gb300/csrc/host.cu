@@ -206,7 +206,8 @@ bool plan_accepts(const Plan& pl, const Call& c) {
   if (pl.feed == kFeedCpAsync) return true;
   const int cls = operand_class(c);
   if (pl.feed == kFeedSkinny) return cls == kClassFast && c.M <= pl.BM && c.N % 4 == 0;
-  if (pl.pretranspose) return cls == kClassFast;
+  if (pl.pretranspose == 2) return true;  // packing accepts any operands
+  if (pl.pretranspose == 1) return cls == kClassFast;
   if (pl.feed == kFeedTMATrans || pl.alayout == kAKChunk) return cls == kClassFast;
   return cls == kClassFastTransA;
 }
@@ -267,7 +268,9 @@ int skinny_splits(const Plan& pl, const Call& c, int* kc) {
 
 // Workspace bytes plan `pl` wants for this call (0 when it needs none).
 size_t plan_work_bytes(const Plan& pl, const Call& c) {
-  if (pl.pretranspose) return (size_t)c.K * (size_t)pre_ld(c.M) * sizeof(float);
+  if (pl.pretranspose == 1) return (size_t)c.K * (size_t)pre_ld(c.M) * sizeof(float);
+  if (pl.pretranspose == 2)
+    return (size_t)c.K * (size_t)(pre_ld(c.M) + pre_ld(c.N)) * sizeof(float);
   if (pl.feed == kFeedSkinny) {
     int kc = 0;
     const int S = skinny_splits(pl, c, &kc);
@@ -401,10 +404,18 @@ int run(const Call& c, int forced_plan, void* stream, void* user_ws = nullptr,
   }
 
   cudaError_t e = cudaSuccess;
-  if (ws && pl->pretranspose) {  // At = A^T, then the kernel reads A stored K x M
+  if (ws && pl->pretranspose == 1) {  // At = A^T, then the kernel reads A stored K x M
     const long long ldat = pre_ld(c.M);
     e = launch_transpose_a(c.A, c.M, c.K, c.lda, ws, ldat, st);
     p.A = ws, p.lda = ldat, p.transA = 1;
+  } else if (ws && pl->pretranspose == 2) {  // At = op(A)^T and Bp = op(B), both aligned
+    const long long ldat = pre_ld(c.M), ldbp = pre_ld(c.N);
+    float* At = ws;
+    float* Bp = ws + (size_t)c.K * ldat;
+    e = launch_pack(c.A, c.lda, c.transA ? 0 : 1, c.K, c.M, At, ldat, st);
+    if (e == cudaSuccess) e = launch_pack(c.B, c.ldb, c.transB ? 1 : 0, c.K, c.N, Bp, ldbp, st);
+    p.A = At, p.lda = ldat, p.transA = 1;
+    p.B = Bp, p.ldb = ldbp, p.transB = 0;
   }
 
   CUtensorMap tmA, tmB;
@@ -415,7 +426,7 @@ int run(const Call& c, int forced_plan, void* stream, void* user_ws = nullptr,
       rc = encode_a_kchunk(&tmA, p.A, c.M, c.K, (int)p.lda, pl->BM, pl->BK);
     else
       rc = encode_2d(&tmA, p.A, c.M, c.K, p.lda, pl->BM, pl->BK);  // A stored K x M
-    if (!rc) rc = encode_2d(&tmB, c.B, c.N, c.K, c.ldb, pl->BN, pl->BK);
+    if (!rc) rc = encode_2d(&tmB, p.B, c.N, c.K, p.ldb, pl->BN, pl->BK);
     pA = &tmA, pB = &tmB;
   }
   if (e == cudaSuccess && !rc) e = pl->launch(p, pA, pB, d->sms, st);

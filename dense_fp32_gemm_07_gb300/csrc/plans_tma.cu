@@ -28,8 +28,11 @@ const Plan kPlansTMA[] = {
     B2G_FFMA_PLAN("tmaT_128x128x16_s6_o1", 128, 128, 16, 4, 2, 8, 6, kAKMajor, kFeedTMA, 1, 1),
     B2G_FFMA_PLAN("tmaT_64x128x16_s6", 64, 128, 16, 2, 2, 8, 6, kAKMajor, kFeedTMA, 1, 0),
     // row-major A: transposed into a workspace first, then the kernels above
-    B2G_FFMA_PLAN_PRE("pre_128x128x16_s6_o1", 128, 128, 16, 4, 2, 8, 6, 1, 1),
-    B2G_FFMA_PLAN_PRE("pre_64x128x16_s6", 64, 128, 16, 2, 2, 8, 6, 1, 0),
+    B2G_FFMA_PLAN_PRE("pre_128x128x16_s6_o1", 128, 128, 16, 4, 2, 8, 6, 1, 1, 1),
+    B2G_FFMA_PLAN_PRE("pre_64x128x16_s6", 64, 128, 16, 2, 2, 8, 6, 1, 0, 1),
+    // any operands: A^T and B packed aligned into a workspace first
+    B2G_FFMA_PLAN_PRE("pack_128x128x16_s6_o1", 128, 128, 16, 4, 2, 8, 6, 1, 1, 2),
+    B2G_FFMA_PLAN_PRE("pack_64x128x16_s6", 64, 128, 16, 2, 2, 8, 6, 1, 0, 2),
 };
 const int kNumPlansTMA = sizeof(kPlansTMA) / sizeof(kPlansTMA[0]);
 

@@ -433,13 +433,14 @@ cudaError_t launch_ffma(const SgemmParams& p, const CUtensorMap* tmA, const CUte
         &launch_ffma<BM, BN, BK, WM, WN, TN, ST, ALAY, FEED, PW, ORD>, 0, nullptr                \
   }
 
-// The same kernel behind a transpose of row-major A into a workspace.
-#define B2G_FFMA_PLAN_PRE(NAME, BM, BN, BK, WM, WN, TN, ST, PW, ORD)                              \
+// The same kernel behind a transpose of row-major A (PRE = 1) or a packing of
+// both operands (PRE = 2) into a workspace.
+#define B2G_FFMA_PLAN_PRE(NAME, BM, BN, BK, WM, WN, TN, ST, PW, ORD, PRE)                         \
   Plan {                                                                                         \
     NAME, BM, BN, BK, ST, TN, kAKMajor, kFeedTMA,                                                \
         FfmaCfg<BM, BN, BK, WM, WN, TN, ST, kAKMajor, kFeedTMA, PW, ORD>::kThreads,              \
         FfmaCfg<BM, BN, BK, WM, WN, TN, ST, kAKMajor, kFeedTMA, PW, ORD>::kSmemBytes,            \
-        &launch_ffma<BM, BN, BK, WM, WN, TN, ST, kAKMajor, kFeedTMA, PW, ORD>, 1, nullptr        \
+        &launch_ffma<BM, BN, BK, WM, WN, TN, ST, kAKMajor, kFeedTMA, PW, ORD>, PRE, nullptr      \
   }
 
 }  // namespace b2g

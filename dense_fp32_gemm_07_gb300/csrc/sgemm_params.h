@@ -59,7 +59,9 @@ struct Plan {
   int smem_bytes;
   LaunchFn launch;
   int pretranspose;  // 1: row-major A is first transposed into a workspace, then this
-                     // plan's kernel (which reads A stored K x M) runs on it
+                     // plan's kernel (which reads A stored K x M) runs on it; 2: both
+                     // operands are packed into a workspace first (A^T and B, aligned,
+                     // from any alignment, leading dimension or op() flags)
   int (*occupancy)();  // CTAs of this plan resident per SM on the current device (0 on
                        // failure); set for plans whose host side sizes a split by it
 };

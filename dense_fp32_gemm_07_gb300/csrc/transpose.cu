@@ -63,3 +63,50 @@ cudaError_t launch_transpose_a(const float* A, int M, int K, long long lda, floa
 }
 
 }  // namespace b2g
+
+namespace b2g {
+
+// out (R x Cc, row-major, leading dimension ldo) = trans ? in^T : in, where in
+// is read element by element (any alignment, any leading dimension):
+//   trans == 0: out[r][c] = in[r * ld + c]
+//   trans != 0: out[r][c] = in[c * ld + r]
+// 32 x 32 tiles through shared memory (rows padded to 33: no bank conflicts),
+// coalesced on both sides in either direction.
+__global__ void __launch_bounds__(256) pack_kernel(const float* __restrict__ in, long long ld,
+                                                   int trans, int R, int Cc,
+                                                   float* __restrict__ out, long long ldo) {
+  __shared__ float tile[32][33];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+  const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
+  if (trans) {
+    // read in rows (c0 + i), columns r0 + tx: coalesced along r
+#pragma unroll
+    for (int i = ty; i < 32; i += 8) {
+      const int c = c0 + i, r = r0 + tx;
+      tile[i][tx] = (c < Cc && r < R) ? in[(long long)c * ld + r] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = ty; i < 32; i += 8) {
+      const int r = r0 + i, c = c0 + tx;
+      if (r < R && c < Cc) out[(long long)r * ldo + c] = tile[tx][i];
+    }
+  } else {
+#pragma unroll
+    for (int i = ty; i < 32; i += 8) {
+      const int r = r0 + i, c = c0 + tx;
+      if (r < R && c < Cc) out[(long long)r * ldo + c] = in[(long long)r * ld + c];
+    }
+  }
+}
+
+cudaError_t launch_pack(const float* in, long long ld, int trans, int R, int Cc, float* out,
+                        long long ldo, cudaStream_t stream) {
+  const dim3 grid((unsigned)((Cc + 31) / 32), (unsigned)((R + 31) / 32));
+  void* args[] = {(void*)&in, (void*)&ld, (void*)&trans, (void*)&R, (void*)&Cc, (void*)&out,
+                  (void*)&ldo};
+  return cudaLaunchKernel(reinterpret_cast<const void*>(&pack_kernel), grid, dim3(256), args, 0,
+                          stream);
+}
+
+}  // namespace b2g

@@ -10,4 +10,10 @@ namespace b2g {
 cudaError_t launch_transpose_a(const float* A, int M, int K, long long lda, float* At,
                                long long ldat, cudaStream_t stream);
 
+// out (R x Cc, leading dimension ldo) = trans ? in^T : in, in read element by
+// element: any alignment and leading dimension ld.  Grid-limited to R and Cc
+// below 2^31 / 32 tiles.
+cudaError_t launch_pack(const float* in, long long ld, int trans, int R, int Cc, float* out,
+                        long long ldo, cudaStream_t stream);
+
 }  // namespace b2g

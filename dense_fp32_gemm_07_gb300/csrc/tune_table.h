@@ -45,6 +45,13 @@ const TuneRule kTuneTable[] = {
     {kClassFastTransA, 0, kInf, 0, kInf, 0, "tmaT_64x128x16_s6", nullptr, 2.5e10},
     {kClassFastTransA, 0, kInf, 0, kInf, 2.5e10, "tmaT_64x128x16_s6", nullptr, 4.0e11},
     {kClassFastTransA, 0, kInf, 0, kInf, 4.0e11, "tmaT_128x128x16_s6_o1", nullptr},
+    // anything else (misaligned pointers, odd leading dimensions, K % 4 != 0,
+    // op(B) = B^T): pack A^T and B aligned into the workspace, then the
+    // transposed-layout kernel; the 4-byte feed needs no workspace
+    {kClassGeneral, 0, kInf, 0, kInf, 5.0e7, "pack_64x128x16_s6", "gen_64x64x16_s4", 2.0e9},
+    {kClassGeneral, 0, kInf, 0, kInf, 2.0e9, "pack_128x128x16_s6_o1", "gen_64x64x16_s4", 2.5e10},
+    {kClassGeneral, 0, kInf, 0, kInf, 2.5e10, "pack_64x128x16_s6", "gen_64x64x16_s4", 4.0e11},
+    {kClassGeneral, 0, kInf, 0, kInf, 4.0e11, "pack_128x128x16_s6_o1", "gen_64x64x16_s4"},
     {kClassGeneral, 0, kInf, 0, kInf, 0, "gen_64x64x16_s4", nullptr},
 };
 

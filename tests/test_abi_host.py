@@ -53,7 +53,7 @@ def test_version_and_plans(b2g):
         info = b2g.b2g_plan_info(i)
         assert info["BM"] > 0 and info["BN"] > 0 and info["BK"] % 4 == 0
         assert info["threads"] % 32 == 0 and info["smem_bytes"] <= 227 * 1024
-        assert n.startswith(("tma", "gen", "pre", "skinny"))
+        assert n.startswith(("tma", "gen", "pre", "pack", "skinny"))
     assert b2g.b2g_plan_name(len(names)) is None
     with pytest.raises(b2g.B2GError):
         b2g.b2g_plan_info(-1)
@@ -109,15 +109,17 @@ def test_tune_table_classes(b2g):
     # skinny M with N % 4 != 0 takes a tiled plan
     assert _plan(b2g, 0, 0, 16, 4095, 4096, 1.0, FAKE, 4096, FAKE, 4096, FAKE, 4096).startswith("tma_")
     assert _plan(b2g, 0, 0, 64, 64, 64, 1.0, FAKE, 64, FAKE, 64, FAKE, 64).startswith("tma_")
-    # odd leading dimension -> 4-byte feed
-    assert _plan(b2g, 0, 0, 1000, 1025, 777, 0.75, FAKE, 777, FAKE, 1025, FAKE, 1025).startswith("gen_")
-    # misaligned base pointer -> 4-byte feed
-    assert _plan(b2g, 0, 0, 512, 512, 512, 1.0, FAKE + 4, 512, FAKE, 512, FAKE, 512).startswith("gen_")
-    # K not a multiple of 4 -> 4-byte feed
-    assert _plan(b2g, 0, 0, 512, 512, 510, 1.0, FAKE, 512, FAKE, 512, FAKE, 512).startswith("gen_")
-    # op(A) = A^T aligned -> transposed-layout bulk-tensor plan; op(B) = B^T -> 4-byte feed
+    # odd leading dimension -> operands packed into the workspace first
+    assert _plan(b2g, 0, 0, 1000, 1025, 777, 0.75, FAKE, 777, FAKE, 1025, FAKE, 1025).startswith("pack_")
+    # misaligned base pointer -> packed
+    assert _plan(b2g, 0, 0, 512, 512, 512, 1.0, FAKE + 4, 512, FAKE, 512, FAKE, 512).startswith("pack_")
+    # K not a multiple of 4 -> packed
+    assert _plan(b2g, 0, 0, 512, 512, 510, 1.0, FAKE, 512, FAKE, 512, FAKE, 512).startswith("pack_")
+    # small general problems -> 4-byte feed (no workspace)
+    assert _plan(b2g, 0, 0, 64, 64, 63, 1.0, FAKE, 64, FAKE, 64, FAKE, 64).startswith("gen_")
+    # op(A) = A^T aligned -> transposed-layout bulk-tensor plan; op(B) = B^T -> packed
     assert _plan(b2g, 1, 0, 512, 512, 512, 1.0, FAKE, 512, FAKE, 512, FAKE, 512).startswith("tmaT_")
-    assert _plan(b2g, 0, 1, 512, 512, 512, 1.0, FAKE, 512, FAKE, 512, FAKE, 512).startswith("gen_")
+    assert _plan(b2g, 0, 1, 512, 512, 512, 1.0, FAKE, 512, FAKE, 512, FAKE, 512).startswith("pack_")
 
 
 def test_workspace_size_query(b2g):
@@ -135,6 +137,10 @@ def test_workspace_size_query(b2g):
     assert rc == 0 and n > 0 and n % (16 * 4096 * 4) == 0
     rc, n = b2g.b2g_sgemm_workspace_size(0, 0, 64, 64, 64, 1.0, FAKE, 63, FAKE, 64, FAKE, 64)
     assert rc == -2
+    # packing: A^T (K x round_up(M, 4)) and B (K x round_up(N, 4))
+    rc, n = b2g.b2g_sgemm_workspace_size(0, 0, 1000, 1025, 777, 1.0, FAKE, 777, FAKE, 1025,
+                                         FAKE, 1025)
+    assert rc == 0 and n == 777 * (1000 + 1028) * 4
     assert b2g.b2g_release_workspaces() == 0  # nothing allocated yet: no CUDA call needed
 
 
