@@ -36,7 +36,7 @@ B2G_ERR_SCRATCH_LIMIT = -11
 EXPORTS = (
     "b2g_sgemm", "b2g_sgemm_ex", "b2g_sgemm_with_plan", "b2g_sgemm_select_plan",
     "b2g_sgemm_ws", "b2g_sgemm_workspace_size", "b2g_release_workspaces", "b2g_sgemm_noalloc",
-    "b2g_sgemm_3xtf32",
+    "b2g_sgemm_3xtf32", "b2g_sgemm_strided_batched",
     "b2g_plan_count", "b2g_plan_name", "b2g_plan_info", "b2g_status", "b2g_set_wait_limit_ns",
     "b2g_debug_stop_after", "b2g_strerror", "b2g_version",
 )
@@ -74,6 +74,9 @@ def _load():
         lib.b2g_release_workspaces.argtypes = []
         lib.b2g_sgemm_noalloc.argtypes = gemm
         lib.b2g_sgemm_3xtf32.argtypes = gemm
+        ll = ctypes.c_longlong
+        lib.b2g_sgemm_strided_batched.argtypes = [i, i, i, i, i, f, vp, i, ll, vp, i, ll, f, vp,
+                                                  i, ll, i, vp]
         lib.b2g_plan_count.argtypes = []
         lib.b2g_plan_name.argtypes = [i]
         lib.b2g_plan_name.restype = ctypes.c_char_p
@@ -156,6 +159,43 @@ def sgemm_3xtf32(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):
         raise ValueError("shape mismatch")
     rc = b2g_sgemm_3xtf32(M, N, K, float(alpha), A.data_ptr(), lda, B.data_ptr(), ldb,
                           float(beta), C.data_ptr(), ldc, _stream_handle(stream))
+    if rc:
+        raise B2GError(rc)
+    return C
+
+
+def b2g_sgemm_strided_batched(transA, transB, M, N, K, alpha, A, lda, strideA, B, ldb, strideB,
+                              beta, C, ldc, strideC, batch, stream=0) -> int:
+    return _load().b2g_sgemm_strided_batched(transA, transB, M, N, K, alpha, A, lda, strideA, B,
+                                             ldb, strideB, beta, C, ldc, strideC, batch, stream)
+
+
+def sgemm_batched(A, B, C, alpha: float = 1.0, beta: float = 0.0, transA: bool = False,
+                  transB: bool = False, stream=None):
+    """C[b] <- alpha * op(A[b]) @ op(B[b]) + beta * C[b] for 3-D float32 CUDA
+    tensors (batch first; each matrix row-major with unit column stride)."""
+    import torch
+
+    for t, name in ((A, "A"), (B, "B"), (C, "C")):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or t.dim() != 3 or not t.is_cuda:
+            raise TypeError(f"{name} must be a 3-D float32 CUDA tensor")
+        if t.size(2) > 1 and t.stride(2) != 1:
+            raise ValueError(f"{name} must have unit column stride")
+    batch = A.size(0)
+    if B.size(0) != batch or C.size(0) != batch:
+        raise ValueError("batch sizes differ")
+    M, K = (A.size(2), A.size(1)) if transA else (A.size(1), A.size(2))
+    Kb, N = (B.size(2), B.size(1)) if transB else (B.size(1), B.size(2))
+    if Kb != K or tuple(C.shape[1:]) != (M, N):
+        raise ValueError("shape mismatch")
+
+    def ld(t):
+        return max(1, t.stride(1)) if t.size(1) > 1 else max(1, t.size(2))
+
+    rc = b2g_sgemm_strided_batched(int(transA), int(transB), M, N, K, float(alpha), A.data_ptr(),
+                                   ld(A), A.stride(0), B.data_ptr(), ld(B), B.stride(0),
+                                   float(beta), C.data_ptr(), ld(C), C.stride(0), batch,
+                                   _stream_handle(stream))
     if rc:
         raise B2GError(rc)
     return C

@@ -27,12 +27,15 @@ __device__ unsigned int g_status_word;
 
 // C = beta * C over an M x N window with leading dimension ldc (beta == 0 writes
 // zeros without reading C).  Used when the product term vanishes.
-__global__ void scale_c_kernel(int M, int N, float beta, float* __restrict__ C, long long ldc) {
-  const long long total = (long long)M * N;
+__global__ void scale_c_kernel(int M, int N, float beta, float* __restrict__ C, long long ldc,
+                               int batch, long long strideC) {
+  const long long per = (long long)M * N;
+  const long long total = per * batch;
   for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
        idx += (long long)gridDim.x * blockDim.x) {
-    const long long i = idx / N, j = idx - i * N;
-    float* q = C + i * ldc + j;
+    const long long b = idx / per, r = idx - b * per;
+    const long long i = r / N, j = r - i * N;
+    float* q = C + b * strideC + i * ldc + j;
     *q = (beta == 0.f) ? 0.f : beta * *q;
   }
 }
@@ -177,26 +180,32 @@ struct Call {
   int ldb;
   float* C;
   int ldc;
+  int batch = 1;  // independent problems, operands advancing by the strides (elements)
+  long long strideA = 0, strideB = 0, strideC = 0;
 };
 
 // 0 when the arguments are valid, else the B2G_ERR_* code.
 int validate(const Call& c) {
-  if (c.M < 0 || c.N < 0 || c.K < 0) return B2G_ERR_INVALID_DIM;
+  if (c.M < 0 || c.N < 0 || c.K < 0 || c.batch < 0) return B2G_ERR_INVALID_DIM;
+  if (c.strideA < 0 || c.strideB < 0 || c.strideC < 0) return B2G_ERR_INVALID_LD;
   const int a_cols = c.transA ? c.M : c.K;
   const int b_cols = c.transB ? c.K : c.N;
   if (c.lda < (a_cols > 1 ? a_cols : 1) || c.ldb < (b_cols > 1 ? b_cols : 1) ||
       c.ldc < (c.N > 1 ? c.N : 1))
     return B2G_ERR_INVALID_LD;
-  if (c.M == 0 || c.N == 0) return 0;
+  if (c.M == 0 || c.N == 0 || c.batch == 0) return 0;
   if (c.C == nullptr) return B2G_ERR_NULL;
   if (c.K > 0 && c.alpha != 0.f && (c.A == nullptr || c.B == nullptr)) return B2G_ERR_NULL;
   return 0;
 }
 
-bool needs_gemm(const Call& c) { return c.M > 0 && c.N > 0 && c.K > 0 && c.alpha != 0.f; }
+bool needs_gemm(const Call& c) {
+  return c.M > 0 && c.N > 0 && c.K > 0 && c.batch > 0 && c.alpha != 0.f;
+}
 
 int operand_class(const Call& c) {
-  const bool ab_aligned = aligned16(c.A) && aligned16(c.B) && c.lda % 4 == 0 && c.ldb % 4 == 0;
+  const bool ab_aligned = aligned16(c.A) && aligned16(c.B) && c.lda % 4 == 0 && c.ldb % 4 == 0 &&
+                          (c.batch <= 1 || (c.strideA % 4 == 0 && c.strideB % 4 == 0));
   if (!ab_aligned || c.transB) return kClassGeneral;
   if (c.transA) return kClassFastTransA;
   return c.K % 4 == 0 ? kClassFast : kClassGeneral;
@@ -205,7 +214,8 @@ int operand_class(const Call& c) {
 bool plan_accepts(const Plan& pl, const Call& c) {
   if (pl.feed == kFeedCpAsync) return true;
   const int cls = operand_class(c);
-  if (pl.feed == kFeedSkinny) return cls == kClassFast && c.M <= pl.BM && c.N % 4 == 0;
+  if (pl.feed == kFeedSkinny)
+    return cls == kClassFast && c.M <= pl.BM && c.N % 4 == 0 && c.batch <= 65535;
   if (pl.pretranspose == 2) return true;  // packing accepts any operands
   if (pl.pretranspose == 1) return cls == kClassFast;
   if (pl.feed == kFeedTMATrans || pl.alayout == kAKChunk) return cls == kClassFast;
@@ -255,7 +265,7 @@ void skinny_capacity(const Plan& pl, int* sms, int* occ) {
 int skinny_splits(const Plan& pl, const Call& c, int* kc) {
   int sms = 0, occ = 0;
   skinny_capacity(pl, &sms, &occ);
-  const long long slabs = (c.N + 127) / 128;
+  const long long slabs = (c.N + 127) / 128 * (c.batch > 0 ? c.batch : 1);
   long long S = (long long)sms * occ / slabs;
   const long long smax = c.K / 64 > 1 ? c.K / 64 : 1;
   if (S > smax) S = smax;
@@ -268,28 +278,33 @@ int skinny_splits(const Plan& pl, const Call& c, int* kc) {
 
 // Workspace bytes plan `pl` wants for this call (0 when it needs none).
 size_t plan_work_bytes(const Plan& pl, const Call& c) {
-  if (pl.pretranspose == 1) return (size_t)c.K * (size_t)pre_ld(c.M) * sizeof(float);
+  const size_t nb = (size_t)(c.batch > 0 ? c.batch : 0);
+  if (pl.pretranspose == 1) return nb * (size_t)c.K * (size_t)pre_ld(c.M) * sizeof(float);
   if (pl.pretranspose == 2)
-    return (size_t)c.K * (size_t)(pre_ld(c.M) + pre_ld(c.N)) * sizeof(float);
+    return nb * (size_t)c.K * (size_t)(pre_ld(c.M) + pre_ld(c.N)) * sizeof(float);
   if (pl.feed == kFeedSkinny) {
     int kc = 0;
     const int S = skinny_splits(pl, c, &kc);
-    return S > 1 ? (size_t)S * c.M * c.N * sizeof(float) : 0;
+    return S > 1 ? nb * (size_t)S * c.M * c.N * sizeof(float) : 0;
   }
   return 0;
 }
 
 
 
+// Row-major {inner, outer} matrices, `batch` of them `batch_stride_elems`
+// apart: a 3-D view {inner, outer, batch} with boxes {box_inner, box_outer, 1}.
 int encode_2d(CUtensorMap* m, const float* base, long long inner, long long outer,
-              long long row_stride_elems, int box_inner, int box_outer) {
+              long long row_stride_elems, int box_inner, int box_outer, int batch = 1,
+              long long batch_stride_elems = 0) {
   auto enc = encoder();
   if (!enc) return B2G_ERR_TENSOR_MAP;
-  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
-  cuuint64_t strides[1] = {(cuuint64_t)row_stride_elems * 4};
-  cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides,
+  cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)outer, (cuuint64_t)batch};
+  cuuint64_t strides[2] = {(cuuint64_t)row_stride_elems * 4,
+                           batch > 1 ? (cuuint64_t)batch_stride_elems * 4 : 16};
+  cuuint32_t box[3] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? 0 : B2G_ERR_TENSOR_MAP;
@@ -312,29 +327,32 @@ int encode_2d_sw128(CUtensorMap* m, const float* base, long long inner, long lon
   return r == CUDA_SUCCESS ? 0 : B2G_ERR_TENSOR_MAP;
 }
 
-// Row-major A (M x K, lda) seen as a 3-D tensor {4, M, K/4}: element (e, r, q) is
-// A[r][4q + e].  A box {4, BM, BK/4} lands in shared memory as [BK/4][BM][4].
-int encode_a_kchunk(CUtensorMap* m, const float* A, int M, int K, int lda, int BM, int BK) {
+// Row-major A (M x K, lda) seen as a 4-D tensor {4, M, K/4, batch}: element
+// (e, r, q, b) is A_b[r][4q + e].  A box {4, BM, BK/4, 1} lands in shared memory
+// as [BK/4][BM][4].
+int encode_a_kchunk(CUtensorMap* m, const float* A, int M, int K, int lda, int BM, int BK,
+                    int batch = 1, long long batch_stride_elems = 0) {
   auto enc = encoder();
   if (!enc) return B2G_ERR_TENSOR_MAP;
-  cuuint64_t dims[3] = {4, (cuuint64_t)M, (cuuint64_t)(K / 4)};
-  cuuint64_t strides[2] = {(cuuint64_t)lda * 4, 16};
-  cuuint32_t box[3] = {4, (cuuint32_t)BM, (cuuint32_t)(BK / 4)};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(A), dims, strides,
+  cuuint64_t dims[4] = {4, (cuuint64_t)M, (cuuint64_t)(K / 4), (cuuint64_t)batch};
+  cuuint64_t strides[3] = {(cuuint64_t)lda * 4, 16,
+                           batch > 1 ? (cuuint64_t)batch_stride_elems * 4 : 16};
+  cuuint32_t box[4] = {4, (cuuint32_t)BM, (cuuint32_t)(BK / 4), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float*>(A), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? 0 : B2G_ERR_TENSOR_MAP;
 }
 
 int launch_scale(const Call& c, const DeviceState& d, cudaStream_t st) {
-  const long long total = (long long)c.M * c.N;
+  const long long total = (long long)c.M * c.N * c.batch;
   long long blocks = (total + 255) / 256;
   const long long cap = (long long)d.sms * 8;
   if (blocks > cap) blocks = cap;
-  void* args[] = {(void*)&c.M, (void*)&c.N, (void*)&c.beta, (void*)&c.C, nullptr};
-  long long ldc = c.ldc;
-  args[4] = &ldc;
+  long long ldc = c.ldc, strideC = c.strideC;
+  int batch = c.batch;
+  void* args[] = {(void*)&c.M, (void*)&c.N, (void*)&c.beta, (void*)&c.C, &ldc, &batch, &strideC};
   cudaError_t e = cudaLaunchKernel(reinterpret_cast<const void*>(&scale_c_kernel),
                                    dim3((unsigned)blocks), dim3(256), args, 0, st);
   return e == cudaSuccess ? 0 : B2G_ERR_LAUNCH;
@@ -349,7 +367,7 @@ int run(const Call& c, int forced_plan, void* stream, void* user_ws = nullptr,
         size_t user_ws_bytes = 0, bool allow_auto_ws = true) {
   int rc = validate(c);
   if (rc) return rc;
-  if (c.M == 0 || c.N == 0) return 0;
+  if (c.M == 0 || c.N == 0 || c.batch == 0) return 0;
   if (forced_plan >= num_plans()) return B2G_ERR_INVALID_PLAN;
   DeviceState* d = nullptr;
   rc = device_state(&d);
@@ -389,9 +407,14 @@ int run(const Call& c, int forced_plan, void* stream, void* user_ws = nullptr,
   p.alpha = c.alpha, p.beta = c.beta;
   p.A = c.A, p.lda = c.lda, p.B = c.B, p.ldb = c.ldb, p.C = c.C, p.ldc = c.ldc;
   p.transA = c.transA, p.transB = c.transB;
-  p.c_vec4 = aligned16(c.C) && c.ldc % 4 == 0;
+  p.batch = c.batch, p.strideA = c.strideA, p.strideB = c.strideB, p.strideC = c.strideC;
+  p.c_vec4 = aligned16(c.C) && c.ldc % 4 == 0 && (c.batch <= 1 || c.strideC % 4 == 0);
   p.tiles_m = (c.M + pl->BM - 1) / pl->BM;
   p.tiles_n = (c.N + pl->BN - 1) / pl->BN;
+  if ((long long)p.tiles_m * p.tiles_n * c.batch >= 0x7fffffffLL) {
+    if (auto_ws) ws_release(dev, st);
+    return B2G_ERR_INVALID_DIM;  // more output tiles than the tile index can address
+  }
   p.group_m = 8;
   p.k_tiles = (c.K + pl->BK - 1) / pl->BK;
   p.wait_limit_ns = g_wait_limit_ns.load();
@@ -405,17 +428,21 @@ int run(const Call& c, int forced_plan, void* stream, void* user_ws = nullptr,
 
   cudaError_t e = cudaSuccess;
   if (ws && pl->pretranspose == 1) {  // At = A^T, then the kernel reads A stored K x M
-    const long long ldat = pre_ld(c.M);
-    e = launch_transpose_a(c.A, c.M, c.K, c.lda, ws, ldat, st);
-    p.A = ws, p.lda = ldat, p.transA = 1;
+    const long long ldat = pre_ld(c.M), sat = (long long)c.K * ldat;
+    e = launch_transpose_a(c.A, c.M, c.K, c.lda, ws, ldat, st, c.batch, c.strideA, sat);
+    p.A = ws, p.lda = ldat, p.transA = 1, p.strideA = sat;
   } else if (ws && pl->pretranspose == 2) {  // At = op(A)^T and Bp = op(B), both aligned
     const long long ldat = pre_ld(c.M), ldbp = pre_ld(c.N);
+    const long long sat = (long long)c.K * ldat, sbp = (long long)c.K * ldbp;
     float* At = ws;
-    float* Bp = ws + (size_t)c.K * ldat;
-    e = launch_pack(c.A, c.lda, c.transA ? 0 : 1, c.K, c.M, At, ldat, st);
-    if (e == cudaSuccess) e = launch_pack(c.B, c.ldb, c.transB ? 1 : 0, c.K, c.N, Bp, ldbp, st);
-    p.A = At, p.lda = ldat, p.transA = 1;
-    p.B = Bp, p.ldb = ldbp, p.transB = 0;
+    float* Bp = ws + (size_t)c.batch * sat;
+    e = launch_pack(c.A, c.lda, c.transA ? 0 : 1, c.K, c.M, At, ldat, st, c.batch, c.strideA,
+                    sat);
+    if (e == cudaSuccess)
+      e = launch_pack(c.B, c.ldb, c.transB ? 1 : 0, c.K, c.N, Bp, ldbp, st, c.batch, c.strideB,
+                      sbp);
+    p.A = At, p.lda = ldat, p.transA = 1, p.strideA = sat;
+    p.B = Bp, p.ldb = ldbp, p.transB = 0, p.strideB = sbp;
   }
 
   CUtensorMap tmA, tmB;
@@ -423,10 +450,10 @@ int run(const Call& c, int forced_plan, void* stream, void* user_ws = nullptr,
   const CUtensorMap* pB = nullptr;
   if (e == cudaSuccess && pl->feed != kFeedCpAsync && pl->feed != kFeedSkinny) {
     if (pl->feed != kFeedTMA || pl->alayout == kAKChunk)
-      rc = encode_a_kchunk(&tmA, p.A, c.M, c.K, (int)p.lda, pl->BM, pl->BK);
-    else
-      rc = encode_2d(&tmA, p.A, c.M, c.K, p.lda, pl->BM, pl->BK);  // A stored K x M
-    if (!rc) rc = encode_2d(&tmB, p.B, c.N, c.K, p.ldb, pl->BN, pl->BK);
+      rc = encode_a_kchunk(&tmA, p.A, c.M, c.K, (int)p.lda, pl->BM, pl->BK, c.batch, p.strideA);
+    else  // A stored K x M
+      rc = encode_2d(&tmA, p.A, c.M, c.K, p.lda, pl->BM, pl->BK, c.batch, p.strideA);
+    if (!rc) rc = encode_2d(&tmB, p.B, c.N, c.K, p.ldb, pl->BN, pl->BK, c.batch, p.strideB);
     pA = &tmA, pB = &tmB;
   }
   if (e == cudaSuccess && !rc) e = pl->launch(p, pA, pB, d->sms, st);
@@ -513,6 +540,15 @@ int b2g_sgemm_with_plan(int plan, int transA, int transB, int M, int N, int K, f
   if (plan < 0 || plan >= num_plans()) return B2G_ERR_INVALID_PLAN;
   return run(Call{transA != 0, transB != 0, M, N, K, alpha, beta, A, lda, B, ldb, C, ldc}, plan,
              stream);
+}
+
+int b2g_sgemm_strided_batched(int transA, int transB, int M, int N, int K, float alpha,
+                              const float* A, int lda, long long strideA, const float* B, int ldb,
+                              long long strideB, float beta, float* C, int ldc,
+                              long long strideC, int batch, void* stream) {
+  Call c{transA != 0, transB != 0, M, N, K, alpha, beta, A, lda, B, ldb, C, ldc};
+  c.batch = batch, c.strideA = strideA, c.strideB = strideB, c.strideC = strideC;
+  return run(c, -1, stream);
 }
 
 int b2g_sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int lda, const float* B,

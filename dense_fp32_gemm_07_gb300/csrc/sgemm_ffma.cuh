@@ -94,10 +94,15 @@ __device__ __forceinline__ void outer_product(float (&acc)[8][TN], const float (
   }
 }
 
-// Output tile of linear index `tile`: tiles run down a group of `group_m` tile
-// rows before moving one tile column right, so CTAs that run together share A
-// row panels and B column panels in L2.
-__device__ __forceinline__ void tile_coords(const SgemmParams& p, int tile, int& tm, int& tn) {
+// Output tile of linear index `tile`: problem b = tile / (tiles_m * tiles_n) of
+// a batch; inside a problem, tiles run down a group of `group_m` tile rows
+// before moving one tile column right, so CTAs that run together share A row
+// panels and B column panels in L2.
+__device__ __forceinline__ void tile_coords(const SgemmParams& p, int tile, int& b, int& tm,
+                                            int& tn) {
+  const int per_batch = p.tiles_m * p.tiles_n;
+  b = tile / per_batch;
+  tile -= b * per_batch;
   const int per_group = p.group_m * p.tiles_n;
   const int g = tile / per_group;
   const int first_m = g * p.group_m;
@@ -135,7 +140,7 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
   }
   __syncthreads();
 
-  const int total_tiles = p.tiles_m * p.tiles_n;
+  const int total_tiles = p.tiles_m * p.tiles_n * p.batch;
 
   // ------------------------------------------------------------------ producer
   // Producer warps come first (warps 0 .. PWARPS-1), consumers after them.
@@ -148,8 +153,8 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
       prefetch_tmap(&tmA);
       prefetch_tmap(&tmB);
       for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-        int tm, tn;
-        tile_coords(p, tile, tm, tn);
+        int bt, tm, tn;
+        tile_coords(p, tile, bt, tm, tn);
         const int m0 = tm * BM, n0 = tn * BN;
         for (int kt = 0; kt < p.k_tiles; ++kt) {
           if (p.debug_stop_ktile >= 0 && issued >= p.debug_stop_ktile) goto drain_tma;
@@ -162,11 +167,12 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
           const uint32_t dA = smem_addr(FEED == kFeedTMATrans ? sAst + stage * Cfg::kStaging
                                                               : sA + stage * Cfg::kAStage);
           const uint32_t dB = smem_addr(sB + stage * Cfg::kBStage);
+          // the batch index is each view's outermost coordinate
           if constexpr (ALAY == kAKChunk || FEED == kFeedTMATrans)
-            tma_load_3d(dA, &tmA, 0, m0, kt * (BK / 4), fb);  // view {4, M, K/4}
+            tma_load_4d(dA, &tmA, 0, m0, kt * (BK / 4), bt, fb);  // view {4, M, K/4, batch}
           else
-            tma_load_2d(dA, &tmA, m0, kt * BK, fb);  // A stored K x M
-          tma_load_2d(dB, &tmB, n0, kt * BK, fb);
+            tma_load_3d(dA, &tmA, m0, kt * BK, bt, fb);  // A stored K x M: {M, K, batch}
+          tma_load_3d(dB, &tmB, n0, kt * BK, bt, fb);    // {N, K, batch}
           ++issued;
           if (++stage == STAGES) stage = 0, phase ^= 1u;
         }
@@ -181,9 +187,11 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
     } else {
       const int pt = threadIdx.x;
       for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-        int tm, tn;
-        tile_coords(p, tile, tm, tn);
+        int bt, tm, tn;
+        tile_coords(p, tile, bt, tm, tn);
         const int m0 = tm * BM, n0 = tn * BN;
+        const float* Ab = p.A + (long long)bt * p.strideA;
+        const float* Bb = p.B + (long long)bt * p.strideB;
         for (int kt = 0; kt < p.k_tiles; ++kt) {
           if (p.debug_stop_ktile >= 0 && issued >= p.debug_stop_ktile) goto drain_cp;
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, p.wait_limit_ns, p.status,
@@ -203,7 +211,7 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
             const long long off = ok ? (p.transA ? (long long)gk * p.lda + gr
                                                  : (long long)gr * p.lda + gk)
                                      : 0;
-            cp_async_4(dA + 4u * (k * BM + r), p.A + off, ok ? 4u : 0u);
+            cp_async_4(dA + 4u * (k * BM + r), Ab + off, ok ? 4u : 0u);
           }
           // B tile -> Bs[k][n]
 #pragma unroll 4
@@ -215,7 +223,7 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
             const long long off = ok ? (p.transB ? (long long)gn * p.ldb + gk
                                                  : (long long)gk * p.ldb + gn)
                                      : 0;
-            cp_async_4(dB + 4u * (k * BN + n), p.B + off, ok ? 4u : 0u);
+            cp_async_4(dB + 4u * (k * BN + n), Bb + off, ok ? 4u : 0u);
           }
           cp_async_arrive_noinc(full0 + 8 * stage);
           ++issued;
@@ -278,8 +286,8 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
   }
 
   for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-    int tm, tn;
-    tile_coords(p, tile, tm, tn);
+    int bt, tm, tn;
+    tile_coords(p, tile, bt, tm, tn);
     float acc[8][TN];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
@@ -361,7 +369,7 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
       const int r = m0 + ((ALAY == kAKChunk) ? wm * 32 + tr + 4 * i
                                             : wm * 32 + 4 * tr + (i & 3) + 16 * (i >> 2));
       if (r >= p.M) continue;
-      float* crow = p.C + (long long)r * p.ldc;
+      float* crow = p.C + (long long)bt * p.strideC + (long long)r * p.ldc;
 #pragma unroll
       for (int j4 = 0; j4 < TN / 4; ++j4) {
         const int c = n0 + b_off + 32 * j4;
@@ -414,7 +422,7 @@ cudaError_t launch_ffma(const SgemmParams& p, const CUtensorMap* tmA, const CUte
     if (occ < 1) return cudaErrorInvalidConfiguration;
     resident[dev].store(occ, std::memory_order_release);
   }
-  const long long tiles = (long long)p.tiles_m * p.tiles_n;
+  const long long tiles = (long long)p.tiles_m * p.tiles_n * p.batch;
   const int grid = (int)std::min<long long>(tiles, (long long)num_sms * occ);
   CUtensorMap none;
   memset(&none, 0, sizeof(none));

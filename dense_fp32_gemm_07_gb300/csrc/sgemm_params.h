@@ -23,6 +23,8 @@ struct SgemmParams {
   unsigned long long wait_limit_ns;  // bound on every mbarrier wait
   int debug_stop_ktile;              // < 0 normally; >= 0 stops the producer (timeout test)
   unsigned int* status;              // device status word (timeout flags)
+  int batch;                         // independent problems (strided batched); 1 otherwise
+  long long strideA, strideB, strideC;  // elements between consecutive problems
   float* work;                       // split-K partial sums (skinny plans), or null
   int splits;                        // split-K factor (skinny plans); 1 = no split
   int kc;                            // k extent of one split (skinny plans)

@@ -44,6 +44,11 @@ __global__ void __launch_bounds__(kSkThreads) skinny_kernel(const __grid_constan
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int s = blockIdx.y;
   const int kb = s * p.kc, ke = min(p.K, kb + p.kc);
+  const int bz = blockIdx.z;  // problem of a batch
+  const float* Ab = p.A + (long long)bz * p.strideA;
+  const float* Bb = p.B + (long long)bz * p.strideB;
+  float* Cb = p.C + (long long)bz * p.strideC;
+  float* Wb = p.splits > 1 ? p.work + (long long)bz * p.splits * p.M * p.N : nullptr;
   const int col = blockIdx.x * kSkCols + 4 * lane;
   const bool col_ok = col < p.N;  // N % 4 == 0, so col + 3 < N as well
   const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -59,7 +64,7 @@ __global__ void __launch_bounds__(kSkThreads) skinny_kernel(const __grid_constan
     for (int idx = threadIdx.x; idx < MR * (cl / 4); idx += kSkThreads) {
       const int m = idx % MR, k4 = idx / MR;
       const float4 v = (m < p.M)
-                           ? *reinterpret_cast<const float4*>(p.A + (long long)m * p.lda + c0 + 4 * k4)
+                           ? *reinterpret_cast<const float4*>(Ab + (long long)m * p.lda + c0 + 4 * k4)
                            : zero;
       As[(4 * k4 + 0) * MR + m] = v.x;
       As[(4 * k4 + 1) * MR + m] = v.y;
@@ -68,7 +73,7 @@ __global__ void __launch_bounds__(kSkThreads) skinny_kernel(const __grid_constan
     }
     __syncthreads();
     const int kw = cl / 4;  // this warp's share of the chunk
-    const float* bp = p.B + (long long)(c0 + warp * kw) * p.ldb + col;
+    const float* bp = Bb + (long long)(c0 + warp * kw) * p.ldb + col;
     const float* ap = As + warp * kw * MR;
 #pragma unroll UNR
     for (int k = 0; k < kw; ++k) {
@@ -112,10 +117,10 @@ __global__ void __launch_bounds__(kSkThreads) skinny_kernel(const __grid_constan
   for (int i = 0; i < MR; ++i) {
     if (i >= p.M) break;
     if (p.splits > 1) {
-      *reinterpret_cast<float4*>(p.work + ((long long)s * p.M + i) * p.N + col) =
+      *reinterpret_cast<float4*>(Wb + ((long long)s * p.M + i) * p.N + col) =
           make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
     } else {
-      float* crow = p.C + (long long)i * p.ldc + col;
+      float* crow = Cb + (long long)i * p.ldc + col;
       if (p.c_vec4) {
         float4 o;
         if (beta != 0.f) {
@@ -139,20 +144,22 @@ __global__ void __launch_bounds__(kSkThreads) skinny_kernel(const __grid_constan
 // C = alpha * (P[0] + P[1] + ... + P[S-1]) + beta * C, partials added in s order.
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constant__ SgemmParams p) {
   const long long nv = p.N / 4;
-  const long long total = (long long)p.M * nv;
+  const long long per = (long long)p.M * nv;
+  const long long total = per * p.batch;
   const long long plane = (long long)p.M * p.N;
   const float alpha = p.alpha, beta = p.beta;
   for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
        idx += (long long)gridDim.x * blockDim.x) {
-    const long long m = idx / nv, c = (idx - m * nv) * 4;
-    const float* w = p.work + m * p.N + c;
+    const long long bz = idx / per, r = idx - bz * per;
+    const long long m = r / nv, c = (r - m * nv) * 4;
+    const float* w = p.work + bz * p.splits * plane + m * p.N + c;
     float4 sum = *reinterpret_cast<const float4*>(w);
     for (int s = 1; s < p.splits; ++s) {
       const float4 v = *reinterpret_cast<const float4*>(w + s * plane);
       sum.x += v.x, sum.y += v.y, sum.z += v.z, sum.w += v.w;
     }
     const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
-    float* crow = p.C + m * p.ldc + c;
+    float* crow = p.C + bz * p.strideC + m * p.ldc + c;
     if (p.c_vec4) {
       float4 o;
       if (beta != 0.f) {
@@ -172,7 +179,7 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constan
 }
 
 cudaError_t launch_splitk_reduce(const SgemmParams& p, cudaStream_t stream, int num_sms) {
-  const long long total = (long long)p.M * (p.N / 4);
+  const long long total = (long long)p.M * (p.N / 4) * p.batch;
   long long blocks = (total + 255) / 256;
   const long long cap = (long long)num_sms * 8;
   if (blocks > cap) blocks = cap;
@@ -217,7 +224,8 @@ cudaError_t launch_skinny(const SgemmParams& p, const CUtensorMap*, const CUtens
     if (e != cudaSuccess) return e;
     configured[dev].store(1, std::memory_order_release);
   }
-  const dim3 grid((unsigned)((p.N + kSkCols - 1) / kSkCols), (unsigned)p.splits);
+  const dim3 grid((unsigned)((p.N + kSkCols - 1) / kSkCols), (unsigned)p.splits,
+                  (unsigned)p.batch);
   SgemmParams pc = p;
   void* args[] = {&pc};
   e = cudaLaunchKernel(reinterpret_cast<const void*>(kern), grid, dim3(kSkThreads), args,

@@ -20,8 +20,11 @@ constexpr int kTT = 64;  // tile edge (m and k)
 __global__ void __launch_bounds__(256) transpose_a_kernel(const float* __restrict__ A, int M,
                                                           int K, long long lda,
                                                           float* __restrict__ At,
-                                                          long long ldat) {
+                                                          long long ldat, long long strideA,
+                                                          long long strideAt) {
   __shared__ __align__(16) float tile[kTT][kTT];  // [k][m]
+  A += (long long)blockIdx.z * strideA;  // problem blockIdx.z of a batch
+  At += (long long)blockIdx.z * strideAt;
   const int m0 = blockIdx.x * kTT, k0 = blockIdx.y * kTT;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   // load: warp w takes 4-k chunks c = w, w+8; lanes take 32 consecutive rows
@@ -55,11 +58,21 @@ __global__ void __launch_bounds__(256) transpose_a_kernel(const float* __restric
 }
 
 cudaError_t launch_transpose_a(const float* A, int M, int K, long long lda, float* At,
-                               long long ldat, cudaStream_t stream) {
-  const dim3 grid((unsigned)((M + kTT - 1) / kTT), (unsigned)((K + kTT - 1) / kTT));
-  void* args[] = {(void*)&A, (void*)&M, (void*)&K, (void*)&lda, (void*)&At, (void*)&ldat};
-  return cudaLaunchKernel(reinterpret_cast<const void*>(&transpose_a_kernel), grid, dim3(256),
-                          args, 0, stream);
+                               long long ldat, cudaStream_t stream, int batch,
+                               long long strideA, long long strideAt) {
+  for (int b0 = 0; b0 < batch; b0 += 65535) {  // grid z is at most 65535
+    const int nb = batch - b0 < 65535 ? batch - b0 : 65535;
+    const float* Ab = A + (long long)b0 * strideA;
+    float* Atb = At + (long long)b0 * strideAt;
+    const dim3 grid((unsigned)((M + kTT - 1) / kTT), (unsigned)((K + kTT - 1) / kTT),
+                    (unsigned)nb);
+    void* args[] = {(void*)&Ab, (void*)&M, (void*)&K, (void*)&lda, (void*)&Atb, (void*)&ldat,
+                    (void*)&strideA, (void*)&strideAt};
+    const cudaError_t e = cudaLaunchKernel(reinterpret_cast<const void*>(&transpose_a_kernel),
+                                           grid, dim3(256), args, 0, stream);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace b2g
@@ -74,8 +87,11 @@ namespace b2g {
 // coalesced on both sides in either direction.
 __global__ void __launch_bounds__(256) pack_kernel(const float* __restrict__ in, long long ld,
                                                    int trans, int R, int Cc,
-                                                   float* __restrict__ out, long long ldo) {
+                                                   float* __restrict__ out, long long ldo,
+                                                   long long stride_in, long long stride_out) {
   __shared__ float tile[32][33];
+  in += (long long)blockIdx.z * stride_in;  // problem blockIdx.z of a batch
+  out += (long long)blockIdx.z * stride_out;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
   const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
   if (trans) {
@@ -101,12 +117,20 @@ __global__ void __launch_bounds__(256) pack_kernel(const float* __restrict__ in,
 }
 
 cudaError_t launch_pack(const float* in, long long ld, int trans, int R, int Cc, float* out,
-                        long long ldo, cudaStream_t stream) {
-  const dim3 grid((unsigned)((Cc + 31) / 32), (unsigned)((R + 31) / 32));
-  void* args[] = {(void*)&in, (void*)&ld, (void*)&trans, (void*)&R, (void*)&Cc, (void*)&out,
-                  (void*)&ldo};
-  return cudaLaunchKernel(reinterpret_cast<const void*>(&pack_kernel), grid, dim3(256), args, 0,
-                          stream);
+                        long long ldo, cudaStream_t stream, int batch, long long stride_in,
+                        long long stride_out) {
+  for (int b0 = 0; b0 < batch; b0 += 65535) {
+    const int nb = batch - b0 < 65535 ? batch - b0 : 65535;
+    const float* ib = in + (long long)b0 * stride_in;
+    float* ob = out + (long long)b0 * stride_out;
+    const dim3 grid((unsigned)((Cc + 31) / 32), (unsigned)((R + 31) / 32), (unsigned)nb);
+    void* args[] = {(void*)&ib, (void*)&ld, (void*)&trans, (void*)&R, (void*)&Cc, (void*)&ob,
+                    (void*)&ldo, (void*)&stride_in, (void*)&stride_out};
+    const cudaError_t e = cudaLaunchKernel(reinterpret_cast<const void*>(&pack_kernel), grid,
+                                           dim3(256), args, 0, stream);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace b2g

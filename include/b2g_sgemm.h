@@ -81,6 +81,21 @@ int b2g_sgemm_ex(int transA, int transB, int M, int N, int K, float alpha, const
                  const float* B, int ldb, float beta, float* C, int ldc, void* stream);
 
 /*
+ * `batch` independent products C_b = alpha * op(A_b) * op(B_b) + beta * C_b,
+ * b = 0 .. batch-1, with A_b = A + b*strideA, B_b = B + b*strideB and
+ * C_b = C + b*strideC (strides in elements, >= 0; C_b must not overlap each
+ * other).  Same layout rules, plans and workspace behaviour as b2g_sgemm_ex
+ * (workspace scaled by batch); one launch covers the whole batch (the batch
+ * index is the outermost coordinate of the tile scheduler).  batch == 0 does
+ * nothing; batch < 0 is B2G_ERR_INVALID_DIM, a negative stride
+ * B2G_ERR_INVALID_LD.  Batched GEMM is not on the pages; it shares their kernel.
+ */
+int b2g_sgemm_strided_batched(int transA, int transB, int M, int N, int K, float alpha,
+                              const float* A, int lda, long long strideA, const float* B, int ldb,
+                              long long strideB, float beta, float* C, int ldc,
+                              long long strideC, int batch, void* stream);
+
+/*
  * As b2g_sgemm_ex with a caller-owned device workspace of workspace_bytes
  * (16-byte aligned).  Never allocates.  When the workspace is NULL or smaller
  * than b2g_sgemm_workspace_size reports, a plan that needs none runs instead
