@@ -36,7 +36,7 @@ UNIT = "TFLOP/s"
 SMS, LANES, MAX_MHZ = 152, 128, 2070.0
 L2_BYTES = 129e6
 # device code of the dominant kernel: a change here voids the recorded traffic
-KERNEL_SOURCES = ("csrc/sgemm_ffma.cuh", "csrc/ptx.cuh", "csrc/plans_tma.cu",
+KERNEL_SOURCES = ("csrc/sgemm_ffma.cuh", "csrc/ptx.cuh", "csrc/plans_tmat.cu",
                   "csrc/sgemm_params.h")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_square4096.txt")
 

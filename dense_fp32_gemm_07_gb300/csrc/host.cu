@@ -151,12 +151,14 @@ void ws_release(int dev, cudaStream_t st) {
   w.mu.unlock();
 }
 
-int num_plans() { return kNumPlansTMA + kNumPlansGeneral + kNumPlansSkinny; }
+int num_plans() { return kNumPlansTMA + kNumPlansT + kNumPlansGeneral + kNumPlansSkinny; }
 
 const Plan* plan_at(int i) {
   if (i < 0) return nullptr;
   if (i < kNumPlansTMA) return &kPlansTMA[i];
   i -= kNumPlansTMA;
+  if (i < kNumPlansT) return &kPlansT[i];
+  i -= kNumPlansT;
   if (i < kNumPlansGeneral) return &kPlansGeneral[i];
   i -= kNumPlansGeneral;
   if (i < kNumPlansSkinny) return &kPlansSkinny[i];

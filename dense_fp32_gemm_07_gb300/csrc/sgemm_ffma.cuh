@@ -67,8 +67,9 @@ struct FfmaCfg {
 
 // One k step of the register outer product, acc[i][j] += a[i] * b[j], as FP32
 // FFMAs.  ORD picks the issue order (0: row by row, 1: column by column,
-// 2: rows with alternating column direction); every order performs the same
-// FFMAs on the same accumulators, so results are identical, but the order
+// 2: rows with alternating column direction, 3: 2 x 2 blocks walked as a
+// snake, 4: columns with alternating row direction); every order performs the
+// same FFMAs on the same accumulators, so results are identical, but the order
 // changes which operand consecutive FFMAs share.
 template <int ORD, int TN>
 __device__ __forceinline__ void outer_product(float (&acc)[8][TN], const float (&a)[8],
@@ -78,6 +79,26 @@ __device__ __forceinline__ void outer_product(float (&acc)[8][TN], const float (
     for (int j = 0; j < TN; ++j)
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+  } else if constexpr (ORD == 3) {
+#pragma unroll
+    for (int i2 = 0; i2 < 4; ++i2)
+#pragma unroll
+      for (int jj = 0; jj < TN / 2; ++jj) {
+        const int j2 = (i2 & 1) ? TN / 2 - 1 - jj : jj;
+        const int i = 2 * i2, j = 2 * j2;
+        acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        acc[i][j + 1] = fmaf(a[i], b[j + 1], acc[i][j + 1]);
+        acc[i + 1][j + 1] = fmaf(a[i + 1], b[j + 1], acc[i + 1][j + 1]);
+        acc[i + 1][j] = fmaf(a[i + 1], b[j], acc[i + 1][j]);
+      }
+  } else if constexpr (ORD == 4) {
+#pragma unroll
+    for (int j = 0; j < TN; ++j)
+#pragma unroll
+      for (int ii = 0; ii < 8; ++ii) {
+        const int i = (j & 1) ? 7 - ii : ii;
+        acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+      }
   } else if constexpr (ORD == 2) {
 #pragma unroll
     for (int i = 0; i < 8; ++i)

@@ -77,6 +77,8 @@ cudaError_t launch_splitk_reduce(const SgemmParams& p, cudaStream_t stream, int 
 // Plans compiled in each kernel translation unit.
 extern const Plan kPlansTMA[];
 extern const int kNumPlansTMA;
+extern const Plan kPlansT[];
+extern const int kNumPlansT;
 extern const Plan kPlansGeneral[];
 extern const int kNumPlansGeneral;
 

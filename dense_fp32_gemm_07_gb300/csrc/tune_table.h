@@ -34,24 +34,15 @@ const TuneRule kTuneTable[] = {
     {kClassFast, 17, 32, 0, kInf, 0, "skinny_m32", nullptr},
     // other small M: too few row tiles to fill 152 SMs with the tiled plans
     {kClassFast, 0, 48, 0, kInf, 0, "tma_64x128x16_s6_o1", nullptr},
-    // up to ~1.3e9 multiply-adds the transpose costs more than it saves
+    // up to ~2e9 multiply-adds the transpose costs about what it saves
     {kClassFast, 49, kInf, 0, kInf, 0, "tma_64x128x16_s6_o2", nullptr, 2.0e9},
-    // 2048^3-class: 128x128 tiles fill the SMs better than 64x128
-    {kClassFast, 49, kInf, 0, kInf, 2.0e9, "pre_128x128x16_s6_o1", "tmaX_128x128x16_s6_o2", 2.5e10},
-    // 4096^3 and 8192x11008x4096
-    {kClassFast, 49, kInf, 0, kInf, 2.5e10, "pre_64x128x16_s6", "tmaX_128x128x16_s6_o2", 4.0e11},
-    // 8192^3 and larger
-    {kClassFast, 49, kInf, 0, kInf, 4.0e11, "pre_128x128x16_s6_o1", "tmaX_128x128x16_s6_o2"},
-    {kClassFastTransA, 0, kInf, 0, kInf, 0, "tmaT_64x128x16_s6", nullptr, 2.5e10},
-    {kClassFastTransA, 0, kInf, 0, kInf, 2.5e10, "tmaT_64x128x16_s6", nullptr, 4.0e11},
-    {kClassFastTransA, 0, kInf, 0, kInf, 4.0e11, "tmaT_128x128x16_s6_o1", nullptr},
+    // larger: A transposed into the workspace, then the transposed-layout kernel
+    {kClassFast, 49, kInf, 0, kInf, 2.0e9, "pre_64x128x16_s6_o2", "tmaX_128x128x16_s6_o2"},
+    {kClassFastTransA, 0, kInf, 0, kInf, 0, "tmaT_64x128x16_s6_o2", nullptr},
     // anything else (misaligned pointers, odd leading dimensions, K % 4 != 0,
     // op(B) = B^T): pack A^T and B aligned into the workspace, then the
     // transposed-layout kernel; the 4-byte feed needs no workspace
-    {kClassGeneral, 0, kInf, 0, kInf, 5.0e7, "pack_64x128x16_s6", "gen_64x64x16_s4", 2.0e9},
-    {kClassGeneral, 0, kInf, 0, kInf, 2.0e9, "pack_128x128x16_s6_o1", "gen_64x64x16_s4", 2.5e10},
-    {kClassGeneral, 0, kInf, 0, kInf, 2.5e10, "pack_64x128x16_s6", "gen_64x64x16_s4", 4.0e11},
-    {kClassGeneral, 0, kInf, 0, kInf, 4.0e11, "pack_128x128x16_s6_o1", "gen_64x64x16_s4"},
+    {kClassGeneral, 0, kInf, 0, kInf, 5.0e7, "pack_64x128x16_s6_o2", "gen_64x64x16_s4"},
     {kClassGeneral, 0, kInf, 0, kInf, 0, "gen_64x64x16_s4", nullptr},
 };
 

@@ -16,7 +16,7 @@ def tb():
     return env()
 
 
-@pytest.mark.parametrize("plan_name", ["tma_64x128x16_s6", "tmaX_64x128x16_s6_o1",
+@pytest.mark.parametrize("plan_name", ["tma_64x128x16_s6_o2", "tmaX_64x128x16_s6_o1",
                                        "gen_64x64x16_s4"])
 def test_wait_runs_out_and_context_survives(tb, plan_name):
     torch, b2g = tb
