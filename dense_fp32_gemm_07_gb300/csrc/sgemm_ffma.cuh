@@ -39,7 +39,7 @@
 namespace b2g {
 
 template <int BM, int BN, int BK, int WM, int WN, int TN, int STAGES, int ALAY, int FEED,
-          int PWARPS, int ORD = 0>
+          int PWARPS, int ORD = 0, int KU = BK>
 struct FfmaCfg {
   static constexpr int TM = 8;
   static constexpr int kConsumerWarps = WM * WN;
@@ -134,12 +134,12 @@ __device__ __forceinline__ void tile_coords(const SgemmParams& p, int tile, int&
 }
 
 template <int BM, int BN, int BK, int WM, int WN, int TN, int STAGES, int ALAY, int FEED,
-          int PWARPS, int ORD>
+          int PWARPS, int ORD, int KU>
 __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
     sgemm_ffma_kernel(const __grid_constant__ SgemmParams p,
                       const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB) {
-  using Cfg = FfmaCfg<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS, ORD>;
+  using Cfg = FfmaCfg<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS, ORD, KU>;
   extern __shared__ __align__(1024) unsigned char smem[];
   float* sA = reinterpret_cast<float*>(smem);
   float* sB = sA + STAGES * Cfg::kAStage;
@@ -358,7 +358,8 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
           }
         }
       } else {
-#pragma unroll
+        // KU < BK keeps the loop body (and the instruction footprint) smaller
+#pragma unroll KU
         for (int k = 0; k < BK; ++k) {
           const float4 a0 = *reinterpret_cast<const float4*>(As + k * Cfg::kARow);
           const float4 a1 = *reinterpret_cast<const float4*>(As + k * Cfg::kARow + 16);
@@ -422,11 +423,11 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
 }
 
 template <int BM, int BN, int BK, int WM, int WN, int TN, int STAGES, int ALAY, int FEED,
-          int PWARPS, int ORD>
+          int PWARPS, int ORD, int KU = BK>
 cudaError_t launch_ffma(const SgemmParams& p, const CUtensorMap* tmA, const CUtensorMap* tmB,
                         int num_sms, cudaStream_t stream) {
-  using Cfg = FfmaCfg<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS, ORD>;
-  auto kern = sgemm_ffma_kernel<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS, ORD>;
+  using Cfg = FfmaCfg<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS, ORD, KU>;
+  auto kern = sgemm_ffma_kernel<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS, ORD, KU>;
   // Per device, once: opt in to the dynamic shared memory size and record how
   // many CTAs fit on one SM (the persistent grid is SMs x that).
   static std::atomic<int> resident[kMaxDevices];
