@@ -35,7 +35,8 @@ B2G_ERR_SCRATCH_LIMIT = -11
 # every symbol include/b2g_sgemm.h declares
 EXPORTS = (
     "b2g_sgemm", "b2g_sgemm_ex", "b2g_sgemm_with_plan", "b2g_sgemm_select_plan",
-    "b2g_sgemm_ws", "b2g_sgemm_workspace_size", "b2g_release_workspaces", "b2g_sgemm_noalloc",
+    "b2g_sgemm_ws", "b2g_sgemm_workspace_size", "b2g_sgemm_launch_count",
+    "b2g_release_workspaces", "b2g_sgemm_noalloc",
     "b2g_sgemm_3xtf32", "b2g_sgemm_strided_batched",
     "b2g_plan_count", "b2g_plan_name", "b2g_plan_info", "b2g_status", "b2g_set_wait_limit_ns",
     "b2g_debug_stop_after", "b2g_strerror", "b2g_version",
@@ -71,6 +72,8 @@ def _load():
                                      vp]
         lib.b2g_sgemm_workspace_size.argtypes = [i, i, i, i, i, f, vp, i, vp, i, vp, i,
                                                  ctypes.POINTER(ctypes.c_size_t)]
+        lib.b2g_sgemm_launch_count.argtypes = [i, i, i, i, i, f, vp, i, vp, i, vp, i,
+                                               ctypes.POINTER(ctypes.c_int)]
         lib.b2g_release_workspaces.argtypes = []
         lib.b2g_sgemm_noalloc.argtypes = gemm
         lib.b2g_sgemm_3xtf32.argtypes = gemm
@@ -132,6 +135,14 @@ def b2g_sgemm_workspace_size(transA, transB, M, N, K, alpha, A, lda, B, ldb, C, 
     n = ctypes.c_size_t(0)
     rc = _load().b2g_sgemm_workspace_size(transA, transB, M, N, K, alpha, A, lda, B, ldb, C, ldc,
                                           ctypes.byref(n))
+    return rc, n.value
+
+
+def b2g_sgemm_launch_count(transA, transB, M, N, K, alpha, A, lda, B, ldb, C, ldc):
+    """(rc, kernel launches one b2g_sgemm_ex call with these arguments makes)."""
+    n = ctypes.c_int(0)
+    rc = _load().b2g_sgemm_launch_count(transA, transB, M, N, K, alpha, A, lda, B, ldb, C, ldc,
+                                        ctypes.byref(n))
     return rc, n.value
 
 

@@ -251,7 +251,7 @@ long long pre_ld(int M) { return ((long long)M + 3) / 4 * 4; }
 
 // SMs and resident CTAs per SM of plan `pl` on the current device (152 and 4
 // when no device answers, as on a machine without a GPU).
-void skinny_capacity(const Plan& pl, int* sms, int* occ) {
+void plan_capacity(const Plan& pl, int* sms, int* occ) {
   *sms = 152, *occ = 4;
   DeviceState* d = nullptr;
   if (device_state(&d) == 0) {
@@ -266,7 +266,7 @@ void skinny_capacity(const Plan& pl, int* sms, int* occ) {
 // receives the k extent of one split (a multiple of 16).
 int skinny_splits(const Plan& pl, const Call& c, int* kc) {
   int sms = 0, occ = 0;
-  skinny_capacity(pl, &sms, &occ);
+  plan_capacity(pl, &sms, &occ);
   const long long slabs = (c.N + 127) / 128 * (c.batch > 0 ? c.batch : 1);
   long long S = (long long)sms * occ / slabs;
   const long long smax = c.K / 64 > 1 ? c.K / 64 : 1;
@@ -278,8 +278,44 @@ int skinny_splits(const Plan& pl, const Call& c, int* kc) {
   return (int)((c.K + k - 1) / k);
 }
 
-// Workspace bytes plan `pl` wants for this call (0 when it needs none).
-size_t plan_work_bytes(const Plan& pl, const Call& c) {
+// Split tail of an FFMA plan: with T output tiles and G = SMs x resident
+// CTAs, T = q*G + r.  When 0 < r, the last r tiles are each cut into S = G / r
+// k slices (at most one slice per CTA, at least 128 k per slice), so the
+// persistent grid's last round keeps every CTA busy instead of r of them.
+// Returns S (1: no split) and the first split tile in *first.
+constexpr int kMinSliceK = 128;
+
+int tail_split(const Plan& pl, const Call& c, int* first) {
+  *first = 0;
+  if (pl.feed == kFeedSkinny || !pl.occupancy) return 1;
+  const long long tiles =
+      (long long)((c.M + pl.BM - 1) / pl.BM) * ((c.N + pl.BN - 1) / pl.BN) * c.batch;
+  int sms = 0, occ = 0;
+  plan_capacity(pl, &sms, &occ);
+  const long long G = (long long)sms * occ;
+  if (tiles <= 0 || G <= 0) return 1;
+  const long long q = tiles / G, r = tiles - q * G;
+  if (r == 0) return 1;
+  long long S = G / r;
+  const long long smax = c.K / kMinSliceK;
+  if (S > smax) S = smax;
+  if (S < 2) return 1;
+  *first = (int)(q * G);
+  return (int)S;
+}
+
+// Bytes of the split tail's partial sums (0 without a split) and where they
+// start in the workspace (after what the plan itself needs, 256-byte aligned).
+size_t tail_bytes(const Plan& pl, const Call& c, int S, int first) {
+  if (S <= 1) return 0;
+  const long long tiles =
+      (long long)((c.M + pl.BM - 1) / pl.BM) * ((c.N + pl.BN - 1) / pl.BN) * c.batch;
+  return (size_t)(tiles - first) * S * pl.BM * pl.BN * sizeof(float);
+}
+size_t tail_offset(size_t base) { return (base + 255) / 256 * 256; }
+
+// Workspace bytes plan `pl` cannot do without for this call (0 when none).
+size_t plan_base_bytes(const Plan& pl, const Call& c) {
   const size_t nb = (size_t)(c.batch > 0 ? c.batch : 0);
   if (pl.pretranspose == 1) return nb * (size_t)c.K * (size_t)pre_ld(c.M) * sizeof(float);
   if (pl.pretranspose == 2)
@@ -290,6 +326,16 @@ size_t plan_work_bytes(const Plan& pl, const Call& c) {
     return S > 1 ? nb * (size_t)S * c.M * c.N * sizeof(float) : 0;
   }
   return 0;
+}
+
+// Workspace bytes plan `pl` wants for this call: its own need plus room for
+// the split tail's partial sums.
+size_t plan_work_bytes(const Plan& pl, const Call& c) {
+  const size_t base = plan_base_bytes(pl, c);
+  int first = 0;
+  const int S = tail_split(pl, c, &first);
+  const size_t t = tail_bytes(pl, c, S, first);
+  return t ? tail_offset(base) + t : base;
 }
 
 
@@ -387,14 +433,22 @@ int run(const Call& c, int forced_plan, void* stream, void* user_ws = nullptr,
   cudaGetDevice(&dev);
   float* ws = nullptr;
   bool auto_ws = false;
-  const size_t need = plan_work_bytes(*pl, c);
+  const size_t base = plan_base_bytes(*pl, c);
+  int tail_first = 0;
+  int tail_S = tail_split(*pl, c, &tail_first);
+  const size_t tail = tail_bytes(*pl, c, tail_S, tail_first);
+  const size_t need = tail ? tail_offset(base) + tail : base;
   if (need) {
-    if (user_ws && user_ws_bytes >= need && aligned16(user_ws)) {
+    if (user_ws && aligned16(user_ws) && user_ws_bytes >= need) {
       ws = static_cast<float*>(user_ws);
+    } else if (user_ws && aligned16(user_ws) && base && user_ws_bytes >= base) {
+      ws = static_cast<float*>(user_ws);  // room for the plan, not for the split tail
+      tail_S = 1;
     } else if (allow_auto_ws) {
       ws = static_cast<float*>(ws_acquire(dev, st, need));
       auto_ws = ws != nullptr;
     }
+    if (!ws) tail_S = 1;
     if (!ws && pl->pretranspose) {
       if (forced_plan >= 0 || fallback < 0) return B2G_ERR_UNSUPPORTED;
       pi = fallback;
@@ -423,9 +477,13 @@ int run(const Call& c, int forced_plan, void* stream, void* user_ws = nullptr,
   p.debug_stop_ktile = g_debug_stop.load();
   p.status = d->status;
   p.work = nullptr, p.splits = 1, p.kc = c.K;
+  p.tail_first = 0, p.tail_splits = 1;
   if (pl->feed == kFeedSkinny && ws) {
     p.splits = skinny_splits(*pl, c, &p.kc);
     p.work = ws;
+  } else if (ws && tail_S > 1) {
+    p.tail_first = tail_first, p.tail_splits = tail_S;
+    p.work = ws + tail_offset(base) / sizeof(float);
   }
 
   cudaError_t e = cudaSuccess;
@@ -459,6 +517,8 @@ int run(const Call& c, int forced_plan, void* stream, void* user_ws = nullptr,
     pA = &tmA, pB = &tmB;
   }
   if (e == cudaSuccess && !rc) e = pl->launch(p, pA, pB, d->sms, st);
+  if (e == cudaSuccess && !rc && p.tail_splits > 1)
+    e = launch_tail_reduce(p, pl->BM, pl->BN, st);
   if (auto_ws) ws_release(dev, st);
   if (rc) return rc;
   return e == cudaSuccess ? 0 : B2G_ERR_LAUNCH;
@@ -519,6 +579,21 @@ int run_tf32x3(const Call& c, void* stream) {
 }
 
 }  // namespace
+
+int sgemm_min_workspace_bytes(int M, int N, int K, float alpha, const float* A, int lda,
+                              const float* B, int ldb, const float* C, int ldc, size_t* bytes) {
+  if (!bytes) return B2G_ERR_NULL;
+  Call c{0, 0, M, N, K, alpha, 0.f, A, lda, B, ldb, const_cast<float*>(C), ldc};
+  const int rc = validate(c);
+  if (rc) return rc;
+  *bytes = 0;
+  if (needs_gemm(c)) {
+    const Plan* pl = plan_at(select_plan(c));
+    if (pl) *bytes = plan_base_bytes(*pl, c);
+  }
+  return 0;
+}
+
 }  // namespace b2g
 
 using namespace b2g;
@@ -577,6 +652,33 @@ int b2g_sgemm_workspace_size(int transA, int transB, int M, int N, int K, float 
     const Plan* pl = plan_at(select_plan(c));
     if (pl) *bytes = plan_work_bytes(*pl, c);
   }
+  return 0;
+}
+
+int b2g_sgemm_launch_count(int transA, int transB, int M, int N, int K, float alpha,
+                           const float* A, int lda, const float* B, int ldb, const float* C,
+                           int ldc, int* launches) {
+  if (!launches) return B2G_ERR_NULL;
+  Call c{transA != 0, transB != 0, M, N, K, alpha, 0.f, A, lda, B, ldb, const_cast<float*>(C), ldc};
+  const int rc = validate(c);
+  if (rc) return rc;
+  *launches = 0;
+  if (M == 0 || N == 0) return 0;
+  if (!needs_gemm(c)) {
+    *launches = 1;  // C = beta * C
+    return 0;
+  }
+  const Plan* pl = plan_at(select_plan(c));
+  if (!pl) return B2G_ERR_INVALID_PLAN;
+  int n = 1 + (pl->pretranspose == 1 ? 1 : pl->pretranspose == 2 ? 2 : 0);
+  if (pl->feed == kFeedSkinny) {
+    int kc = 0;
+    if (skinny_splits(*pl, c, &kc) > 1) n += 1;  // the split-K reduction
+  } else {
+    int first = 0;
+    if (tail_split(*pl, c, &first) > 1) n += 1;  // the split tail's reduction
+  }
+  *launches = n;
   return 0;
 }
 

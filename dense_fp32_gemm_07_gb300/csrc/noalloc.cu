@@ -33,27 +33,41 @@ static __device__ __align__(256) float g_noalloc_scratch[kScratchBytes / sizeof(
 std::mutex g_scratch_mu;
 float* g_scratch_addr[b2g::kMaxDevices];  // device address of the array, per device
 
+// Device address of the array on the current device (looked up on the first
+// call there), or an error code.
+int scratch_address(float** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= b2g::kMaxDevices)
+    return B2G_ERR_DEVICE;
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return B2G_ERR_CUDA;
+    g_scratch_addr[dev] = static_cast<float*>(p);
+  }
+  *out = g_scratch_addr[dev];
+  return 0;
+}
+
 }  // namespace
 
 extern "C" int b2g_sgemm_noalloc(int M, int N, int K, float alpha, const float* A, int lda,
                                  const float* B, int ldb, float beta, float* C, int ldc,
                                  void* stream) {
-  size_t need = 0;
-  int rc = b2g_sgemm_workspace_size(0, 0, M, N, K, alpha, A, lda, B, ldb, C, ldc, &need);
+  // `need` is what the plan cannot do without (A^T for the transposing plans);
+  // `want` adds the split tail's partial sums, which take the array's
+  // remaining room when they fit (the plan runs without the split otherwise).
+  size_t need = 0, want = 0;
+  int rc = b2g::sgemm_min_workspace_bytes(M, N, K, alpha, A, lda, B, ldb, C, ldc, &need);
+  if (!rc) rc = b2g_sgemm_workspace_size(0, 0, M, N, K, alpha, A, lda, B, ldb, C, ldc, &want);
   if (rc) return rc;
   if (need > kScratchBytes) return B2G_ERR_SCRATCH_LIMIT;
   float* scratch = nullptr;
-  if (need > 0) {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= b2g::kMaxDevices)
-      return B2G_ERR_DEVICE;
-    std::lock_guard<std::mutex> lk(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {  // first call on this device, which is current
-      void* p = nullptr;
-      if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return B2G_ERR_CUDA;
-      g_scratch_addr[dev] = static_cast<float*>(p);
-    }
-    scratch = g_scratch_addr[dev];
+  size_t give = 0;
+  if (want > 0) {
+    rc = scratch_address(&scratch);
+    if (rc) return rc;
+    give = want < kScratchBytes ? want : kScratchBytes;
   }
-  return b2g_sgemm_ws(0, 0, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, scratch, need, stream);
+  return b2g_sgemm_ws(0, 0, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, scratch, give, stream);
 }

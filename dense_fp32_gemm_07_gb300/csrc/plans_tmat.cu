@@ -19,6 +19,7 @@ const Plan kPlansT[] = {
     B2G_FFMA_PLAN_PRE("pre_128x128x16_s6_o2", 128, 128, 16, 4, 2, 8, 6, 1, 2, 1),
     // any operands: A^T and B packed aligned into a workspace first
     B2G_FFMA_PLAN_PRE("pack_64x128x16_s6_o2", 64, 128, 16, 2, 2, 8, 6, 1, 2, 2),
+    B2G_FFMA_PLAN_PRE("pack_128x64x16_s6_o2", 128, 64, 16, 4, 1, 8, 6, 1, 2, 2),
     B2G_FFMA_PLAN_PRE("pack_128x128x16_s6_o2", 128, 128, 16, 4, 2, 8, 6, 1, 2, 2),
 };
 const int kNumPlansT = sizeof(kPlansT) / sizeof(kPlansT[0]);

@@ -133,6 +133,31 @@ __device__ __forceinline__ void tile_coords(const SgemmParams& p, int tile, int&
   tn = r / gsize;
 }
 
+// Work unit u of the persistent loop: the first tail_first units are whole
+// output tiles (k tiles 0 .. k_tiles-1); with a split tail (tail_splits > 1)
+// every later tile is tail_splits units, slice s covering k tiles
+// [s*k_tiles/S, (s+1)*k_tiles/S).  part is the slice's index among all slices
+// (where its partial sums go), -1 for a whole tile.
+__device__ __forceinline__ void unit_range(const SgemmParams& p, int u, int& tile, int& kt0,
+                                           int& kt1, int& part) {
+  if (p.tail_splits <= 1 || u < p.tail_first) {
+    tile = u, kt0 = 0, kt1 = p.k_tiles, part = -1;
+    return;
+  }
+  const int v = u - p.tail_first;
+  const int S = p.tail_splits;
+  const int s = v % S;
+  tile = p.tail_first + v / S;
+  kt0 = (int)((long long)s * p.k_tiles / S);
+  kt1 = (int)((long long)(s + 1) * p.k_tiles / S);
+  part = v;
+}
+
+__device__ __forceinline__ int total_units(const SgemmParams& p) {
+  const int tiles = p.tiles_m * p.tiles_n * p.batch;
+  return p.tail_splits > 1 ? p.tail_first + (tiles - p.tail_first) * p.tail_splits : tiles;
+}
+
 template <int BM, int BN, int BK, int WM, int WN, int TN, int STAGES, int ALAY, int FEED,
           int PWARPS, int ORD, int KU>
 __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
@@ -161,7 +186,7 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
   }
   __syncthreads();
 
-  const int total_tiles = p.tiles_m * p.tiles_n * p.batch;
+  const int units = total_units(p);
 
   // ------------------------------------------------------------------ producer
   // Producer warps come first (warps 0 .. PWARPS-1), consumers after them.
@@ -173,11 +198,13 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
       if (lane != 0) return;
       prefetch_tmap(&tmA);
       prefetch_tmap(&tmB);
-      for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+      for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        int tile, kt0, kt1, part;
+        unit_range(p, u, tile, kt0, kt1, part);
         int bt, tm, tn;
         tile_coords(p, tile, bt, tm, tn);
         const int m0 = tm * BM, n0 = tn * BN;
-        for (int kt = 0; kt < p.k_tiles; ++kt) {
+        for (int kt = kt0; kt < kt1; ++kt) {
           if (p.debug_stop_ktile >= 0 && issued >= p.debug_stop_ktile) goto drain_tma;
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, p.wait_limit_ns, p.status,
                          kStatusTimeoutEmpty))
@@ -207,13 +234,15 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
       }
     } else {
       const int pt = threadIdx.x;
-      for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+      for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        int tile, kt0, kt1, part;
+        unit_range(p, u, tile, kt0, kt1, part);
         int bt, tm, tn;
         tile_coords(p, tile, bt, tm, tn);
         const int m0 = tm * BM, n0 = tn * BN;
         const float* Ab = p.A + (long long)bt * p.strideA;
         const float* Bb = p.B + (long long)bt * p.strideB;
-        for (int kt = 0; kt < p.k_tiles; ++kt) {
+        for (int kt = kt0; kt < kt1; ++kt) {
           if (p.debug_stop_ktile >= 0 && issued >= p.debug_stop_ktile) goto drain_cp;
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, p.wait_limit_ns, p.status,
                          kStatusTimeoutEmpty))
@@ -295,9 +324,11 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
     }
   };
   if constexpr (Cfg::kStaged) {
-    const int my_tiles =
-        blockIdx.x < total_tiles ? (total_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-    total_stages = (long long)my_tiles * p.k_tiles;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      int tile, kt0, kt1, part;
+      unit_range(p, u, tile, kt0, kt1, part);
+      total_stages += kt1 - kt0;
+    }
     if (total_stages > 0) {
       if (!mbar_wait(full0, 0, p.wait_limit_ns, p.status, kStatusTimeoutFull)) return;
       x_load(0);
@@ -306,7 +337,9 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
     }
   }
 
-  for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    int tile, kt0, kt1, part;
+    unit_range(p, u, tile, kt0, kt1, part);
     int bt, tm, tn;
     tile_coords(p, tile, bt, tm, tn);
     float acc[8][TN];
@@ -315,7 +348,7 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
 #pragma unroll
       for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
 
-    for (int kt = 0; kt < p.k_tiles; ++kt) {
+    for (int kt = kt0; kt < kt1; ++kt) {
       const float* As;
       bool next = false;
       if constexpr (Cfg::kStaged) {
@@ -383,20 +416,27 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
     }
 
     // Epilogue: C = alpha*acc + beta*C, C read only when beta != 0, float4
-    // where the 4 columns are in range and C is 16-byte aligned.
-    const int m0 = tm * BM, n0 = tn * BN;
-    const float alpha = p.alpha, beta = p.beta;
+    // where the 4 columns are in range and C is 16-byte aligned.  A slice of a
+    // split tile instead stores its raw sums (alpha 1, beta 0: exact) as a
+    // whole BM x BN block with leading dimension BN for the tail reduction.
+    const bool slice = part >= 0;
+    float* const cb = slice ? p.work + (size_t)part * (BM * BN) : p.C + (long long)bt * p.strideC;
+    const long long ldc = slice ? BN : p.ldc;
+    const int m0 = slice ? 0 : tm * BM, n0 = slice ? 0 : tn * BN;
+    const int mlim = slice ? BM : p.M, nlim = slice ? BN : p.N;
+    const bool vec4 = slice || p.c_vec4;
+    const float alpha = slice ? 1.f : p.alpha, beta = slice ? 0.f : p.beta;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int r = m0 + ((ALAY == kAKChunk) ? wm * 32 + tr + 4 * i
                                             : wm * 32 + 4 * tr + (i & 3) + 16 * (i >> 2));
-      if (r >= p.M) continue;
-      float* crow = p.C + (long long)bt * p.strideC + (long long)r * p.ldc;
+      if (r >= mlim) continue;
+      float* crow = cb + (long long)r * ldc;
 #pragma unroll
       for (int j4 = 0; j4 < TN / 4; ++j4) {
         const int c = n0 + b_off + 32 * j4;
         const float* av = &acc[i][4 * j4];
-        if (p.c_vec4 && c + 3 < p.N) {
+        if (vec4 && c + 3 < nlim) {
           float4 o;
           if (beta != 0.f) {
             const float4 cv = *reinterpret_cast<const float4*>(crow + c);
@@ -411,7 +451,7 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
         } else {
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            if (c + e < p.N) {
+            if (c + e < nlim) {
               float* q = crow + c + e;
               *q = (beta != 0.f) ? fmaf(alpha, av[e], beta * *q) : alpha * av[e];
             }
@@ -422,30 +462,43 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
   }
 }
 
+// CTAs of one plan resident per SM on the current device, queried once per
+// device (after opting in to the plan's dynamic shared memory); 0 on failure.
+template <int BM, int BN, int BK, int WM, int WN, int TN, int STAGES, int ALAY, int FEED,
+          int PWARPS, int ORD, int KU = BK>
+int ffma_occupancy() {
+  using Cfg = FfmaCfg<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS, ORD, KU>;
+  auto kern = sgemm_ffma_kernel<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS, ORD, KU>;
+  static std::atomic<int> resident[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  int occ = resident[dev].load(std::memory_order_acquire);
+  if (occ == 0) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg::kSmemBytes) != cudaSuccess)
+      return 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, Cfg::kThreads,
+                                                      Cfg::kSmemBytes) != cudaSuccess ||
+        occ < 1)
+      return 0;
+    resident[dev].store(occ, std::memory_order_release);
+  }
+  return occ;
+}
+
 template <int BM, int BN, int BK, int WM, int WN, int TN, int STAGES, int ALAY, int FEED,
           int PWARPS, int ORD, int KU = BK>
 cudaError_t launch_ffma(const SgemmParams& p, const CUtensorMap* tmA, const CUtensorMap* tmB,
                         int num_sms, cudaStream_t stream) {
   using Cfg = FfmaCfg<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS, ORD, KU>;
   auto kern = sgemm_ffma_kernel<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS, ORD, KU>;
-  // Per device, once: opt in to the dynamic shared memory size and record how
-  // many CTAs fit on one SM (the persistent grid is SMs x that).
-  static std::atomic<int> resident[kMaxDevices];
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  int occ = resident[dev].load(std::memory_order_acquire);
-  if (occ == 0) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, Cfg::kThreads, Cfg::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    if (occ < 1) return cudaErrorInvalidConfiguration;
-    resident[dev].store(occ, std::memory_order_release);
-  }
+  // The persistent grid is SMs x resident CTAs, or one CTA per work unit.
+  const int occ = ffma_occupancy<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS, ORD, KU>();
+  if (occ < 1) return cudaErrorInvalidConfiguration;
   const long long tiles = (long long)p.tiles_m * p.tiles_n * p.batch;
-  const int grid = (int)std::min<long long>(tiles, (long long)num_sms * occ);
+  const long long units =
+      p.tail_splits > 1 ? p.tail_first + (tiles - p.tail_first) * p.tail_splits : tiles;
+  const int grid = (int)std::min<long long>(units, (long long)num_sms * occ);
   CUtensorMap none;
   memset(&none, 0, sizeof(none));
   SgemmParams pc = p;
@@ -460,7 +513,8 @@ cudaError_t launch_ffma(const SgemmParams& p, const CUtensorMap* tmA, const CUte
     NAME, BM, BN, BK, ST, TN, ALAY, FEED,                                                        \
         FfmaCfg<BM, BN, BK, WM, WN, TN, ST, ALAY, FEED, PW, ORD>::kThreads,                      \
         FfmaCfg<BM, BN, BK, WM, WN, TN, ST, ALAY, FEED, PW, ORD>::kSmemBytes,                    \
-        &launch_ffma<BM, BN, BK, WM, WN, TN, ST, ALAY, FEED, PW, ORD>, 0, nullptr                \
+        &launch_ffma<BM, BN, BK, WM, WN, TN, ST, ALAY, FEED, PW, ORD>, 0,                        \
+        &ffma_occupancy<BM, BN, BK, WM, WN, TN, ST, ALAY, FEED, PW, ORD>                         \
   }
 
 // The same kernel behind a transpose of row-major A (PRE = 1) or a packing of
@@ -470,7 +524,8 @@ cudaError_t launch_ffma(const SgemmParams& p, const CUtensorMap* tmA, const CUte
     NAME, BM, BN, BK, ST, TN, kAKMajor, kFeedTMA,                                                \
         FfmaCfg<BM, BN, BK, WM, WN, TN, ST, kAKMajor, kFeedTMA, PW, ORD>::kThreads,              \
         FfmaCfg<BM, BN, BK, WM, WN, TN, ST, kAKMajor, kFeedTMA, PW, ORD>::kSmemBytes,            \
-        &launch_ffma<BM, BN, BK, WM, WN, TN, ST, kAKMajor, kFeedTMA, PW, ORD>, PRE, nullptr      \
+        &launch_ffma<BM, BN, BK, WM, WN, TN, ST, kAKMajor, kFeedTMA, PW, ORD>, PRE,              \
+        &ffma_occupancy<BM, BN, BK, WM, WN, TN, ST, kAKMajor, kFeedTMA, PW, ORD>                 \
   }
 
 }  // namespace b2g

@@ -25,9 +25,15 @@ struct SgemmParams {
   unsigned int* status;              // device status word (timeout flags)
   int batch;                         // independent problems (strided batched); 1 otherwise
   long long strideA, strideB, strideC;  // elements between consecutive problems
-  float* work;                       // split-K partial sums (skinny plans), or null
+  float* work;                       // partial sums (skinny split-K, FFMA split tail), or null
   int splits;                        // split-K factor (skinny plans); 1 = no split
   int kc;                            // k extent of one split (skinny plans)
+  // FFMA plans' split tail: output tiles tail_first .. tiles-1 are each cut
+  // into tail_splits k slices (tail_splits == 1: none).  A slice writes its raw
+  // BM x BN sums to work + (slice unit index) * BM * BN; launch_tail_reduce
+  // then adds each tile's slices in order and applies the epilogue.
+  int tail_first;
+  int tail_splits;
 };
 
 // How A is laid out in one shared-memory stage.
@@ -65,7 +71,7 @@ struct Plan {
                      // operands are packed into a workspace first (A^T and B, aligned,
                      // from any alignment, leading dimension or op() flags)
   int (*occupancy)();  // CTAs of this plan resident per SM on the current device (0 on
-                       // failure); set for plans whose host side sizes a split by it
+                       // failure); the host sizes split-K and split tails by it
 };
 
 // Skinny-M plans (M <= BM), compiled in skinny.cu.
@@ -73,6 +79,18 @@ extern const Plan kPlansSkinny[];
 extern const int kNumPlansSkinny;
 // C = alpha * sum_s P[s] + beta * C over the M x N window (split-K reduction).
 cudaError_t launch_splitk_reduce(const SgemmParams& p, cudaStream_t stream, int num_sms);
+
+// FFMA plans' split tail: C = alpha * (slice 0 + slice 1 + ...) + beta * C for
+// every split tile (p.tail_splits > 1), BM x BN the plan's tile.
+cudaError_t launch_tail_reduce(const SgemmParams& p, int BM, int BN, cudaStream_t stream);
+
+// Workspace bytes that the tune table's plan cannot do without for these
+// row-major arguments (A^T for the transposing plans; 0 when none).  It is at
+// most what b2g_sgemm_workspace_size reports, which adds room for the split
+// tail's partial sums; with less than that the plan runs without the split.
+// Returns 0 or a B2G_ERR_* code.
+int sgemm_min_workspace_bytes(int M, int N, int K, float alpha, const float* A, int lda,
+                              const float* B, int ldb, const float* C, int ldc, size_t* bytes);
 
 // Plans compiled in each kernel translation unit.
 extern const Plan kPlansTMA[];

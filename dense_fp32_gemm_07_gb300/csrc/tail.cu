@@ -1,0 +1,79 @@
+// tail.cu -- the second half of the FFMA plans' split tail.
+//
+// A persistent grid of G CTAs that runs T output tiles finishes when its
+// busiest SM does: with T = q*G + r (0 < r < G) the last round keeps only r
+// CTAs busy.  The host therefore cuts each of the last r tiles into S k slices
+// (S = G / r, at least 128 k per slice), so every CTA gets q whole tiles plus
+// at most one slice.  The GEMM kernel writes each slice's raw BM x BN sums to
+// the workspace; this kernel adds a tile's S slices in slice order (a fixed
+// order: results are reproducible run to run) and applies the same epilogue
+// as the GEMM kernel, C = alpha * sum + beta * C, reading C only when
+// beta != 0.
+#include <cuda_runtime.h>
+
+#include "sgemm_ffma.cuh"
+
+namespace b2g {
+
+// blockIdx.x: split tile (tail_first + blockIdx.x); blockIdx.y and the
+// threads stride over the tile's BM x BN / 4 float4 positions.
+__global__ void __launch_bounds__(256) tail_reduce_kernel(const __grid_constant__ SgemmParams p,
+                                                          int BM, int BN) {
+  int b, tm, tn;
+  tile_coords(p, p.tail_first + (int)blockIdx.x, b, tm, tn);
+  const int S = p.tail_splits;
+  const size_t tile_elems = (size_t)BM * BN;
+  const float* __restrict__ P = p.work + (size_t)blockIdx.x * S * tile_elems;
+  float* __restrict__ Cb = p.C + (long long)b * p.strideC;
+  const int n4 = BN / 4;
+  const int m0 = tm * BM, n0 = tn * BN;
+  const float alpha = p.alpha, beta = p.beta;
+  for (int q = blockIdx.y * blockDim.x + threadIdx.x; q < BM * n4;
+       q += gridDim.y * blockDim.x) {
+    const int r = q / n4, c = (q - r * n4) * 4;
+    const int gr = m0 + r, gc = n0 + c;
+    if (gr >= p.M || gc >= p.N) continue;
+    float4 acc = *reinterpret_cast<const float4*>(P + (size_t)q * 4);
+    for (int s = 1; s < S; ++s) {
+      const float4 v = *reinterpret_cast<const float4*>(P + s * tile_elems + (size_t)q * 4);
+      acc.x += v.x, acc.y += v.y, acc.z += v.z, acc.w += v.w;
+    }
+    const float av[4] = {acc.x, acc.y, acc.z, acc.w};
+    float* crow = Cb + (long long)gr * p.ldc;
+    if (p.c_vec4 && gc + 3 < p.N) {
+      float4 o;
+      if (beta != 0.f) {
+        const float4 cv = *reinterpret_cast<const float4*>(crow + gc);
+        o.x = fmaf(alpha, av[0], beta * cv.x);
+        o.y = fmaf(alpha, av[1], beta * cv.y);
+        o.z = fmaf(alpha, av[2], beta * cv.z);
+        o.w = fmaf(alpha, av[3], beta * cv.w);
+      } else {
+        o.x = alpha * av[0], o.y = alpha * av[1], o.z = alpha * av[2], o.w = alpha * av[3];
+      }
+      *reinterpret_cast<float4*>(crow + gc) = o;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (gc + e < p.N) {
+          float* o = crow + gc + e;
+          *o = (beta != 0.f) ? fmaf(alpha, av[e], beta * *o) : alpha * av[e];
+        }
+      }
+    }
+  }
+}
+
+cudaError_t launch_tail_reduce(const SgemmParams& p, int BM, int BN, cudaStream_t stream) {
+  const long long tiles = (long long)p.tiles_m * p.tiles_n * p.batch;
+  const long long n = tiles - p.tail_first;
+  if (p.tail_splits <= 1 || n <= 0) return cudaSuccess;
+  // two float4 positions per thread
+  const unsigned gy = (unsigned)((BM * BN / 4 + 511) / 512);
+  SgemmParams pc = p;
+  void* args[] = {&pc, &BM, &BN};
+  return cudaLaunchKernel(reinterpret_cast<const void*>(&tail_reduce_kernel),
+                          dim3((unsigned)n, gy), dim3(256), args, 0, stream);
+}
+
+}  // namespace b2g

@@ -1,17 +1,19 @@
 """Per-plan timing sweep behind the shape-keyed tune table (csrc/tune_table.h).
 
-    python -m dense_fp32_gemm_07_gb300.tune [--once] MxNxK[xALPHAxBETA] ...
+    python -m dense_fp32_gemm_07_gb300.tune [--once] [--plans REGEX] MxNxK[xALPHAxBETA] ...
 
 Times every compiled plan that accepts the operands on each shape (CUDA events
 on the launching stream, after warm-up, operands uniform[-1, 1) made by
 torch), prints TFLOP/s per plan and marks the one the table picks.  Plans
 that read A stored K x M (tmaT_*) get a transposed copy of A.  With --once
 every plan runs exactly one launch per shape and nothing is timed: that is the
-form to run under ncu to compare plans' counters.
+form to run under ncu to compare plans' counters.  --plans keeps only the
+plans whose name matches REGEX (re.search); the table's plan is always kept.
 """
 from __future__ import annotations
 
 import argparse
+import re
 import sys
 
 import dense_fp32_gemm_07_gb300 as b2g
@@ -25,7 +27,7 @@ def parse_shape(s: str):
     return M, N, K, alpha, beta
 
 
-def sweep(shapes, once=False, out=sys.stdout):
+def sweep(shapes, once=False, out=sys.stdout, pattern=None):
     import torch
 
     from dense_fp32_gemm_07_gb300 import build
@@ -42,6 +44,8 @@ def sweep(shapes, once=False, out=sys.stdout):
         sel = b2g.b2g_sgemm_select_plan(0, 0, M, N, K, alpha, A.data_ptr(), K, B.data_ptr(), N,
                                         C.data_ptr(), N)
         for pi, name in enumerate(names):
+            if pattern and pi != sel and not re.search(pattern, name):
+                continue
             trans = name.startswith("tmaT")
 
             def call():
@@ -74,8 +78,9 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("shapes", nargs="*", default=["4096x4096x4096x1x0.5"])
     ap.add_argument("--once", action="store_true")
+    ap.add_argument("--plans", default=None, help="regex: time only the matching plans")
     args = ap.parse_args()
-    sweep([parse_shape(s) for s in args.shapes], once=args.once)
+    sweep([parse_shape(s) for s in args.shapes], once=args.once, pattern=args.plans)
 
 
 if __name__ == "__main__":

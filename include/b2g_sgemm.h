@@ -68,6 +68,14 @@ extern "C" {
  * CUDA graph, or when the allocation fails, the call takes a plan that needs no
  * workspace instead.  b2g_sgemm_ws lets the caller supply the workspace and
  * never allocates; b2g_release_workspaces frees the library-owned ones.
+ *
+ * Split tail: a persistent grid of G CTAs over T output tiles, T = q*G + r
+ * with 0 < r < G, would keep only r CTAs busy in its last round.  The last r
+ * tiles are then cut into S = G / r k slices (at least 128 k each) whose
+ * partial sums go to the workspace, after A^T, and a second kernel adds each
+ * tile's slices in slice order and applies the epilogue.  The summation order
+ * is fixed for given arguments, so results stay reproducible run to run; the
+ * result bound is unchanged.  Without a workspace the tiles run whole.
  */
 int b2g_sgemm(int M, int N, int K, float alpha, const float* A, int lda, const float* B, int ldb,
               float beta, float* C, int ldc, void* stream);
@@ -97,10 +105,12 @@ int b2g_sgemm_strided_batched(int transA, int transB, int M, int N, int K, float
 
 /*
  * As b2g_sgemm_ex with a caller-owned device workspace of workspace_bytes
- * (16-byte aligned).  Never allocates.  When the workspace is NULL or smaller
- * than b2g_sgemm_workspace_size reports, a plan that needs none runs instead
- * (slower, same result bound).  The caller orders reuse of the workspace
- * across streams.
+ * (16-byte aligned).  Never allocates.  With at least what
+ * b2g_sgemm_workspace_size reports, the tune table's plan runs with its split
+ * tail; with less, but room for A^T (K x round_up(M, 4) floats) when the plan
+ * transposes A first, it runs without the split tail; with less than that, or
+ * a NULL workspace, a plan that needs none runs instead (slower, same result
+ * bound).  The caller orders reuse of the workspace across streams.
  */
 int b2g_sgemm_ws(int transA, int transB, int M, int N, int K, float alpha, const float* A, int lda,
                  const float* B, int ldb, float beta, float* C, int ldc, void* workspace,
@@ -108,12 +118,28 @@ int b2g_sgemm_ws(int transA, int transB, int M, int N, int K, float alpha, const
 
 /*
  * Workspace bytes the tune table's plan wants for these arguments (0 when it
- * needs none), stored in *bytes.  Returns 0, a B2G_ERR_* code for invalid
+ * needs none), stored in *bytes: A^T or the packed operands when the plan
+ * writes them, then (256-byte aligned) the split tail's partial sums, at most
+ * SMs x resident CTAs x BM x BN floats.  The split depends on the current
+ * device's SM count and occupancy.  Returns 0, a B2G_ERR_* code for invalid
  * arguments, or B2G_ERR_NULL when bytes is NULL.  Launches nothing.
  */
 int b2g_sgemm_workspace_size(int transA, int transB, int M, int N, int K, float alpha,
                              const float* A, int lda, const float* B, int ldb, const float* C,
                              int ldc, size_t* bytes);
+
+/*
+ * Number of kernel launches that one b2g_sgemm_ex call with these arguments
+ * makes when the workspace can be had, stored in *launches: 0 when M or N is
+ * 0, 1 when only C is scaled, else the GEMM kernel plus the plan's prepasses
+ * (1 transpose, or 2 packing launches) plus 1 when a split-K or split-tail
+ * reduction follows.  Depends on the current device like the split itself.
+ * Returns 0, a B2G_ERR_* code for invalid arguments, or B2G_ERR_NULL when
+ * launches is NULL.  Launches nothing.
+ */
+int b2g_sgemm_launch_count(int transA, int transB, int M, int N, int K, float alpha,
+                           const float* A, int lda, const float* B, int ldb, const float* C,
+                           int ldc, int* launches);
 
 /*
  * Free the library-owned workspaces of all devices, after waiting for the
@@ -127,9 +153,10 @@ int b2g_release_workspaces(void);
  * that must not have the library allocate device memory -- for instance an
  * application whose allocator reserved device memory at start-up and forbids
  * later cudaMalloc / cudaMallocAsync calls.  It never allocates: its scratch
- * (A^T for the plans that transpose A first) is a fixed 64 MiB array that every
- * device loading the library holds until the process exits.
- *   - Calls whose scratch need, K x round_up(M, 4) floats for those plans,
+ * (A^T for the plans that transpose A first, then the split tail's partial
+ * sums when they fit) is a fixed 64 MiB array that every device loading the
+ * library holds until the process exits.
+ *   - Calls whose A^T, K x round_up(M, 4) floats for those plans,
  *     exceeds 64 MiB (16,777,216 floats) are rejected with
  *     B2G_ERR_SCRATCH_LIMIT and launch nothing; use b2g_sgemm_ws with your own
  *     buffer for them.

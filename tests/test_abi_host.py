@@ -122,26 +122,90 @@ def test_tune_table_classes(b2g):
     assert _plan(b2g, 0, 1, 512, 512, 512, 1.0, FAKE, 512, FAKE, 512, FAKE, 512).startswith("pack_")
 
 
+# With no device answering, the host sizes splits for 152 SMs x 4 resident CTAs.
+NO_DEVICE_SLOTS = 152 * 4
+
+
+def split_tail(M, N, K, BM, BN, slots=NO_DEVICE_SLOTS):
+    """(first split tile, slices) of the split-tail rule: T tiles over G slots,
+    T = q*G + r; the last r tiles get S = G // r slices of at least 128 k."""
+    T = -(-M // BM) * -(-N // BN)
+    q, r = divmod(T, slots)
+    if r == 0:
+        return 0, 1
+    S = min(slots // r, K // 128)
+    return (q * slots, S) if S >= 2 else (0, 1)
+
+
+def want_bytes(base, M, N, K, BM, BN):
+    first, S = split_tail(M, N, K, BM, BN)
+    if S == 1:
+        return base
+    T = -(-M // BM) * -(-N // BN)
+    return -(-base // 256) * 256 + (T - first) * S * BM * BN * 4
+
+
+def plan_tile(b2g, M, N, K, lda, ldb, ldc):
+    pi = b2g.b2g_sgemm_select_plan(0, 0, M, N, K, 1.0, FAKE, lda, FAKE, ldb, FAKE, ldc)
+    info = b2g.b2g_plan_info(pi)
+    return info["BM"], info["BN"]
+
+
+def test_split_tail_rule_examples():
+    # 4096^3 on 128 x 64 tiles: 2048 = 3 * 608 + 224 -> the last 224 tiles in 2 slices
+    assert split_tail(4096, 4096, 4096, 128, 64) == (1824, 2)
+    assert split_tail(4096, 4096, 4096, 128, 64, slots=456) == (1824, 2)
+    # 2048^3 on 64 x 128 tiles over 456 slots: 512 = 456 + 56 -> 8 slices
+    assert split_tail(2048, 2048, 2048, 64, 128, slots=456) == (456, 8)
+    # whole waves, too little k, or r too large for 2 slices: no split
+    assert split_tail(64 * 608, 128, 4096, 64, 128) == (0, 1)
+    assert split_tail(4096, 4096, 255, 128, 64) == (0, 1)
+    assert split_tail(4096, 640, 4096, 128, 64) == (0, 1)  # 320 tiles > 608 / 2
+
+
 def test_workspace_size_query(b2g):
+    BM, BN = plan_tile(b2g, 4096, 4096, 4096, 4096, 4096, 4096)
     rc, n = b2g.b2g_sgemm_workspace_size(0, 0, 4096, 4096, 4096, 1.0, FAKE, 4096, FAKE, 4096,
                                          FAKE, 4096)
-    assert rc == 0 and n == 4096 * 4096 * 4  # A^T, K x round_up(M, 4) floats
+    # A^T (K x round_up(M, 4) floats), then the split tail's partial sums
+    assert rc == 0 and n == want_bytes(4096 * 4096 * 4, 4096, 4096, 4096, BM, BN)
+    assert n > 4096 * 4096 * 4
+    BM, BN = plan_tile(b2g, 1001, 4096, 4096, 4096, 4096, 4096)
     rc, n = b2g.b2g_sgemm_workspace_size(0, 0, 1001, 4096, 4096, 1.0, FAKE, 4096, FAKE, 4096,
                                          FAKE, 4096)
-    assert rc == 0 and n == 4096 * 1004 * 4
+    assert rc == 0 and n == want_bytes(4096 * 1004 * 4, 1001, 4096, 4096, BM, BN)
     rc, n = b2g.b2g_sgemm_workspace_size(0, 0, 64, 64, 64, 1.0, FAKE, 64, FAKE, 64, FAKE, 64)
-    assert rc == 0 and n == 0
+    assert rc == 0 and n == 0  # one tile, 64 k: nothing to split
     # skinny: split-K partial sums, S x M x N floats for some S > 1
     rc, n = b2g.b2g_sgemm_workspace_size(0, 0, 16, 4096, 4096, 1.0, FAKE, 4096, FAKE, 4096,
                                          FAKE, 4096)
     assert rc == 0 and n > 0 and n % (16 * 4096 * 4) == 0
     rc, n = b2g.b2g_sgemm_workspace_size(0, 0, 64, 64, 64, 1.0, FAKE, 63, FAKE, 64, FAKE, 64)
     assert rc == -2
-    # packing: A^T (K x round_up(M, 4)) and B (K x round_up(N, 4))
+    # packing: A^T (K x round_up(M, 4)) and B (K x round_up(N, 4)), then the tail
+    BM, BN = plan_tile(b2g, 1000, 1025, 777, 777, 1025, 1025)
     rc, n = b2g.b2g_sgemm_workspace_size(0, 0, 1000, 1025, 777, 1.0, FAKE, 777, FAKE, 1025,
                                          FAKE, 1025)
-    assert rc == 0 and n == 777 * (1000 + 1028) * 4
+    assert rc == 0 and n == want_bytes(777 * (1000 + 1028) * 4, 1000, 1025, 777, BM, BN)
     assert b2g.b2g_release_workspaces() == 0  # nothing allocated yet: no CUDA call needed
+
+
+def test_launch_count_query(b2g):
+    def count(M, N, K, alpha=1.0, lda=None, ldb=None, ldc=None):
+        lda, ldb, ldc = lda or max(K, 1), ldb or max(N, 1), ldc or max(N, 1)
+        rc, n = b2g.b2g_sgemm_launch_count(0, 0, M, N, K, alpha, FAKE, lda, FAKE, ldb, FAKE,
+                                           ldc)
+        assert rc == 0
+        return n
+
+    assert count(0, 64, 64) == 0 and count(64, 0, 64) == 0
+    assert count(64, 64, 64, alpha=0.0) == 1 and count(64, 64, 0) == 1  # C = beta * C
+    assert count(64, 64, 64) == 1                    # one tile, one kernel
+    assert count(4096, 4096, 4096) == 3              # transpose, GEMM, tail reduction
+    assert count(16, 4096, 4096) == 2                # skinny split-K and its reduction
+    assert count(1000, 1025, 777, lda=777) == 4      # two packing launches, GEMM, tail
+    rc, _ = b2g.b2g_sgemm_launch_count(0, 0, 64, 64, 64, 1.0, FAKE, 63, FAKE, 64, FAKE, 64)
+    assert rc == -2
 
 
 def test_forced_plan_range(b2g):
