@@ -36,8 +36,9 @@ UNIT = "TFLOP/s"
 SMS, LANES, MAX_MHZ = 152, 128, 2070.0
 L2_BYTES = 129e6
 # device code of the dominant kernel: a change here voids the recorded traffic
-KERNEL_SOURCES = ("csrc/sgemm_ffma.cuh", "csrc/ptx.cuh", "csrc/plans_tmat.cu",
-                  "csrc/sgemm_params.h")
+# The recorded traffic is valid while these headers and the translation unit
+# that compiles the plan's kernel are unchanged.
+KERNEL_HEADERS = ("csrc/sgemm_ffma.cuh", "csrc/ptx.cuh", "csrc/sgemm_params.h")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_square4096.txt")
 
 
@@ -60,10 +61,21 @@ def fp32_peak_tflops(mhz: float) -> float:
     return SMS * LANES * 2 * mhz * 1e6 / 1e12
 
 
-def kernel_sources_hash() -> str:
+def kernel_unit(plan: str) -> str:
+    """The csrc/*.cu file that defines `plan` (and compiles its kernel)."""
+    csrc = os.path.join(ROOT, "dense_fp32_gemm_07_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith(".cu"):
+            with open(os.path.join(csrc, f)) as fh:
+                if f'"{plan}"' in fh.read():
+                    return "csrc/" + f
+    raise KeyError(plan)
+
+
+def kernel_sources_hash(plan: str) -> str:
     h = hashlib.sha256()
     pkg = os.path.join(ROOT, "dense_fp32_gemm_07_gb300")
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_HEADERS + (kernel_unit(plan),):
         with open(os.path.join(pkg, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -79,7 +91,7 @@ def recorded_traffic(plan: str):
                 if ":" in line and not line.startswith("#"):
                     k, v = line.split(":", 1)
                     kv[k.strip()] = v.strip()
-        if kv.get("kernel_sources_sha256") != kernel_sources_hash() or kv.get("plan") != plan:
+        if kv.get("plan") != plan or kv.get("kernel_sources_sha256") != kernel_sources_hash(plan):
             return None
         return float(kv["dram_bytes_per_launch"])
     except (OSError, KeyError, ValueError):

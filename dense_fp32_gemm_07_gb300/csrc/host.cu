@@ -151,17 +151,30 @@ void ws_release(int dev, cudaStream_t st) {
   w.mu.unlock();
 }
 
-int num_plans() { return kNumPlansTMA + kNumPlansT + kNumPlansGeneral + kNumPlansSkinny; }
+// Every compiled plan, indexed in this order.
+struct PlanGroup {
+  const Plan* plans;
+  const int* count;
+};
+const PlanGroup kGroups[] = {
+    {kPlansTMA, &kNumPlansTMA},         {kPlansT, &kNumPlansT},
+    {kPlansT64x128, &kNumPlansT64x128}, {kPlansT128x64, &kNumPlansT128x64},
+    {kPlansT128x128, &kNumPlansT128x128}, {kPlansGeneral, &kNumPlansGeneral},
+    {kPlansSkinny, &kNumPlansSkinny},
+};
+
+int num_plans() {
+  int n = 0;
+  for (const PlanGroup& g : kGroups) n += *g.count;
+  return n;
+}
 
 const Plan* plan_at(int i) {
   if (i < 0) return nullptr;
-  if (i < kNumPlansTMA) return &kPlansTMA[i];
-  i -= kNumPlansTMA;
-  if (i < kNumPlansT) return &kPlansT[i];
-  i -= kNumPlansT;
-  if (i < kNumPlansGeneral) return &kPlansGeneral[i];
-  i -= kNumPlansGeneral;
-  if (i < kNumPlansSkinny) return &kPlansSkinny[i];
+  for (const PlanGroup& g : kGroups) {
+    if (i < *g.count) return &g.plans[i];
+    i -= *g.count;
+  }
   return nullptr;
 }
 

@@ -77,11 +77,15 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 
 // Slow path of a bounded wait: poll until the phase with `parity` completes or
 // `limit_ns` of wall time has passed; on timeout OR `flag` into *status.
+// sleep_ns > 0 backs off between polls (fewer issue slots taken from the
+// other warps of the SM sub-partition while waiting).
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, uint64_t limit_ns,
-                                            unsigned int* status, unsigned int flag) {
+                                            unsigned int* status, unsigned int flag,
+                                            uint32_t sleep_ns) {
   const uint64_t t0 = global_ns();
   for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (sleep_ns) __nanosleep(sleep_ns);
     if ((it & 63u) == 63u && global_ns() - t0 > limit_ns) {
       atomicOr(status, flag);
       return false;
@@ -92,9 +96,10 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
 // Wait for the phase with `parity` of barrier `bar`.  One try on the fast path,
 // the timed loop only when the data is not there yet.  Returns false on timeout.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns,
-                                          unsigned int* status, unsigned int flag) {
+                                          unsigned int* status, unsigned int flag,
+                                          uint32_t sleep_ns = 0) {
   if (mbar_try_wait(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity, limit_ns, status, flag);
+  return mbar_wait_slow(bar, parity, limit_ns, status, flag, sleep_ns);
 }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {

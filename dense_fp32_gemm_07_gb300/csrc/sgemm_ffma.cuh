@@ -39,7 +39,7 @@
 namespace b2g {
 
 template <int BM, int BN, int BK, int WM, int WN, int TN, int STAGES, int ALAY, int FEED,
-          int PWARPS, int ORD = 0, int KU = BK>
+          int PWARPS, int ORD = 0>
 struct FfmaCfg {
   static constexpr int TM = 8;
   static constexpr int kConsumerWarps = WM * WN;
@@ -159,12 +159,12 @@ __device__ __forceinline__ int total_units(const SgemmParams& p) {
 }
 
 template <int BM, int BN, int BK, int WM, int WN, int TN, int STAGES, int ALAY, int FEED,
-          int PWARPS, int ORD, int KU>
+          int PWARPS, int ORD>
 __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
     sgemm_ffma_kernel(const __grid_constant__ SgemmParams p,
                       const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB) {
-  using Cfg = FfmaCfg<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS, ORD, KU>;
+  using Cfg = FfmaCfg<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS, ORD>;
   extern __shared__ __align__(1024) unsigned char smem[];
   float* sA = reinterpret_cast<float*>(smem);
   float* sB = sA + STAGES * Cfg::kAStage;
@@ -391,8 +391,7 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
           }
         }
       } else {
-        // KU < BK keeps the loop body (and the instruction footprint) smaller
-#pragma unroll KU
+#pragma unroll
         for (int k = 0; k < BK; ++k) {
           const float4 a0 = *reinterpret_cast<const float4*>(As + k * Cfg::kARow);
           const float4 a1 = *reinterpret_cast<const float4*>(As + k * Cfg::kARow + 16);
@@ -465,10 +464,10 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
 // CTAs of one plan resident per SM on the current device, queried once per
 // device (after opting in to the plan's dynamic shared memory); 0 on failure.
 template <int BM, int BN, int BK, int WM, int WN, int TN, int STAGES, int ALAY, int FEED,
-          int PWARPS, int ORD, int KU = BK>
+          int PWARPS, int ORD>
 int ffma_occupancy() {
-  using Cfg = FfmaCfg<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS, ORD, KU>;
-  auto kern = sgemm_ffma_kernel<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS, ORD, KU>;
+  using Cfg = FfmaCfg<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS, ORD>;
+  auto kern = sgemm_ffma_kernel<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS, ORD>;
   static std::atomic<int> resident[kMaxDevices];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
@@ -487,13 +486,13 @@ int ffma_occupancy() {
 }
 
 template <int BM, int BN, int BK, int WM, int WN, int TN, int STAGES, int ALAY, int FEED,
-          int PWARPS, int ORD, int KU = BK>
+          int PWARPS, int ORD>
 cudaError_t launch_ffma(const SgemmParams& p, const CUtensorMap* tmA, const CUtensorMap* tmB,
                         int num_sms, cudaStream_t stream) {
-  using Cfg = FfmaCfg<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS, ORD, KU>;
-  auto kern = sgemm_ffma_kernel<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS, ORD, KU>;
+  using Cfg = FfmaCfg<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS, ORD>;
+  auto kern = sgemm_ffma_kernel<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS, ORD>;
   // The persistent grid is SMs x resident CTAs, or one CTA per work unit.
-  const int occ = ffma_occupancy<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS, ORD, KU>();
+  const int occ = ffma_occupancy<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS, ORD>();
   if (occ < 1) return cudaErrorInvalidConfiguration;
   const long long tiles = (long long)p.tiles_m * p.tiles_n * p.batch;
   const long long units =

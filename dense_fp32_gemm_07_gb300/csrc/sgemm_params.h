@@ -97,6 +97,12 @@ extern const Plan kPlansTMA[];
 extern const int kNumPlansTMA;
 extern const Plan kPlansT[];
 extern const int kNumPlansT;
+extern const Plan kPlansT64x128[];
+extern const int kNumPlansT64x128;
+extern const Plan kPlansT128x64[];
+extern const int kNumPlansT128x64;
+extern const Plan kPlansT128x128[];
+extern const int kNumPlansT128x128;
 extern const Plan kPlansGeneral[];
 extern const int kNumPlansGeneral;
 
