@@ -37,7 +37,7 @@ EXPORTS = (
     "b2g_sgemm", "b2g_sgemm_ex", "b2g_sgemm_with_plan", "b2g_sgemm_select_plan",
     "b2g_sgemm_ws", "b2g_sgemm_workspace_size", "b2g_sgemm_launch_count",
     "b2g_release_workspaces", "b2g_sgemm_noalloc",
-    "b2g_sgemm_3xtf32", "b2g_sgemm_strided_batched",
+    "b2g_sgemm_3xtf32", "b2g_sgemm_3xtf32_variant", "b2g_sgemm_strided_batched",
     "b2g_plan_count", "b2g_plan_name", "b2g_plan_info", "b2g_status", "b2g_set_wait_limit_ns",
     "b2g_debug_stop_after", "b2g_strerror", "b2g_version",
 )
@@ -77,6 +77,7 @@ def _load():
         lib.b2g_release_workspaces.argtypes = []
         lib.b2g_sgemm_noalloc.argtypes = gemm
         lib.b2g_sgemm_3xtf32.argtypes = gemm
+        lib.b2g_sgemm_3xtf32_variant.argtypes = [i] + gemm
         ll = ctypes.c_longlong
         lib.b2g_sgemm_strided_batched.argtypes = [i, i, i, i, i, f, vp, i, ll, vp, i, ll, f, vp,
                                                   i, ll, i, vp]
@@ -160,16 +161,25 @@ def b2g_sgemm_3xtf32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> 
     return _load().b2g_sgemm_3xtf32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
 
 
-def sgemm_3xtf32(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):
+def b2g_sgemm_3xtf32_variant(variant, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                             stream=0) -> int:
+    return _load().b2g_sgemm_3xtf32_variant(variant, M, N, K, alpha, A, lda, B, ldb, beta, C,
+                                            ldc, stream)
+
+
+def sgemm_3xtf32(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None,
+                 variant: Optional[int] = None):
     """C <- alpha * A @ B + beta * C on the tensor cores (3xTF32 split); see
-    b2g_sgemm_3xtf32 in include/b2g_sgemm.h."""
+    b2g_sgemm_3xtf32 in include/b2g_sgemm.h.  variant: None for the default
+    kernel, 0 (one CTA per tile) or 1 (a CTA pair per tile)."""
     lda, ldb, ldc = _check(A, "A"), _check(B, "B"), _check(C, "C")
     M, K = A.shape
     Kb, N = B.shape
     if Kb != K or tuple(C.shape) != (M, N):
         raise ValueError("shape mismatch")
-    rc = b2g_sgemm_3xtf32(M, N, K, float(alpha), A.data_ptr(), lda, B.data_ptr(), ldb,
-                          float(beta), C.data_ptr(), ldc, _stream_handle(stream))
+    args = (M, N, K, float(alpha), A.data_ptr(), lda, B.data_ptr(), ldb, float(beta),
+            C.data_ptr(), ldc, _stream_handle(stream))
+    rc = b2g_sgemm_3xtf32(*args) if variant is None else b2g_sgemm_3xtf32_variant(variant, *args)
     if rc:
         raise B2GError(rc)
     return C

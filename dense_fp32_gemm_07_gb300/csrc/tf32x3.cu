@@ -311,6 +311,235 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 }
 
+// ------------------------------------------------- the CTA-pair tensor-core GEMM
+//
+// Two CTAs of a cluster share each 256 x 128 output tile: CTA r stages rows
+// 128r .. 128r+127 of A (hi and lo) and rows 64r .. 64r+63 of B^T (columns of
+// B), and holds rows 128r .. 128r+127 of the accumulator in its own tensor
+// memory.  One lane of the even CTA issues tcgen05.mma.cta_group::2 (M 256,
+// N 128), which reads both CTAs' shared memory.  Per SM this stages 48 KB per
+// 32-k step instead of 64 KB (4 stages fit where 3 did) and reads B once for
+// two SMs.
+//
+// Signalling: both CTAs' copies of a stage complete on the even CTA's `full`
+// barrier (the pair form of the bulk-tensor copy); the MMA issuer commits
+// "stage read" and "accumulator final" to its own barriers and to the odd
+// CTA's (a second commit aimed at the peer's address); the odd CTA's epilogue
+// warps arrive remotely on the even CTA's "accumulator drained" barrier.
+// Every wait is bounded; every thread of both CTAs reaches the final cluster
+// barrier before tensor memory is freed.
+
+constexpr int kTpThreads = 192;  // warp 0 copies, 1 MMA, 2-5 epilogue
+constexpr int kTpStages = 4;
+constexpr uint32_t kTpATile = 128 * kTcBK * 4;  // this CTA's 128 rows of A_hi or A_lo: 16 KB
+constexpr uint32_t kTpBTile = 64 * kTcBK * 4;   // this CTA's 64 rows of B_hi^T or B_lo^T: 8 KB
+constexpr uint32_t kTpStageBytes = 2 * kTpATile + 2 * kTpBTile;  // 48 KB
+constexpr uint32_t kTpTmemCols = 2 * kTcBN;                      // two 128-column accumulators
+constexpr int kTpNumBars = 2 * kTpStages + 5;
+// 8 KB of slack after the barriers: an operand read one B tile longer than
+// intended would still stay inside this CTA's shared memory.
+constexpr int kTpSmemBytes = kTpStages * kTpStageBytes + 1024 + kTpNumBars * 8 + 16 + 8192;
+
+__global__ void __launch_bounds__(kTpThreads, 1)
+    sgemm_tf32x3_pair_kernel(const __grid_constant__ Tf32x3Params p,
+                             const __grid_constant__ CUtensorMap mAhi,
+                             const __grid_constant__ CUtensorMap mAlo,
+                             const __grid_constant__ CUtensorMap mBhi,
+                             const __grid_constant__ CUtensorMap mBlo) {
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle atoms: 1024-byte aligned
+  unsigned char* gbase = smem_raw + (base - raw);
+  const uint32_t bars = base + kTpStages * kTpStageBytes;
+  auto full = [&](int s) { return bars + 8u * s; };  // even CTA: both CTAs' copies landed
+  auto empty = [&](int s) { return bars + 8u * (kTpStages + s); };  // stage read by the MMAs
+  auto tfull = [&](int a) { return bars + 8u * (2 * kTpStages + a); };
+  auto tempty = [&](int a) { return bars + 8u * (2 * kTpStages + 2 + a); };
+  const uint32_t drain = bars + 8u * (2 * kTpStages + 4);
+  uint32_t* tmem_slot =
+      reinterpret_cast<uint32_t*>(gbase + kTpStages * kTpStageBytes + kTpNumBars * 8);
+
+  const uint32_t rank = cluster_ctarank() & 1u;
+  const bool even = rank == 0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kTpStages; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull(a), 1);
+      mbar_init(tempty(a), 8);  // four epilogue warps in each CTA
+    }
+    mbar_init(drain, 1);
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_addr(tmem_slot), kTpTmemCols);
+    tmem_relinquish_pair();
+  }
+  __syncwarp();
+  tc_fence_before_sync();
+  cluster_sync();  // barriers initialised and tensor memory allocated in both CTAs
+  tc_fence_after_sync();
+  // The even CTA's base address names the pair's accumulator columns in both.
+  const uint32_t tmem =
+      even ? *tmem_slot : ld_shared_cluster_u32(mapa_shared(smem_addr(tmem_slot), 0));
+  const int total_tiles = p.tiles_m * p.tiles_n;
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- copy issuer
+    if (lane == 0) {
+      prefetch_tmap(&mAhi);
+      prefetch_tmap(&mAlo);
+      prefetch_tmap(&mBhi);
+      prefetch_tmap(&mBlo);
+      int s = 0, issued = 0;
+      uint32_t ph = 0;
+      for (int tile = pair; tile < total_tiles; tile += npairs) {
+        int tm, tn;
+        tc_tile_coords(p, tile, tm, tn);
+        const int ma = tm * 2 * kTcBM + (int)rank * kTcBM;    // this CTA's rows of A
+        const int nb = tn * kTcBN + (int)rank * (kTcBN / 2);  // this CTA's rows of B^T
+        for (int kt = 0; kt < p.k_tiles; ++kt) {
+          if (p.debug_stop_ktile >= 0 && issued >= p.debug_stop_ktile) goto copies_done;
+          if (!mbar_wait(empty(s), ph ^ 1u, p.wait_limit_ns, p.status, kStatusTimeoutEmpty))
+            goto copies_done;
+          const uint32_t st = base + s * kTpStageBytes;
+          // both CTAs' bytes complete on the even CTA's barrier
+          if (even) mbar_arrive_expect_tx(full(s), 2 * kTpStageBytes);
+          const uint32_t fb = even ? full(s) : mapa_shared(full(s), 0);
+          tma_load_2d_pair(st, &mAhi, kt * kTcBK, ma, fb);
+          tma_load_2d_pair(st + kTpATile, &mAlo, kt * kTcBK, ma, fb);
+          tma_load_2d_pair(st + 2 * kTpATile, &mBhi, kt * kTcBK, nb, fb);
+          tma_load_2d_pair(st + 2 * kTpATile + kTpBTile, &mBlo, kt * kTcBK, nb, fb);
+          ++issued;
+          if (++s == kTpStages) s = 0, ph ^= 1u;
+        }
+      }
+    copies_done:
+      // Leave only after the copies started here have landed: the even CTA
+      // sees its `full` barriers complete (they count both CTAs' bytes), the
+      // odd CTA sees the MMAs release the stages (they read what landed).
+      for (int d = 0, pending = min(issued, kTpStages); d < pending; ++d) {
+        if (--s < 0) s = kTpStages - 1, ph ^= 1u;
+        if (!mbar_wait(even ? full(s) : empty(s), ph, p.wait_limit_ns, p.status,
+                       kStatusTimeoutDrain))
+          break;
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer (even CTA)
+    if (even && lane == 0) {
+      constexpr uint32_t idesc = idesc_tf32(2 * kTcBM, kTcBN);
+      int s = 0, a = 0;
+      uint32_t ph = 0, aph = 0;
+      for (int tile = pair; tile < total_tiles; tile += npairs) {
+        if (!mbar_wait(tempty(a), aph ^ 1u, p.wait_limit_ns, p.status, kStatusTimeoutTmem))
+          goto mma_done;
+        tc_fence_after_sync();
+        const uint32_t d = tmem + (uint32_t)(a * kTcBN);
+        for (int kt = 0; kt < p.k_tiles; ++kt) {
+          if (!mbar_wait(full(s), ph, p.wait_limit_ns, p.status, kStatusTimeoutFull)) goto mma_done;
+          tc_fence_after_sync();
+          const uint32_t st = base + s * kTpStageBytes;
+#pragma unroll
+          for (int kk = 0; kk < kTcBK / 8; ++kk) {  // 8 TF32 = 32 bytes per K step
+            const uint32_t off = kk * 32u;
+            const uint64_t ahi = smem_desc_sw128_kmajor(st + off);
+            const uint64_t alo = smem_desc_sw128_kmajor(st + kTpATile + off);
+            const uint64_t bhi = smem_desc_sw128_kmajor(st + 2 * kTpATile + off);
+            const uint64_t blo = smem_desc_sw128_kmajor(st + 2 * kTpATile + kTpBTile + off);
+            mma_tf32_pair(d, alo, bhi, idesc, (kt > 0 || kk > 0) ? 1u : 0u);
+            mma_tf32_pair(d, ahi, blo, idesc, 1u);
+            mma_tf32_pair(d, ahi, bhi, idesc, 1u);
+          }
+          mma_commit_pair(empty(s));                  // this CTA may refill the stage
+          mma_commit_pair(mapa_shared(empty(s), 1));  // and so may the odd one
+          if (++s == kTpStages) s = 0, ph ^= 1u;
+        }
+        mma_commit_pair(tfull(a));  // the accumulator is final in both CTAs
+        mma_commit_pair(mapa_shared(tfull(a), 1));
+        if (++a == 2) a = 0, aph ^= 1u;
+      }
+    mma_done:
+      mma_commit_pair(drain);
+      mbar_wait(drain, 0, p.wait_limit_ns, p.status, kStatusTimeoutTmem);
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int q = warp & 3;  // tensor-memory lanes 32q .. 32q+31 belong to this warp
+    int a = 0;
+    uint32_t aph = 0;
+    const float alpha = p.alpha, beta = p.beta;
+    for (int tile = pair; tile < total_tiles; tile += npairs) {
+      int tm, tn;
+      tc_tile_coords(p, tile, tm, tn);
+      if (!mbar_wait(tfull(a), aph, p.wait_limit_ns, p.status, kStatusTimeoutTmem)) break;
+      tc_fence_after_sync();
+      const int r = tm * 2 * kTcBM + (int)rank * kTcBM + 32 * q + lane;
+      float* crow = p.C + (long long)r * p.ldc;
+#pragma unroll 1
+      for (int c = 0; c < kTcBN / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(a * kTcBN + 32 * c), v);
+        tmem_ld_wait();
+        if (r < p.M) {
+          const int n = tn * kTcBN + 32 * c;
+          if (p.c_vec4 && n + 31 < p.N) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+              float4 o;
+              const float a0 = __uint_as_float(v[j]), a1 = __uint_as_float(v[j + 1]);
+              const float a2 = __uint_as_float(v[j + 2]), a3 = __uint_as_float(v[j + 3]);
+              if (beta != 0.f) {
+                const float4 cv = *reinterpret_cast<const float4*>(crow + n + j);
+                o = make_float4(fmaf(alpha, a0, beta * cv.x), fmaf(alpha, a1, beta * cv.y),
+                                fmaf(alpha, a2, beta * cv.z), fmaf(alpha, a3, beta * cv.w));
+              } else {
+                o = make_float4(alpha * a0, alpha * a1, alpha * a2, alpha * a3);
+              }
+              *reinterpret_cast<float4*>(crow + n + j) = o;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if (n + j < p.N) {
+                float* qp = crow + n + j;
+                const float acc = __uint_as_float(v[j]);
+                *qp = (beta != 0.f) ? fmaf(alpha, acc, beta * *qp) : alpha * acc;
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) {
+        if (even)
+          mbar_arrive(tempty(a));
+        else
+          mbar_arrive_remote(mapa_shared(tempty(a), 0));
+      }
+      if (++a == 2) a = 0, aph ^= 1u;
+    }
+  }
+
+  // teardown: no copy, MMA, remote arrival or tensor-memory read of either
+  // CTA is still outstanding once both have passed this barrier
+  __syncwarp();
+  tc_fence_before_sync();
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc_pair(*tmem_slot, kTpTmemCols);
+  }
+}
+
 // ------------------------------------------------------------------- launchers
 
 cudaError_t launch_split_a(const float* A, int M, int K, long long lda, float* Ahi, float* Alo,
@@ -353,6 +582,46 @@ cudaError_t launch_tf32x3(const Tf32x3Params& p, const CUtensorMap* maps, int nu
   void* args[] = {&pc, &m0, &m1, &m2, &m3};
   return cudaLaunchKernel(reinterpret_cast<const void*>(&sgemm_tf32x3_kernel), dim3(grid),
                           dim3(kTcThreads), args, kTcSmemBytes, stream);
+}
+
+cudaError_t launch_tf32x3_pair(const Tf32x3Params& p, const CUtensorMap* maps, int num_sms,
+                               cudaStream_t stream) {
+  // Per device, once: opt in to the shared memory and ask how many CTA pairs
+  // can be resident at once (the persistent grid is that many pairs).
+  static std::atomic<int> resident_pairs[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kTpThreads);
+  cfg.dynamicSmemBytes = kTpSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const void* kern = reinterpret_cast<const void*>(&sgemm_tf32x3_pair_kernel);
+  int pairs = resident_pairs[dev].load(std::memory_order_acquire);
+  if (pairs == 0) {
+    e = cudaFuncSetAttribute(sgemm_tf32x3_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kTpSmemBytes);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3((unsigned)(num_sms & ~1));
+    e = cudaOccupancyMaxActiveClusters(&pairs, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    if (pairs < 1) return cudaErrorInvalidConfiguration;
+    resident_pairs[dev].store(pairs, std::memory_order_release);
+  }
+  const long long tiles = (long long)p.tiles_m * p.tiles_n;
+  cfg.gridDim = dim3((unsigned)(2 * (tiles < pairs ? tiles : pairs)));
+  Tf32x3Params pc = p;
+  CUtensorMap m0 = maps[0], m1 = maps[1], m2 = maps[2], m3 = maps[3];
+  void* args[] = {&pc, &m0, &m1, &m2, &m3};
+  return cudaLaunchKernelExC(&cfg, kern, args);
 }
 
 }  // namespace b2g

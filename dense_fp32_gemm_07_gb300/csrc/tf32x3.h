@@ -28,8 +28,15 @@ cudaError_t launch_split_bt(const float* B, int K, int N, long long ldb, float* 
                             cudaStream_t stream);
 
 // The GEMM on the split operands.  maps: Ahi, Alo, Bhi^T, Blo^T as 2-D tensors
-// {K, rows} with 128-byte swizzle and boxes {32, 128}.
+// {K, rows} with 128-byte swizzle and boxes {32, 128}.  tiles_m counts
+// 128-row tiles.
 cudaError_t launch_tf32x3(const Tf32x3Params& p, const CUtensorMap* maps, int num_sms,
                           cudaStream_t stream);
+
+// The same GEMM with a CTA pair per 256 x 128 output tile (a cluster of two
+// CTAs, one tcgen05.mma.cta_group::2 per step).  maps: boxes {32, 128} for
+// A_hi and A_lo, {32, 64} for B_hi^T and B_lo^T.  tiles_m counts 256-row tiles.
+cudaError_t launch_tf32x3_pair(const Tf32x3Params& p, const CUtensorMap* maps, int num_sms,
+                               cudaStream_t stream);
 
 }  // namespace b2g

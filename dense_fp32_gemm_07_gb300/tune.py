@@ -1,6 +1,7 @@
 """Per-plan timing sweep behind the shape-keyed tune table (csrc/tune_table.h).
 
     python -m dense_fp32_gemm_07_gb300.tune [--once] [--plans REGEX] MxNxK[xALPHAxBETA] ...
+    python -m dense_fp32_gemm_07_gb300.tune --tf32x3 [--once] MxNxK[xALPHAxBETA] ...
 
 Times every compiled plan that accepts the operands on each shape (CUDA events
 on the launching stream, after warm-up, operands uniform[-1, 1) made by
@@ -9,6 +10,8 @@ that read A stored K x M (tmaT_*) get a transposed copy of A.  With --once
 every plan runs exactly one launch per shape and nothing is timed: that is the
 form to run under ncu to compare plans' counters.  --plans keeps only the
 plans whose name matches REGEX (re.search); the table's plan is always kept.
+--tf32x3 times the 3xTF32 tensor-core path instead, each kernel variant
+(0: one CTA per tile, 1: a CTA pair per tile), split kernels included.
 """
 from __future__ import annotations
 
@@ -74,13 +77,53 @@ def sweep(shapes, once=False, out=sys.stdout, pattern=None):
                   file=out, flush=True)
 
 
+def sweep_tf32x3(shapes, once=False, out=sys.stdout):
+    import torch
+
+    from dense_fp32_gemm_07_gb300 import build
+
+    build.build()
+    for M, N, K, alpha, beta in shapes:
+        A = torch.rand(M, K, device="cuda") * 2 - 1
+        B = torch.rand(K, N, device="cuda") * 2 - 1
+        C = torch.rand(M, N, device="cuda") * 2 - 1
+        flops = 2.0 * M * N * K
+        iters = max(3, min(50, int(2e12 / flops)))
+        for variant in (0, 1):
+            def call():
+                b2g.sgemm_3xtf32(A, B, C, alpha, beta, variant=variant)
+
+            call()
+            torch.cuda.synchronize()
+            if once:
+                print(f"{M}x{N}x{K} tf32x3 variant {variant}", file=out, flush=True)
+                continue
+            for _ in range(2):
+                call()
+            ev0 = torch.cuda.Event(enable_timing=True)
+            ev1 = torch.cuda.Event(enable_timing=True)
+            ev0.record()
+            for _ in range(iters):
+                call()
+            ev1.record()
+            torch.cuda.synchronize()
+            ms = ev0.elapsed_time(ev1) / iters
+            print(f"{M}x{N}x{K} tf32x3 variant {variant}  {ms:9.4f} ms {flops / ms / 1e9:8.2f} "
+                  f"TFLOP/s ({3 * flops / ms / 1e9:7.1f} TF32 TFLOP/s)", file=out, flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("shapes", nargs="*", default=["4096x4096x4096x1x0.5"])
     ap.add_argument("--once", action="store_true")
     ap.add_argument("--plans", default=None, help="regex: time only the matching plans")
+    ap.add_argument("--tf32x3", action="store_true", help="time the 3xTF32 kernel variants")
     args = ap.parse_args()
-    sweep([parse_shape(s) for s in args.shapes], once=args.once, pattern=args.plans)
+    shapes = [parse_shape(s) for s in args.shapes]
+    if args.tf32x3:
+        sweep_tf32x3(shapes, once=args.once)
+    else:
+        sweep(shapes, once=args.once, pattern=args.plans)
 
 
 if __name__ == "__main__":

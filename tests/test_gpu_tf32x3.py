@@ -1,5 +1,7 @@
 """The 3xTF32 tensor-core path (b2g_sgemm_3xtf32) against the oracle, within
-the same elementwise FP32 bound as the FFMA path."""
+the same elementwise FP32 bound as the FFMA path, for both tensor-core kernels:
+variant 0 (one CTA per 128 x 128 tile) and variant 1 (a CTA pair per 256 x 128
+tile, tcgen05.mma.cta_group::2)."""
 import ctypes
 
 import numpy as np
@@ -17,21 +19,28 @@ def tb():
     return env()
 
 
-def run3(torch, b2g, A, B, C, alpha, beta):
+VARIANTS = [0, 1]
+
+
+def run3(torch, b2g, A, B, C, alpha, beta, variant=None):
     M, K = A.shape
     N = B.shape[1]
     dA, dB, dC = (torch.from_numpy(np.ascontiguousarray(x)).cuda() for x in (A, B, C))
     s = torch.cuda.current_stream().cuda_stream
-    rc = b2g.b2g_sgemm_3xtf32(M, N, K, alpha, dA.data_ptr(), K, dB.data_ptr(), N, beta,
-                              dC.data_ptr(), N, s)
+    args = (M, N, K, alpha, dA.data_ptr(), K, dB.data_ptr(), N, beta, dC.data_ptr(), N, s)
+    if variant is None:
+        rc = b2g.b2g_sgemm_3xtf32(*args)
+    else:
+        rc = b2g.b2g_sgemm_3xtf32_variant(variant, *args)
     torch.cuda.synchronize()
     return rc, (dC.cpu().numpy() if rc == 0 else None)
 
 
 @pytest.mark.parametrize("shape", [(128, 128, 32), (128, 128, 64), (256, 128, 32), (128, 256, 96),
                                    (1, 1, 4), (5, 7, 8), (37, 45, 52), (130, 257, 68),
-                                   (300, 200, 1024)])
-def test_shapes_within_bound(tb, shape):
+                                   (300, 200, 1024), (257, 129, 96), (513, 384, 64)])
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_shapes_within_bound(tb, shape, variant):
     torch, b2g = tb
     M, N, K = shape
     rng = np.random.default_rng(M + 3 * N + 7 * K)
@@ -39,12 +48,13 @@ def test_shapes_within_bound(tb, shape):
     B = rng.uniform(-1, 1, size=(K, N)).astype(np.float32)
     C = rng.uniform(-1, 1, size=(M, N)).astype(np.float32)
     ref, bound, _ = oracle.sgemm(A, B, C, 0.75, -1.25)
-    rc, got = run3(torch, b2g, A, B, C, 0.75, -1.25)
+    rc, got = run3(torch, b2g, A, B, C, 0.75, -1.25, variant)
     assert rc == 0, b2g.b2g_strerror(rc)
-    check(got, ref, bound, f"3xtf32 {shape}")
+    check(got, ref, bound, f"3xtf32 {shape} variant {variant}")
 
 
-def test_small_integers_bit_exact(tb):
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_small_integers_bit_exact(tb, variant):
     """Integers up to 2^10 are TF32 values (lo = 0) and every partial sum stays
     below 2^24, so the tensor-core result must be exact."""
     torch, b2g = tb
@@ -54,29 +64,31 @@ def test_small_integers_bit_exact(tb):
     B = rng.integers(-3, 4, size=(K, N)).astype(np.float32)
     C = rng.integers(-3, 4, size=(M, N)).astype(np.float32)
     ref, _, _ = oracle.sgemm(A, B, C, 2.0, -1.0)
-    rc, got = run3(torch, b2g, A, B, C, 2.0, -1.0)
+    rc, got = run3(torch, b2g, A, B, C, 2.0, -1.0, variant)
     assert rc == 0
     assert np.array_equal(got.astype(np.float64), ref)
 
 
 @pytest.mark.parametrize("name", ["square512", "sweep128", "sweep1024", "skinny16x4096x4096"])
-def test_workloads_full(tb, name):
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_workloads_full(tb, name, variant):
     torch, b2g = tb
     w = workloads.WORKLOADS[name]
     A, B, C = w.make()
     ref, bound, _ = oracle.sgemm(A, B, C, w.alpha, w.beta)
-    rc, got = run3(torch, b2g, A, B, C, w.alpha, w.beta)
+    rc, got = run3(torch, b2g, A, B, C, w.alpha, w.beta, variant)
     assert rc == 0
     check(got, ref, bound, name)
 
 
 @pytest.mark.parametrize("name", ["square4096", "mlp8192x11008x4096"])
-def test_workloads_sampled(tb, name):
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_workloads_sampled(tb, name, variant):
     torch, b2g = tb
     w = workloads.WORKLOADS[name]
     A, B, C = w.make()
     dA, dB, dC = (torch.from_numpy(x).cuda() for x in (A, B, C))
-    b2g.sgemm_3xtf32(dA, dB, dC, w.alpha, w.beta)
+    b2g.sgemm_3xtf32(dA, dB, dC, w.alpha, w.beta, variant=variant)
     torch.cuda.synchronize()
     rows, cols = sample_entries(w.M, w.N, seed=w.seed)
     got = dC[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()].cpu().numpy()
@@ -94,7 +106,8 @@ def test_unsupported_operands(tb):
     assert rc == b2g.B2G_ERR_UNSUPPORTED
 
 
-def test_nonfinite_and_beta_zero(tb):
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_nonfinite_and_beta_zero(tb, variant):
     torch, b2g = tb
     rng = np.random.default_rng(9)
     A = rng.uniform(-1, 1, size=(130, 64)).astype(np.float32)
@@ -102,13 +115,14 @@ def test_nonfinite_and_beta_zero(tb):
     A[100, 0] = np.nan
     C = np.full((130, 140), np.nan, np.float32)  # beta == 0: C must not be read
     ref, bound, _ = oracle.sgemm(A, B, C, 1.0, 0.0)
-    rc, got = run3(torch, b2g, A, B, C, 1.0, 0.0)
+    rc, got = run3(torch, b2g, A, B, C, 1.0, 0.0, variant)
     assert rc == 0
     check(got, ref, bound, "nonfinite")
     assert np.isnan(got[100]).all() and np.isfinite(np.delete(got, 100, axis=0)).all()
 
 
-def test_wait_runs_out_and_context_survives(tb):
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_wait_runs_out_and_context_survives(tb, variant):
     torch, b2g = tb
     rng = np.random.default_rng(0)
     A = rng.uniform(-1, 1, size=(128, 128)).astype(np.float32)
@@ -119,7 +133,7 @@ def test_wait_runs_out_and_context_survives(tb):
     try:
         b2g.b2g_set_wait_limit_ns(20_000_000)
         b2g.b2g_debug_stop_after(1)  # 128 / 32 = 4 stages needed, 1 issued
-        rc, _ = run3(torch, b2g, A, B, C, 1.0, 0.0)
+        rc, _ = run3(torch, b2g, A, B, C, 1.0, 0.0, variant)
         assert rc == 0
         rc, flags = b2g.b2g_status(s, clear=True)
         assert rc == b2g.B2G_ERR_TIMEOUT and flags, f"{flags:#x}"
@@ -127,6 +141,14 @@ def test_wait_runs_out_and_context_survives(tb):
         b2g.b2g_debug_stop_after(-1)
         b2g.b2g_set_wait_limit_ns(2_000_000_000)
     ref, bound, _ = oracle.sgemm(A, B, C, 1.0, 0.0)
-    rc, got = run3(torch, b2g, A, B, C, 1.0, 0.0)
+    rc, got = run3(torch, b2g, A, B, C, 1.0, 0.0, variant)
     assert rc == 0
     check(got, ref, bound, "after timeout")
+
+
+def test_unknown_variant(tb):
+    torch, b2g = tb
+    C = torch.zeros(4, 4, device="cuda")
+    rc = b2g.b2g_sgemm_3xtf32_variant(2, 4, 4, 4, 1.0, C.data_ptr(), 4, C.data_ptr(), 4, 0.0,
+                                      C.data_ptr(), 4, 0)
+    assert rc == b2g.B2G_ERR_INVALID_PLAN
