@@ -28,6 +28,7 @@
 #include <cstring>
 
 #include "ptx.cuh"
+#include "tcgen05.cuh"
 #include "sgemm_params.h"
 #include "tf32x3.h"
 
