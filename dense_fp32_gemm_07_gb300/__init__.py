@@ -35,7 +35,7 @@ B2G_ERR_SCRATCH_LIMIT = -11
 # every symbol include/b2g_sgemm.h declares
 EXPORTS = (
     "b2g_sgemm", "b2g_sgemm_ex", "b2g_sgemm_with_plan", "b2g_sgemm_select_plan",
-    "b2g_sgemm_ws", "b2g_sgemm_workspace_size", "b2g_sgemm_launch_count",
+    "b2g_sgemm_ws", "b2g_sgemm_workspace_size", "b2g_sgemm_launch_count", "b2g_sgemm_host",
     "b2g_release_workspaces", "b2g_sgemm_noalloc",
     "b2g_sgemm_3xtf32", "b2g_sgemm_3xtf32_variant", "b2g_sgemm_strided_batched",
     "b2g_plan_count", "b2g_plan_name", "b2g_plan_info", "b2g_status", "b2g_set_wait_limit_ns",
@@ -76,6 +76,7 @@ def _load():
                                                ctypes.POINTER(ctypes.c_int)]
         lib.b2g_release_workspaces.argtypes = []
         lib.b2g_sgemm_noalloc.argtypes = gemm
+        lib.b2g_sgemm_host.argtypes = gemm
         lib.b2g_sgemm_3xtf32.argtypes = gemm
         lib.b2g_sgemm_3xtf32_variant.argtypes = [i] + gemm
         ll = ctypes.c_longlong
@@ -159,6 +160,49 @@ def b2g_sgemm_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) ->
 
 def b2g_sgemm_3xtf32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> int:
     return _load().b2g_sgemm_3xtf32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
+
+
+def b2g_sgemm_host(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> int:
+    return _load().b2g_sgemm_host(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
+
+
+def _host_ld(x, name):
+    """Leading dimension (elements) of a row-major host float32 array or tensor."""
+    import numpy as np
+
+    if isinstance(x, np.ndarray):
+        if x.dtype != np.float32 or x.ndim != 2 or (x.shape[1] > 1 and x.strides[1] != 4):
+            raise ValueError(f"{name}: 2-D float32 array with unit column stride expected")
+        return max(x.strides[0] // 4, 1), x.ctypes.data
+    if x.device.type != "cpu" or x.dtype.is_floating_point is False or x.element_size() != 4:
+        raise ValueError(f"{name}: CPU float32 tensor expected")
+    if x.dim() != 2 or (x.shape[1] > 1 and x.stride(1) != 1):
+        raise ValueError(f"{name}: 2-D tensor with unit column stride expected")
+    return max(x.stride(0), 1), x.data_ptr()
+
+
+def sgemm_host(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None, sync: bool = True):
+    """C <- alpha * A @ B + beta * C for HOST float32 arrays or CPU tensors
+    (page-locked ones copy fastest); see b2g_sgemm_host in include/b2g_sgemm.h.
+    With sync (default) the call waits for the stream, so C holds the result
+    on return."""
+    lda, pa = _host_ld(A, "A")
+    ldb, pb = _host_ld(B, "B")
+    ldc, pc = _host_ld(C, "C")
+    M, K = A.shape
+    Kb, N = B.shape
+    if Kb != K or tuple(C.shape) != (M, N):
+        raise ValueError("shape mismatch")
+    h = _stream_handle(stream)
+    rc = b2g_sgemm_host(M, N, K, float(alpha), pa, lda, pb, ldb, float(beta), pc, ldc, h)
+    if rc:
+        raise B2GError(rc)
+    if sync:
+        import torch
+
+        s = torch.cuda.current_stream() if stream is None else stream
+        s.synchronize() if hasattr(s, "synchronize") else torch.cuda.synchronize()
+    return C
 
 
 def b2g_sgemm_3xtf32_variant(variant, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,

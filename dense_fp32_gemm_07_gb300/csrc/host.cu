@@ -186,6 +186,8 @@ int plan_index(const char* name) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+constexpr int kHostPanelsMax = 16;  // row panels of b2g_sgemm_host
+
 struct Call {
   int transA, transB, M, N, K;
   float alpha, beta;
@@ -537,6 +539,134 @@ int run(const Call& c, int forced_plan, void* stream, void* user_ws = nullptr,
   return e == cudaSuccess ? 0 : B2G_ERR_LAUNCH;
 }
 
+// ------------------------------------------------------------ host operands
+//
+// b2g_sgemm_host: A, B and C live in host memory.  B goes to the device first;
+// A and C then follow in row panels on a copy stream while the caller's stream
+// multiplies the panels that have arrived, and each finished panel of C goes
+// back on a second copy stream.  Only B's copy and the last panel's return are
+// not hidden behind the GEMM.  Device copies are packed with rows padded to a
+// multiple of 4 floats (the bulk-tensor plans' alignment).
+struct HostPath {
+  std::mutex mu;
+  bool init = false;
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t start = nullptr, done = nullptr, b_in = nullptr, c_out = nullptr;
+  cudaEvent_t a_in[kHostPanelsMax] = {}, gemm[kHostPanelsMax] = {};
+  void* buf = nullptr;
+  size_t bytes = 0;
+  bool used = false;
+};
+HostPath g_hostpath[kMaxDevices];
+
+int hostpath_init(HostPath& h) {
+  if (h.init) return 0;
+  if (cudaStreamCreateWithFlags(&h.h2d, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&h.d2h, cudaStreamNonBlocking) != cudaSuccess)
+    return B2G_ERR_CUDA;
+  cudaEvent_t* evs[] = {&h.start, &h.done, &h.b_in, &h.c_out};
+  for (cudaEvent_t* e : evs)
+    if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return B2G_ERR_CUDA;
+  for (int i = 0; i < kHostPanelsMax; ++i)
+    if (cudaEventCreateWithFlags(&h.a_in[i], cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h.gemm[i], cudaEventDisableTiming) != cudaSuccess)
+      return B2G_ERR_CUDA;
+  h.init = true;
+  return 0;
+}
+
+size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+
+int run_host(const Call& c, void* stream) {
+  int rc = validate(c);
+  if (rc) return rc;
+  if (c.M == 0 || c.N == 0) return 0;
+  DeviceState* d = nullptr;
+  rc = device_state(&d);
+  if (rc) return rc;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return B2G_ERR_DEVICE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
+    return B2G_ERR_UNSUPPORTED;  // allocations and host copies stay out of graphs
+
+  const bool gemm = needs_gemm(c);
+  const bool read_c = c.beta != 0.f;
+  const size_t M = (size_t)c.M, N = (size_t)c.N, K = (size_t)c.K;
+  const size_t kp = (K + 3) / 4 * 4, np = (N + 3) / 4 * 4;  // padded row lengths (floats)
+  const size_t a_bytes = gemm ? round256(M * kp * 4) : 0;
+  const size_t b_bytes = gemm ? round256(K * np * 4) : 0;
+  const size_t need = a_bytes + b_bytes + round256(M * np * 4);
+
+  HostPath& h = g_hostpath[dev];
+  std::lock_guard<std::mutex> lk(h.mu);
+  rc = hostpath_init(h);
+  if (rc) return rc;
+  // this call's copies start after the caller's earlier work and after the
+  // previous host-operand call (whatever its stream) has finished with the buffer
+  if (cudaEventRecord(h.start, st) != cudaSuccess) return B2G_ERR_CUDA;
+  if (cudaStreamWaitEvent(h.h2d, h.start, 0) != cudaSuccess) return B2G_ERR_CUDA;
+  if (h.used && cudaStreamWaitEvent(h.h2d, h.done, 0) != cudaSuccess) return B2G_ERR_CUDA;
+  if (h.bytes < need) {
+    if (h.buf) {
+      if (h.used && cudaStreamWaitEvent(st, h.done, 0) != cudaSuccess) return B2G_ERR_CUDA;
+      cudaFreeAsync(h.buf, st);
+      h.buf = nullptr, h.bytes = 0;
+    }
+    if (cudaMallocAsync(&h.buf, need, st) != cudaSuccess) return B2G_ERR_CUDA;
+    h.bytes = need;
+    if (cudaEventRecord(h.start, st) != cudaSuccess) return B2G_ERR_CUDA;
+    if (cudaStreamWaitEvent(h.h2d, h.start, 0) != cudaSuccess) return B2G_ERR_CUDA;
+  }
+  char* base = static_cast<char*>(h.buf);
+  float* dA = reinterpret_cast<float*>(base);
+  float* dB = reinterpret_cast<float*>(base + a_bytes);
+  float* dC = reinterpret_cast<float*>(base + a_bytes + b_bytes);
+
+  // panels of about 1024 rows (at least two waves of output tiles each)
+  int panels = c.M / 1024;
+  panels = panels < 1 ? 1 : panels > kHostPanelsMax ? kHostPanelsMax : panels;
+  const int rows = ((c.M + panels - 1) / panels + 127) / 128 * 128;
+  panels = (c.M + rows - 1) / rows;
+
+  auto fail = [&](cudaError_t e) { return e == cudaSuccess ? 0 : B2G_ERR_CUDA; };
+  if (gemm) {
+    rc = fail(cudaMemcpy2DAsync(dB, np * 4, c.B, (size_t)c.ldb * 4, N * 4, K,
+                                cudaMemcpyHostToDevice, h.h2d));
+    if (!rc) rc = fail(cudaEventRecord(h.b_in, h.h2d));
+    if (!rc) rc = fail(cudaStreamWaitEvent(st, h.b_in, 0));
+  }
+  for (int i = 0; i < panels && !rc; ++i) {
+    const size_t r0 = (size_t)i * rows;
+    const size_t rn = (size_t)(c.M - (int)r0 < rows ? c.M - (int)r0 : rows);
+    if (gemm)
+      rc = fail(cudaMemcpy2DAsync(dA + r0 * kp, kp * 4, c.A + r0 * c.lda, (size_t)c.lda * 4,
+                                  K * 4, rn, cudaMemcpyHostToDevice, h.h2d));
+    if (!rc && read_c)
+      rc = fail(cudaMemcpy2DAsync(dC + r0 * np, np * 4, c.C + r0 * c.ldc, (size_t)c.ldc * 4,
+                                  N * 4, rn, cudaMemcpyHostToDevice, h.h2d));
+    if (!rc) rc = fail(cudaEventRecord(h.a_in[i], h.h2d));
+    if (!rc) rc = fail(cudaStreamWaitEvent(st, h.a_in[i], 0));
+    if (!rc) {
+      Call pc{0, 0, (int)rn, c.N, c.K, c.alpha, c.beta, dA + r0 * kp, (int)(kp > 0 ? kp : 1), dB,
+              (int)np, dC + r0 * np, (int)np};
+      rc = run(pc, -1, st);
+    }
+    if (!rc) rc = fail(cudaEventRecord(h.gemm[i], st));
+    if (!rc) rc = fail(cudaStreamWaitEvent(h.d2h, h.gemm[i], 0));
+    if (!rc)
+      rc = fail(cudaMemcpy2DAsync(c.C + r0 * c.ldc, (size_t)c.ldc * 4, dC + r0 * np, np * 4,
+                                  N * 4, rn, cudaMemcpyDeviceToHost, h.d2h));
+  }
+  // join: the caller's stream holds the whole call; later calls wait for it
+  if (!rc) rc = fail(cudaEventRecord(h.c_out, h.d2h));
+  if (!rc) rc = fail(cudaStreamWaitEvent(st, h.c_out, 0));
+  if (!rc) rc = fail(cudaEventRecord(h.done, st));
+  if (!rc) h.used = true;
+  return rc;
+}
+
 // The 3xTF32 tensor-core path: split the operands into a workspace, then the
 // tcgen05 kernel.  Row-major, no op() flags; A 16-byte aligned with lda and K
 // multiples of 4 (B is read element by element by its split kernel).
@@ -712,6 +842,11 @@ int b2g_sgemm_launch_count(int transA, int transB, int M, int N, int K, float al
   return 0;
 }
 
+int b2g_sgemm_host(int M, int N, int K, float alpha, const float* A, int lda, const float* B,
+                   int ldb, float beta, float* C, int ldc, void* stream) {
+  return run_host(Call{0, 0, M, N, K, alpha, beta, A, lda, B, ldb, C, ldc}, stream);
+}
+
 int b2g_release_workspaces(void) {
   int rc = 0;
   for (int dev = 0; dev < kMaxDevices; ++dev) {
@@ -728,6 +863,22 @@ int b2g_release_workspaces(void) {
     if (cudaFree(w.ptr) != cudaSuccess) rc = B2G_ERR_CUDA;
     w.ptr = nullptr;
     w.bytes = 0;
+    cudaSetDevice(cur);
+  }
+  for (int dev = 0; dev < kMaxDevices; ++dev) {  // the host-operand staging buffers
+    HostPath& h = g_hostpath[dev];
+    std::lock_guard<std::mutex> lk(h.mu);
+    if (!h.buf) continue;
+    int cur = 0;
+    cudaGetDevice(&cur);
+    if (cudaSetDevice(dev) != cudaSuccess) {
+      rc = B2G_ERR_CUDA;
+      continue;
+    }
+    if (h.used) cudaEventSynchronize(h.done);
+    if (cudaFree(h.buf) != cudaSuccess) rc = B2G_ERR_CUDA;
+    h.buf = nullptr;
+    h.bytes = 0;
     cudaSetDevice(cur);
   }
   return rc;

@@ -117,6 +117,28 @@ int b2g_sgemm_ws(int transA, int transB, int M, int N, int K, float alpha, const
                  size_t workspace_bytes, void* stream);
 
 /*
+ * b2g_sgemm on HOST operands: A, B and C are host pointers (same row-major
+ * layout and leading-dimension rules as b2g_sgemm; page-locked memory from
+ * cudaHostAlloc / cudaHostRegister gives full copy speed, pageable memory
+ * works more slowly).  The library copies B to the device, then A and C in
+ * row panels of about 1024 rows on its own copy stream while `stream`
+ * multiplies the panels that have arrived, and copies each finished panel of
+ * C back on a second copy stream; every step is ordered after earlier work on
+ * `stream`, and the call's last copy is joined back into `stream`.  C holds
+ * the result once `stream` has completed the call's work (for instance after
+ * cudaStreamSynchronize(stream)); until then the host buffers must stay valid
+ * and unmodified.  Device staging (A, B and C with rows padded to a multiple
+ * of 4 floats) is a library-owned buffer per device, grown when needed and
+ * freed by b2g_release_workspaces; calls on different streams are ordered one
+ * after the other.  Same return codes as b2g_sgemm, plus B2G_ERR_UNSUPPORTED
+ * while `stream` is being captured into a graph and B2G_ERR_CUDA when a copy
+ * or the allocation fails.  Not on the pages: it serves callers whose data
+ * live in host memory.
+ */
+int b2g_sgemm_host(int M, int N, int K, float alpha, const float* A, int lda, const float* B,
+                   int ldb, float beta, float* C, int ldc, void* stream);
+
+/*
  * Workspace bytes the tune table's plan wants for these arguments (0 when it
  * needs none), stored in *bytes: A^T or the packed operands when the plan
  * writes them, then (256-byte aligned) the split tail's partial sums, at most
@@ -142,8 +164,8 @@ int b2g_sgemm_launch_count(int transA, int transB, int M, int N, int K, float al
                            int ldc, int* launches);
 
 /*
- * Free the library-owned workspaces of all devices, after waiting for the
- * work that used them.  Later calls allocate again when needed.  Returns 0 or
+ * Free the library-owned workspaces (and the staging buffers of
+ * b2g_sgemm_host) of all devices, after waiting for the work that used them.  Later calls allocate again when needed.  Returns 0 or
  * B2G_ERR_CUDA.
  */
 int b2g_release_workspaces(void);

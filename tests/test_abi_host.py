@@ -238,3 +238,13 @@ def test_tensor_api_rejects_cpu_tensors(b2g):
     a = torch.zeros(4, 4)
     with pytest.raises(TypeError):
         b2g.sgemm(a, a, a)
+
+
+def test_host_operand_argument_checks(b2g):
+    """b2g_sgemm_host checks its arguments before touching a device."""
+    args = lambda M, N, K, lda, ldb, ldc, C=FAKE: (M, N, K, 1.0, FAKE, lda, FAKE, ldb, 0.0, C,
+                                                   ldc, 0)
+    assert b2g.b2g_sgemm_host(*args(-1, 4, 4, 4, 4, 4)) == -1
+    assert b2g.b2g_sgemm_host(*args(4, 4, 4, 3, 4, 4)) == -2
+    assert b2g.b2g_sgemm_host(*args(4, 4, 4, 4, 4, 4, C=None)) == -3
+    assert b2g.b2g_sgemm_host(*args(0, 4, 4, 4, 4, 4)) == 0  # nothing to do, no device needed

@@ -1,0 +1,94 @@
+"""b2g_sgemm_host: operands in host memory (page-locked and pageable), copied
+to the device in row panels overlapped with the panel GEMMs, result copied
+back.  Every result is checked against the oracle's FP32 bound."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from gpu_helpers import check, env, sample_entries
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tb():
+    return env()
+
+
+def _inputs(seed, M, N, K, lda=None, ldc=None):
+    rng = np.random.default_rng(seed)
+    A = rng.uniform(-1, 1, size=(M, lda or K)).astype(np.float32)
+    B = rng.uniform(-1, 1, size=(K, N)).astype(np.float32)
+    C = rng.uniform(-1, 1, size=(M, ldc or N)).astype(np.float32)
+    return A, B, C
+
+
+@pytest.mark.parametrize("pinned", [True, False])
+@pytest.mark.parametrize("shape", [(200, 161, 92), (1000, 1025, 777), (2500, 300, 260),
+                                   (4100, 260, 300)])
+def test_host_operands(tb, shape, pinned):
+    torch, b2g = tb
+    M, N, K = shape
+    A, B, C = _inputs(M + N + K, M, N, K)
+    ref, bound, _ = oracle.sgemm(A, B, C, 0.75, -1.25)
+    if pinned:
+        hA, hB, hC = (torch.from_numpy(x).pin_memory() for x in (A, B, C))
+    else:
+        hA, hB, hC = A.copy(), B.copy(), C.copy()
+    b2g.sgemm_host(hA, hB, hC, 0.75, -1.25)
+    got = hC.numpy() if pinned else hC
+    check(got, ref, bound, f"host {shape} pinned={pinned}")
+
+
+def test_padded_leading_dims_untouched(tb):
+    """Logical windows of wider host arrays: padding columns are neither read
+    into the result nor written."""
+    torch, b2g = tb
+    M, N, K = 300, 170, 130
+    A, B, C = _inputs(4, M, N, K, lda=141, ldc=181)
+    C[:, N:] = 7.0
+    ref, bound, _ = oracle.sgemm(A[:, :K], B, C[:, :N], 1.5, 0.5)
+    hC = C.copy()
+    rc = b2g.b2g_sgemm_host(M, N, K, 1.5, A.ctypes.data, 141, B.ctypes.data, N, 0.5,
+                            hC.ctypes.data, 181, torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    check(hC[:, :N], ref, bound, "padded")
+    assert (hC[:, N:] == 7.0).all()
+
+
+def test_beta_zero_does_not_read_c_and_scale_only(tb):
+    torch, b2g = tb
+    M, N, K = 2100, 200, 64
+    A, B, _ = _inputs(5, M, N, K)
+    C = np.full((M, N), np.nan, np.float32)  # beta == 0: C is write-only
+    ref, bound, _ = oracle.sgemm(A, B, None, 1.0, 0.0)
+    b2g.sgemm_host(A, B, C, 1.0, 0.0)
+    check(C, ref, bound, "beta 0")
+    C2 = np.full((M, N), 2.0, np.float32)
+    b2g.sgemm_host(A, B, C2, 0.0, 3.0)  # alpha == 0: C = beta * C
+    assert (C2 == 6.0).all()
+
+
+def test_consecutive_calls_and_stream_order(tb):
+    """Two calls in a row with different data reuse the staging buffer."""
+    torch, b2g = tb
+    for seed in (10, 11):
+        A, B, C = _inputs(seed, 1500, 700, 900)
+        ref, bound, _ = oracle.sgemm(A, B, C, 1.0, 1.0)
+        hA, hB, hC = (torch.from_numpy(x).pin_memory() for x in (A, B, C))
+        b2g.sgemm_host(hA, hB, hC, 1.0, 1.0)
+        check(hC.numpy(), ref, bound, f"call {seed}")
+
+
+def test_square4096_sampled(tb):
+    torch, b2g = tb
+    w = workloads.WORKLOADS["square4096"]
+    A, B, C = w.make()
+    hA, hB, hC = (torch.from_numpy(x).pin_memory() for x in (A, B, C))
+    b2g.sgemm_host(hA, hB, hC, w.alpha, w.beta)
+    rows, cols = sample_entries(w.M, w.N, seed=w.seed)
+    got = hC.numpy()[rows, cols]
+    ref, bound, _ = oracle.sgemm_entries(A, B, C, w.alpha, w.beta, rows, cols)
+    check(got, ref, bound, "square4096 host")
