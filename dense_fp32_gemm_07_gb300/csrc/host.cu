@@ -40,6 +40,22 @@ __global__ void scale_c_kernel(int M, int N, float beta, float* __restrict__ C, 
   }
 }
 
+// Y += b * X over an M x N window (row-major, leading dimensions ldx, ldy, both
+// multiples of 4 with 16-byte aligned bases: float4 throughout).
+__global__ void axpby_rows_kernel(int M, int N4, float b, const float* __restrict__ X,
+                                  long long ldx, float* __restrict__ Y, long long ldy) {
+  const long long total = (long long)M * N4;
+  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const long long i = idx / N4, j = (idx - i * N4) * 4;
+    const float4 x = *reinterpret_cast<const float4*>(X + i * ldx + j);
+    float4* yp = reinterpret_cast<float4*>(Y + i * ldy + j);
+    float4 y = *yp;
+    y.x = fmaf(b, x.x, y.x), y.y = fmaf(b, x.y, y.y), y.z = fmaf(b, x.z, y.z), y.w = fmaf(b, x.w, y.w);
+    *yp = y;
+  }
+}
+
 namespace {
 
 struct DeviceState {
@@ -541,18 +557,28 @@ int run(const Call& c, int forced_plan, void* stream, void* user_ws = nullptr,
 
 // ------------------------------------------------------------ host operands
 //
-// b2g_sgemm_host: A, B and C live in host memory.  B goes to the device first;
-// A and C then follow in row panels on a copy stream while the caller's stream
-// multiplies the panels that have arrived, and each finished panel of C goes
-// back on a second copy stream.  Only B's copy and the last panel's return are
-// not hidden behind the GEMM.  Device copies are packed with rows padded to a
-// multiple of 4 floats (the bulk-tensor plans' alignment).
+// b2g_sgemm_host: A, B and C live in host memory; the host link (about 210 GB/s
+// in, 190 GB/s out on GB300) is much slower than the GEMM, so the copies are
+// overlapped with it:
+//  * K is cut into chunks (for K >= 2048: four chunks, 16-aligned); the copy
+//    stream sends B's rows and A's columns of chunk 0, then of chunk 1, ...,
+//    then C.  The caller's stream multiplies each chunk as soon as it has
+//    landed into a device accumulator D (beta 0 for the first chunk, 1 after).
+//  * The last chunk runs in row panels of about 1024 rows: each panel adds
+//    beta * C (D += beta * C) and goes back to the host on a second copy
+//    stream while the next panel multiplies.
+// So the GEMM starts after 1/4 of A and B have arrived, C's copy hides behind
+// the first chunks, and only the last panel's return is exposed.  With
+// K < 2048 there is one chunk and C goes in with A, panel by panel, straight
+// into D.  Chunked sums are rounded once per chunk, which the FP32 bound
+// covers.  Device copies are packed with rows padded to a multiple of 4 floats.
 struct HostPath {
   std::mutex mu;
   bool init = false;
   cudaStream_t h2d = nullptr, d2h = nullptr;
-  cudaEvent_t start = nullptr, done = nullptr, b_in = nullptr, c_out = nullptr;
-  cudaEvent_t a_in[kHostPanelsMax] = {}, gemm[kHostPanelsMax] = {};
+  cudaEvent_t start = nullptr, done = nullptr, c_in = nullptr, c_out = nullptr;
+  cudaEvent_t chunk[kHostPanelsMax] = {}, panel_in[kHostPanelsMax] = {},
+              gemm[kHostPanelsMax] = {};
   void* buf = nullptr;
   size_t bytes = 0;
   bool used = false;
@@ -564,11 +590,12 @@ int hostpath_init(HostPath& h) {
   if (cudaStreamCreateWithFlags(&h.h2d, cudaStreamNonBlocking) != cudaSuccess ||
       cudaStreamCreateWithFlags(&h.d2h, cudaStreamNonBlocking) != cudaSuccess)
     return B2G_ERR_CUDA;
-  cudaEvent_t* evs[] = {&h.start, &h.done, &h.b_in, &h.c_out};
+  cudaEvent_t* evs[] = {&h.start, &h.done, &h.c_in, &h.c_out};
   for (cudaEvent_t* e : evs)
     if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return B2G_ERR_CUDA;
   for (int i = 0; i < kHostPanelsMax; ++i)
-    if (cudaEventCreateWithFlags(&h.a_in[i], cudaEventDisableTiming) != cudaSuccess ||
+    if (cudaEventCreateWithFlags(&h.chunk[i], cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h.panel_in[i], cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&h.gemm[i], cudaEventDisableTiming) != cudaSuccess)
       return B2G_ERR_CUDA;
   h.init = true;
@@ -595,9 +622,19 @@ int run_host(const Call& c, void* stream) {
   const bool read_c = c.beta != 0.f;
   const size_t M = (size_t)c.M, N = (size_t)c.N, K = (size_t)c.K;
   const size_t kp = (K + 3) / 4 * 4, np = (N + 3) / 4 * 4;  // padded row lengths (floats)
+  // K chunks (16-aligned boundaries) and row panels of the last chunk
+  const int chunks = (gemm && c.K >= 2048) ? 4 : 1;
+  const int kc = ((c.K + chunks - 1) / chunks + 15) / 16 * 16;
+  int panels = c.M / 1024;
+  panels = panels < 1 ? 1 : panels > kHostPanelsMax ? kHostPanelsMax : panels;
+  const int rows = ((c.M + panels - 1) / panels + 127) / 128 * 128;
+  panels = (c.M + rows - 1) / rows;
+  const bool separate_c = chunks > 1 && read_c;  // C kept apart, added at the end
+
   const size_t a_bytes = gemm ? round256(M * kp * 4) : 0;
   const size_t b_bytes = gemm ? round256(K * np * 4) : 0;
-  const size_t need = a_bytes + b_bytes + round256(M * np * 4);
+  const size_t d_bytes = round256(M * np * 4);
+  const size_t need = a_bytes + b_bytes + d_bytes + (separate_c ? d_bytes : 0);
 
   HostPath& h = g_hostpath[dev];
   std::lock_guard<std::mutex> lk(h.mu);
@@ -622,47 +659,90 @@ int run_host(const Call& c, void* stream) {
   char* base = static_cast<char*>(h.buf);
   float* dA = reinterpret_cast<float*>(base);
   float* dB = reinterpret_cast<float*>(base + a_bytes);
-  float* dC = reinterpret_cast<float*>(base + a_bytes + b_bytes);
+  float* dD = reinterpret_cast<float*>(base + a_bytes + b_bytes);
+  float* dC = separate_c ? reinterpret_cast<float*>(base + a_bytes + b_bytes + d_bytes) : dD;
 
-  // panels of about 1024 rows (at least two waves of output tiles each)
-  int panels = c.M / 1024;
-  panels = panels < 1 ? 1 : panels > kHostPanelsMax ? kHostPanelsMax : panels;
-  const int rows = ((c.M + panels - 1) / panels + 127) / 128 * 128;
-  panels = (c.M + rows - 1) / rows;
-
-  auto fail = [&](cudaError_t e) { return e == cudaSuccess ? 0 : B2G_ERR_CUDA; };
-  if (gemm) {
-    rc = fail(cudaMemcpy2DAsync(dB, np * 4, c.B, (size_t)c.ldb * 4, N * 4, K,
+  auto ok = [](cudaError_t e) { return e == cudaSuccess ? 0 : B2G_ERR_CUDA; };
+  const int lda_d = (int)(kp > 0 ? kp : 1);
+  // copy stream: chunks of B's rows and A's columns, then C
+  if (chunks > 1) {
+    for (int j = 0; j < chunks && !rc; ++j) {
+      const int k0 = j * kc, k1 = (j + 1) * kc < c.K ? (j + 1) * kc : c.K;
+      rc = ok(cudaMemcpy2DAsync(dB + (size_t)k0 * np, np * 4, c.B + (size_t)k0 * c.ldb,
+                                (size_t)c.ldb * 4, N * 4, (size_t)(k1 - k0),
                                 cudaMemcpyHostToDevice, h.h2d));
-    if (!rc) rc = fail(cudaEventRecord(h.b_in, h.h2d));
-    if (!rc) rc = fail(cudaStreamWaitEvent(st, h.b_in, 0));
+      if (!rc)
+        rc = ok(cudaMemcpy2DAsync(dA + k0, kp * 4, c.A + k0, (size_t)c.lda * 4,
+                                  (size_t)(k1 - k0) * 4, M, cudaMemcpyHostToDevice, h.h2d));
+      if (!rc) rc = ok(cudaEventRecord(h.chunk[j], h.h2d));
+    }
+    if (!rc && separate_c) {
+      rc = ok(cudaMemcpy2DAsync(dC, np * 4, c.C, (size_t)c.ldc * 4, N * 4, M,
+                                cudaMemcpyHostToDevice, h.h2d));
+      if (!rc) rc = ok(cudaEventRecord(h.c_in, h.h2d));
+    }
+    // all chunks but the last, over all rows, into D
+    for (int j = 0; j + 1 < chunks && !rc; ++j) {
+      const int k0 = j * kc, k1 = (j + 1) * kc;
+      rc = ok(cudaStreamWaitEvent(st, h.chunk[j], 0));
+      if (!rc) {
+        Call pc{0, 0, c.M, c.N, k1 - k0, c.alpha, j == 0 ? 0.f : 1.f, dA + k0, lda_d,
+                dB + (size_t)k0 * np, (int)np, dD, (int)np};
+        rc = run(pc, -1, st);
+      }
+    }
+    if (!rc) rc = ok(cudaStreamWaitEvent(st, h.chunk[chunks - 1], 0));
+    if (!rc && separate_c) rc = ok(cudaStreamWaitEvent(st, h.c_in, 0));
+  } else if (gemm) {
+    rc = ok(cudaMemcpy2DAsync(dB, np * 4, c.B, (size_t)c.ldb * 4, N * 4, K,
+                              cudaMemcpyHostToDevice, h.h2d));
+    if (!rc) rc = ok(cudaEventRecord(h.chunk[0], h.h2d));
+    if (!rc) rc = ok(cudaStreamWaitEvent(st, h.chunk[0], 0));
   }
+  // the last chunk (or the only one), panel by panel, then back to the host
+  const int kl0 = (chunks - 1) * kc;
   for (int i = 0; i < panels && !rc; ++i) {
     const size_t r0 = (size_t)i * rows;
     const size_t rn = (size_t)(c.M - (int)r0 < rows ? c.M - (int)r0 : rows);
-    if (gemm)
-      rc = fail(cudaMemcpy2DAsync(dA + r0 * kp, kp * 4, c.A + r0 * c.lda, (size_t)c.lda * 4,
+    if (chunks == 1) {  // A's and C's rows of this panel come now
+      if (gemm)
+        rc = ok(cudaMemcpy2DAsync(dA + r0 * kp, kp * 4, c.A + r0 * c.lda, (size_t)c.lda * 4,
                                   K * 4, rn, cudaMemcpyHostToDevice, h.h2d));
-    if (!rc && read_c)
-      rc = fail(cudaMemcpy2DAsync(dC + r0 * np, np * 4, c.C + r0 * c.ldc, (size_t)c.ldc * 4,
+      if (!rc && read_c)
+        rc = ok(cudaMemcpy2DAsync(dD + r0 * np, np * 4, c.C + r0 * c.ldc, (size_t)c.ldc * 4,
                                   N * 4, rn, cudaMemcpyHostToDevice, h.h2d));
-    if (!rc) rc = fail(cudaEventRecord(h.a_in[i], h.h2d));
-    if (!rc) rc = fail(cudaStreamWaitEvent(st, h.a_in[i], 0));
+      if (!rc) rc = ok(cudaEventRecord(h.panel_in[i], h.h2d));
+      if (!rc) rc = ok(cudaStreamWaitEvent(st, h.panel_in[i], 0));
+    }
     if (!rc) {
-      Call pc{0, 0, (int)rn, c.N, c.K, c.alpha, c.beta, dA + r0 * kp, (int)(kp > 0 ? kp : 1), dB,
-              (int)np, dC + r0 * np, (int)np};
+      const float beta = chunks == 1 ? c.beta : 1.f;
+      Call pc{0, 0, (int)rn, c.N, c.K - kl0, c.alpha, beta, dA + r0 * kp + kl0, lda_d,
+              dB + (size_t)kl0 * np, (int)np, dD + r0 * np, (int)np};
       rc = run(pc, -1, st);
     }
-    if (!rc) rc = fail(cudaEventRecord(h.gemm[i], st));
-    if (!rc) rc = fail(cudaStreamWaitEvent(h.d2h, h.gemm[i], 0));
+    if (!rc && separate_c) {  // D += beta * C over the panel
+      const int n4 = (int)(np / 4);
+      long long blocks = ((long long)rn * n4 + 255) / 256;
+      if (blocks > (long long)d->sms * 8) blocks = (long long)d->sms * 8;
+      float* dDp = dD + r0 * np;
+      const float* dCp = dC + r0 * np;
+      int rn_i = (int)rn;
+      float beta = c.beta;
+      long long ld = (long long)np;
+      void* args[] = {&rn_i, (void*)&n4, &beta, (void*)&dCp, &ld, &dDp, &ld};
+      rc = ok(cudaLaunchKernel(reinterpret_cast<const void*>(&axpby_rows_kernel),
+                               dim3((unsigned)blocks), dim3(256), args, 0, st));
+    }
+    if (!rc) rc = ok(cudaEventRecord(h.gemm[i], st));
+    if (!rc) rc = ok(cudaStreamWaitEvent(h.d2h, h.gemm[i], 0));
     if (!rc)
-      rc = fail(cudaMemcpy2DAsync(c.C + r0 * c.ldc, (size_t)c.ldc * 4, dC + r0 * np, np * 4,
-                                  N * 4, rn, cudaMemcpyDeviceToHost, h.d2h));
+      rc = ok(cudaMemcpy2DAsync(c.C + r0 * c.ldc, (size_t)c.ldc * 4, dD + r0 * np, np * 4,
+                                N * 4, rn, cudaMemcpyDeviceToHost, h.d2h));
   }
   // join: the caller's stream holds the whole call; later calls wait for it
-  if (!rc) rc = fail(cudaEventRecord(h.c_out, h.d2h));
-  if (!rc) rc = fail(cudaStreamWaitEvent(st, h.c_out, 0));
-  if (!rc) rc = fail(cudaEventRecord(h.done, st));
+  if (!rc) rc = ok(cudaEventRecord(h.c_out, h.d2h));
+  if (!rc) rc = ok(cudaStreamWaitEvent(st, h.c_out, 0));
+  if (!rc) rc = ok(cudaEventRecord(h.done, st));
   if (!rc) h.used = true;
   return rc;
 }
