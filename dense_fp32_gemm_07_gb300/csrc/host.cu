@@ -176,7 +176,7 @@ const PlanGroup kGroups[] = {
     {kPlansTMA, &kNumPlansTMA},         {kPlansT, &kNumPlansT},
     {kPlansT64x128, &kNumPlansT64x128}, {kPlansT128x64, &kNumPlansT128x64},
     {kPlansT128x128, &kNumPlansT128x128}, {kPlansGeneral, &kNumPlansGeneral},
-    {kPlansSkinny, &kNumPlansSkinny},
+    {kPlansSkinny, &kNumPlansSkinny},     {kPlansSkinnyTma, &kNumPlansSkinnyTma},
 };
 
 int num_plans() {
@@ -201,6 +201,8 @@ int plan_index(const char* name) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool is_skinny(const Plan& pl) { return pl.feed == kFeedSkinny || pl.feed == kFeedSkinnyTMA; }
 
 constexpr int kHostPanelsMax = 16;  // row panels of b2g_sgemm_host
 
@@ -247,7 +249,7 @@ int operand_class(const Call& c) {
 bool plan_accepts(const Plan& pl, const Call& c) {
   if (pl.feed == kFeedCpAsync) return true;
   const int cls = operand_class(c);
-  if (pl.feed == kFeedSkinny)
+  if (is_skinny(pl))
     return cls == kClassFast && c.M <= pl.BM && c.N % 4 == 0 && c.batch <= 65535;
   if (pl.pretranspose == 2) return true;  // packing accepts any operands
   if (pl.pretranspose == 1) return cls == kClassFast;
@@ -300,11 +302,13 @@ int skinny_splits(const Plan& pl, const Call& c, int* kc) {
   plan_capacity(pl, &sms, &occ);
   const long long slabs = (c.N + 127) / 128 * (c.batch > 0 ? c.batch : 1);
   long long S = (long long)sms * occ / slabs;
-  const long long smax = c.K / 64 > 1 ? c.K / 64 : 1;
+  long long smax = c.K / 64 > 1 ? c.K / 64 : 1;
+  if (pl.feed == kFeedSkinnyTMA && smax > 8) smax = 8;  // the k slabs of a slab form one cluster
   if (S > smax) S = smax;
   if (S < 1) S = 1;
   long long k = (c.K + S - 1) / S;
-  k = (k + 15) / 16 * 16;
+  const long long granule = pl.feed == kFeedSkinnyTMA ? pl.BK : 16;  // whole stages per split
+  k = (k + granule - 1) / granule * granule;
   *kc = (int)k;
   return (int)((c.K + k - 1) / k);
 }
@@ -318,7 +322,7 @@ constexpr int kMinSliceK = 128;
 
 int tail_split(const Plan& pl, const Call& c, int* first) {
   *first = 0;
-  if (pl.feed == kFeedSkinny || !pl.occupancy) return 1;
+  if (is_skinny(pl) || !pl.occupancy) return 1;
   const long long tiles =
       (long long)((c.M + pl.BM - 1) / pl.BM) * ((c.N + pl.BN - 1) / pl.BN) * c.batch;
   int sms = 0, occ = 0;
@@ -351,7 +355,7 @@ size_t plan_base_bytes(const Plan& pl, const Call& c) {
   if (pl.pretranspose == 1) return nb * (size_t)c.K * (size_t)pre_ld(c.M) * sizeof(float);
   if (pl.pretranspose == 2)
     return nb * (size_t)c.K * (size_t)(pre_ld(c.M) + pre_ld(c.N)) * sizeof(float);
-  if (pl.feed == kFeedSkinny) {
+  if (pl.feed == kFeedSkinny) {  // partial sums per k slab (the cluster plans keep them on chip)
     int kc = 0;
     const int S = skinny_splits(pl, c, &kc);
     return S > 1 ? nb * (size_t)S * c.M * c.N * sizeof(float) : 0;
@@ -509,7 +513,9 @@ int run(const Call& c, int forced_plan, void* stream, void* user_ws = nullptr,
   p.status = d->status;
   p.work = nullptr, p.splits = 1, p.kc = c.K;
   p.tail_first = 0, p.tail_splits = 1;
-  if (pl->feed == kFeedSkinny && ws) {
+  if (pl->feed == kFeedSkinnyTMA) {  // split k slabs meet in a cluster: no workspace
+    p.splits = skinny_splits(*pl, c, &p.kc);
+  } else if (pl->feed == kFeedSkinny && ws) {
     p.splits = skinny_splits(*pl, c, &p.kc);
     p.work = ws;
   } else if (ws && tail_S > 1) {
@@ -539,7 +545,13 @@ int run(const Call& c, int forced_plan, void* stream, void* user_ws = nullptr,
   CUtensorMap tmA, tmB;
   const CUtensorMap* pA = nullptr;
   const CUtensorMap* pB = nullptr;
-  if (e == cudaSuccess && pl->feed != kFeedCpAsync && pl->feed != kFeedSkinny) {
+  if (e == cudaSuccess && pl->feed == kFeedSkinnyTMA) {
+    // A {K, M, batch} in boxes of 32 k x BM rows; B {N, K, batch} in boxes of
+    // 128 columns x 32 k
+    rc = encode_2d(&tmA, p.A, c.K, c.M, p.lda, pl->BK, pl->BM, c.batch, p.strideA);
+    if (!rc) rc = encode_2d(&tmB, p.B, c.N, c.K, p.ldb, pl->BN, pl->BK, c.batch, p.strideB);
+    pA = &tmA, pB = &tmB;
+  } else if (e == cudaSuccess && pl->feed != kFeedCpAsync && pl->feed != kFeedSkinny) {
     if (pl->feed != kFeedTMA || pl->alayout == kAKChunk)
       rc = encode_a_kchunk(&tmA, p.A, c.M, c.K, (int)p.lda, pl->BM, pl->BK, c.batch, p.strideA);
     else  // A stored K x M
@@ -914,6 +926,8 @@ int b2g_sgemm_launch_count(int transA, int transB, int M, int N, int K, float al
   if (pl->feed == kFeedSkinny) {
     int kc = 0;
     if (skinny_splits(*pl, c, &kc) > 1) n += 1;  // the split-K reduction
+  } else if (pl->feed == kFeedSkinnyTMA) {
+    // the split-K sums are added inside the kernel's clusters
   } else {
     int first = 0;
     if (tail_split(*pl, c, &first) > 1) n += 1;  // the split tail's reduction

@@ -49,6 +49,7 @@ enum Feed : int {
   kFeedTMATrans = 2,  // bulk-tensor copies; A lands k-chunked in a staging slot and the
                       // consumer warps rewrite it transposed ([BK][BM]) a few stages ahead
   kFeedSkinny = 3,    // skinny-M split-K kernel: B streamed from global, A staged per k slab
+  kFeedSkinnyTMA = 4,  // skinny-M split-K kernel: B and A in bulk-tensor stages
 };
 
 constexpr int kMaxDevices = 64;
@@ -74,11 +75,16 @@ struct Plan {
                        // failure); the host sizes split-K and split tails by it
 };
 
-// Skinny-M plans (M <= BM), compiled in skinny.cu.
+// Skinny-M plans (M <= BM), compiled in skinny.cu and skinny_tma.cu.
 extern const Plan kPlansSkinny[];
 extern const int kNumPlansSkinny;
+extern const Plan kPlansSkinnyTma[];
+extern const int kNumPlansSkinnyTma;
 // C = alpha * sum_s P[s] + beta * C over the M x N window (split-K reduction).
-cudaError_t launch_splitk_reduce(const SgemmParams& p, cudaStream_t stream, int num_sms);
+// dependent: launched as a programmatic dependent of the kernel just before it
+// on `stream` (it may start early and waits for that kernel's results).
+cudaError_t launch_splitk_reduce(const SgemmParams& p, cudaStream_t stream, int num_sms,
+                                 bool dependent);
 
 // FFMA plans' split tail: C = alpha * (slice 0 + slice 1 + ...) + beta * C for
 // every split tile (p.tail_splits > 1), BM x BN the plan's tile.

@@ -141,8 +141,12 @@ __global__ void __launch_bounds__(kSkThreads) skinny_kernel(const __grid_constan
   }
 }
 
-// C = alpha * (P[0] + P[1] + ... + P[S-1]) + beta * C, partials added in s order.
+// C = alpha * (P[0] + P[1] + ... + P[S-1]) + beta * C, partials added in s order
+// (eight loads in flight per thread, the additions still in s order).  When
+// launched as a programmatic dependent of the split-K kernel it starts early
+// and waits here until that kernel has finished and its writes are visible.
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constant__ SgemmParams p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const long long nv = p.N / 4;
   const long long per = (long long)p.M * nv;
   const long long total = per * p.batch;
@@ -154,7 +158,15 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constan
     const long long m = r / nv, c = (r - m * nv) * 4;
     const float* w = p.work + bz * p.splits * plane + m * p.N + c;
     float4 sum = *reinterpret_cast<const float4*>(w);
-    for (int s = 1; s < p.splits; ++s) {
+    int s = 1;
+    for (; s + 8 <= p.splits; s += 8) {
+      float4 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = *reinterpret_cast<const float4*>(w + (s + j) * plane);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) sum.x += v[j].x, sum.y += v[j].y, sum.z += v[j].z, sum.w += v[j].w;
+    }
+    for (; s < p.splits; ++s) {
       const float4 v = *reinterpret_cast<const float4*>(w + s * plane);
       sum.x += v.x, sum.y += v.y, sum.z += v.z, sum.w += v.w;
     }
@@ -178,7 +190,8 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constan
   }
 }
 
-cudaError_t launch_splitk_reduce(const SgemmParams& p, cudaStream_t stream, int num_sms) {
+cudaError_t launch_splitk_reduce(const SgemmParams& p, cudaStream_t stream, int num_sms,
+                                 bool dependent) {
   const long long total = (long long)p.M * (p.N / 4) * p.batch;
   long long blocks = (total + 255) / 256;
   const long long cap = (long long)num_sms * 8;
@@ -186,8 +199,16 @@ cudaError_t launch_splitk_reduce(const SgemmParams& p, cudaStream_t stream, int 
   if (blocks < 1) blocks = 1;
   SgemmParams pc = p;
   void* args[] = {&pc};
-  return cudaLaunchKernel(reinterpret_cast<const void*>(&splitk_reduce_kernel),
-                          dim3((unsigned)blocks), dim3(256), args, 0, stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = dependent ? 1 : 0;
+  return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(&splitk_reduce_kernel), args);
 }
 
 // CTAs of skinny_kernel<MR, UNR> resident per SM on the current device (the
@@ -230,7 +251,7 @@ cudaError_t launch_skinny(const SgemmParams& p, const CUtensorMap*, const CUtens
   void* args[] = {&pc};
   e = cudaLaunchKernel(reinterpret_cast<const void*>(kern), grid, dim3(kSkThreads), args,
                        SkinnyCfg<MR>::kSmemBytes, stream);
-  if (e == cudaSuccess && p.splits > 1) e = launch_splitk_reduce(p, stream, num_sms);
+  if (e == cudaSuccess && p.splits > 1) e = launch_splitk_reduce(p, stream, num_sms, false);
   return e;
 }
 

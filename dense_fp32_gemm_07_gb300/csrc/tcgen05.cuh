@@ -1,7 +1,7 @@
 // tcgen05.cuh -- inline PTX for the 5th-generation tensor cores: tensor-memory
 // allocation, tcgen05.mma / commit / ld, shared-memory matrix descriptors, and
-// the cluster primitives of the CTA-pair kernel.  Used by tf32x3.cu only (the
-// FFMA kernels need ptx.cuh alone).
+// cluster primitives (the CTA-pair kernel; the skinny kernel's in-cluster
+// split-K reduction).  The FFMA kernels need ptx.cuh alone.
 #pragma once
 #include <cstdint>
 
@@ -106,7 +106,16 @@ __device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t cluster_addr)
   return v;
 }
 
-// Every thread of both CTAs arrives, then waits for all the others.
+__device__ __forceinline__ float4 ld_shared_cluster_f4(uint32_t cluster_addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(cluster_addr)
+               : "memory");
+  return v;
+}
+
+// Every thread of every CTA of the cluster arrives, then waits for all the others.
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                    : "memory");

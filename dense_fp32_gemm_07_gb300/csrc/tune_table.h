@@ -28,7 +28,13 @@ constexpr int kInf = 0x7fffffff;
 // (128^3 .. 8192^3), the 8192x11008x4096 and 16x4096x4096 shapes and the
 // ragged 1000x1025x777 shape.
 const TuneRule kTuneTable[] = {
-    // skinny M: split-K over B streamed from global memory (N % 4 == 0)
+    // skinny M (N % 4 == 0): split-K.  From N = 2048 (16 column slabs) the
+    // bulk-tensor fed plans whose k slabs add up inside a cluster of <= 8
+    // CTAs; below, B streamed from global memory with up to one resident wave
+    // of k splits and a reduction kernel (more k parallelism than 8 slabs)
+    {kClassFast, 0, 8, 2048, kInf, 0, "skinnyT_m8", nullptr},
+    {kClassFast, 9, 16, 2048, kInf, 0, "skinnyT_m16", nullptr},
+    {kClassFast, 17, 32, 2048, kInf, 0, "skinnyT_m32", nullptr},
     {kClassFast, 0, 8, 0, kInf, 0, "skinny_m8", nullptr},
     {kClassFast, 9, 16, 0, kInf, 0, "skinny_m16", nullptr},
     {kClassFast, 17, 32, 0, kInf, 0, "skinny_m32", nullptr},

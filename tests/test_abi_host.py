@@ -104,8 +104,9 @@ def _plan(b2g, *a):
 def test_tune_table_classes(b2g):
     # aligned, ld % 4 == 0, K % 4 == 0 -> bulk-tensor plans; large ones pre-transpose A
     assert _plan(b2g, 0, 0, 4096, 4096, 4096, 1.0, FAKE, 4096, FAKE, 4096, FAKE, 4096).startswith("pre_")
-    assert _plan(b2g, 0, 0, 16, 4096, 4096, 1.0, FAKE, 4096, FAKE, 4096, FAKE, 4096) == "skinny_m16"
-    assert _plan(b2g, 0, 0, 32, 4096, 4096, 1.0, FAKE, 4096, FAKE, 4096, FAKE, 4096) == "skinny_m32"
+    assert _plan(b2g, 0, 0, 16, 4096, 4096, 1.0, FAKE, 4096, FAKE, 4096, FAKE, 4096) == "skinnyT_m16"
+    assert _plan(b2g, 0, 0, 32, 4096, 4096, 1.0, FAKE, 4096, FAKE, 4096, FAKE, 4096) == "skinnyT_m32"
+    assert _plan(b2g, 0, 0, 16, 1024, 8192, 1.0, FAKE, 8192, FAKE, 1024, FAKE, 1024) == "skinny_m16"
     # skinny M with N % 4 != 0 takes a tiled plan
     assert _plan(b2g, 0, 0, 16, 4095, 4096, 1.0, FAKE, 4096, FAKE, 4096, FAKE, 4096).startswith("tma_")
     assert _plan(b2g, 0, 0, 64, 64, 64, 1.0, FAKE, 64, FAKE, 64, FAKE, 64).startswith("tma_")
@@ -176,10 +177,14 @@ def test_workspace_size_query(b2g):
     assert rc == 0 and n == want_bytes(4096 * 1004 * 4, 1001, 4096, 4096, BM, BN)
     rc, n = b2g.b2g_sgemm_workspace_size(0, 0, 64, 64, 64, 1.0, FAKE, 64, FAKE, 64, FAKE, 64)
     assert rc == 0 and n == 0  # one tile, 64 k: nothing to split
-    # skinny: split-K partial sums, S x M x N floats for some S > 1
+    # skinny, N >= 2048: the k slabs add up inside clusters, no workspace
     rc, n = b2g.b2g_sgemm_workspace_size(0, 0, 16, 4096, 4096, 1.0, FAKE, 4096, FAKE, 4096,
                                          FAKE, 4096)
-    assert rc == 0 and n > 0 and n % (16 * 4096 * 4) == 0
+    assert rc == 0 and n == 0
+    # skinny, small N: split-K partial sums, S x M x N floats for some S > 1
+    rc, n = b2g.b2g_sgemm_workspace_size(0, 0, 16, 1024, 8192, 1.0, FAKE, 8192, FAKE, 1024,
+                                         FAKE, 1024)
+    assert rc == 0 and n > 0 and n % (16 * 1024 * 4) == 0
     rc, n = b2g.b2g_sgemm_workspace_size(0, 0, 64, 64, 64, 1.0, FAKE, 63, FAKE, 64, FAKE, 64)
     assert rc == -2
     # packing: A^T (K x round_up(M, 4)) and B (K x round_up(N, 4)), then the tail
@@ -202,7 +207,8 @@ def test_launch_count_query(b2g):
     assert count(64, 64, 64, alpha=0.0) == 1 and count(64, 64, 0) == 1  # C = beta * C
     assert count(64, 64, 64) == 1                    # one tile, one kernel
     assert count(4096, 4096, 4096) == 3              # transpose, GEMM, tail reduction
-    assert count(16, 4096, 4096) == 2                # skinny split-K and its reduction
+    assert count(16, 4096, 4096) == 1                # skinny, split-K summed in clusters
+    assert count(16, 1024, 8192) == 2                # skinny split-K and its reduction
     assert count(1000, 1025, 777, lda=777) == 4      # two packing launches, GEMM, tail
     rc, _ = b2g.b2g_sgemm_launch_count(0, 0, 64, 64, 64, 1.0, FAKE, 63, FAKE, 64, FAKE, 64)
     assert rc == -2
