@@ -95,6 +95,8 @@ __global__ void __launch_bounds__(kSkThreads) skinny_kernel(const __grid_constan
     }
     __syncthreads();  // As is restaged by the next chunk
   }
+  // the reduction kernel may launch now; it waits for this grid's results
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // warps 1..3 -> shared memory; warp 0 adds them in warp order
   if (warp > 0) {
@@ -251,7 +253,7 @@ cudaError_t launch_skinny(const SgemmParams& p, const CUtensorMap*, const CUtens
   void* args[] = {&pc};
   e = cudaLaunchKernel(reinterpret_cast<const void*>(kern), grid, dim3(kSkThreads), args,
                        SkinnyCfg<MR>::kSmemBytes, stream);
-  if (e == cudaSuccess && p.splits > 1) e = launch_splitk_reduce(p, stream, num_sms, false);
+  if (e == cudaSuccess && p.splits > 1) e = launch_splitk_reduce(p, stream, num_sms, true);
   return e;
 }
 
