@@ -766,11 +766,14 @@ size_t tf32x3_bytes(const Call& c) {
   return 2 * ((size_t)c.M * c.K + (size_t)c.N * c.K) * sizeof(float);
 }
 
-// variant: 0 one CTA per 128 x 128 tile, 1 a CTA pair per 256 x 128 tile.
-// Measured on GB300: the pair is 1-2% faster from 4096^3 up (and insensitive
-// to the tile order), 3% slower at 2048^3 and 4% at 1024^3.
+// variant: 0 one CTA per 128 x 128 tile, 1 a CTA pair per 256 x 128 tile,
+// 2 a CTA pair per 256 x 256 tile.
+// Measured on GB300 (TFLOP/s of FP32 results, variants 0 / 1 / 2): 1536^3
+// 145.8 / 136.0 / 104.0, 2048^3 166.8 / 160.9 / 186.1, 4096^3 232.2 / 236.7 /
+// 275.7, 8192^3 266.1 / 266.7 / 345.9: the 256 x 256 pair (twice the work per
+// MMA instruction) from about 1800^3 up, one CTA per 128 x 128 tile below.
 int tc_default_variant(const Call& c) {
-  return (double)c.M * c.N * c.K >= 2.0e10 ? 1 : 0;
+  return ((double)c.M * c.N * c.K >= 6.0e9 && c.M >= 512 && c.N >= 512) ? 2 : 0;
 }
 
 int run_tf32x3(const Call& c, void* stream, int variant) {
@@ -794,7 +797,8 @@ int run_tf32x3(const Call& c, void* stream, int variant) {
   cudaError_t e = launch_split_a(c.A, c.M, c.K, c.lda, Ahi, Alo, d->sms, st);
   if (e == cudaSuccess) e = launch_split_bt(c.B, c.K, c.N, c.ldb, Bhi, Blo, st);
   CUtensorMap maps[4];
-  const int bbox = variant == 1 ? kTcBN / 2 : kTcBN;  // a pair's CTA stages half of B's columns
+  const int pn = variant == 2 ? 256 : 128;            // a pair's N
+  const int bbox = variant >= 1 ? pn / 2 : kTcBN;     // a pair's CTA stages half of B's columns
   if (e == cudaSuccess) {
     rc = encode_2d_sw128(&maps[0], Ahi, c.K, c.M, c.K, kTcBM);
     if (!rc) rc = encode_2d_sw128(&maps[1], Alo, c.K, c.M, c.K, kTcBM);
@@ -807,15 +811,17 @@ int run_tf32x3(const Call& c, void* stream, int variant) {
     p.alpha = c.alpha, p.beta = c.beta;
     p.C = c.C, p.ldc = c.ldc;
     p.c_vec4 = aligned16(c.C) && c.ldc % 4 == 0;
-    const int tile_m = variant == 1 ? 2 * kTcBM : kTcBM;
+    const int tile_m = variant >= 1 ? 2 * kTcBM : kTcBM;
+    const int tile_n = variant >= 1 ? pn : kTcBN;
     p.tiles_m = (c.M + tile_m - 1) / tile_m;
-    p.tiles_n = (c.N + kTcBN - 1) / kTcBN;
+    p.tiles_n = (c.N + tile_n - 1) / tile_n;
     p.group_m = 8;
     p.k_tiles = (c.K + kTcBK - 1) / kTcBK;
     p.wait_limit_ns = g_wait_limit_ns.load();
     p.debug_stop_ktile = g_debug_stop.load();
     p.status = d->status;
-    e = variant == 1 ? launch_tf32x3_pair(p, maps, d->sms, st) : launch_tf32x3(p, maps, d->sms, st);
+    e = variant >= 1 ? launch_tf32x3_pair(p, maps, pn, d->sms, st)
+                     : launch_tf32x3(p, maps, d->sms, st);
   }
   ws_release(dev, st);
   if (rc) return rc;
@@ -881,7 +887,7 @@ int b2g_sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int lda, 
 int b2g_sgemm_3xtf32_variant(int variant, int M, int N, int K, float alpha, const float* A,
                              int lda, const float* B, int ldb, float beta, float* C, int ldc,
                              void* stream) {
-  if (variant != 0 && variant != 1) return B2G_ERR_INVALID_PLAN;
+  if (variant < 0 || variant > 2) return B2G_ERR_INVALID_PLAN;
   return run_tf32x3(Call{0, 0, M, N, K, alpha, beta, A, lda, B, ldb, C, ldc}, stream, variant);
 }
 

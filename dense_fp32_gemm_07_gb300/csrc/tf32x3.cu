@@ -331,22 +331,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // barrier before tensor memory is freed.
 
 constexpr int kTpThreads = 192;  // warp 0 copies, 1 MMA, 2-5 epilogue
-constexpr int kTpStages = 4;
 constexpr uint32_t kTpATile = 128 * kTcBK * 4;  // this CTA's 128 rows of A_hi or A_lo: 16 KB
-constexpr uint32_t kTpBTile = 64 * kTcBK * 4;   // this CTA's 64 rows of B_hi^T or B_lo^T: 8 KB
-constexpr uint32_t kTpStageBytes = 2 * kTpATile + 2 * kTpBTile;  // 48 KB
-constexpr uint32_t kTpTmemCols = 2 * kTcBN;                      // two 128-column accumulators
-constexpr int kTpNumBars = 2 * kTpStages + 5;
-// 8 KB of slack after the barriers: an operand read one B tile longer than
-// intended would still stay inside this CTA's shared memory.
-constexpr int kTpSmemBytes = kTpStages * kTpStageBytes + 1024 + kTpNumBars * 8 + 16 + 8192;
 
+// PN: the pair's N per MMA (128 or 256); each CTA stages PN/2 rows of B^T.
+template <int PN>
+struct PairCfg {
+  static constexpr int kStages = PN == 128 ? 4 : 3;
+  static constexpr uint32_t kBTile = (PN / 2) * kTcBK * 4;  // 8 or 16 KB
+  static constexpr uint32_t kStageBytes = 2 * kTpATile + 2 * kBTile;  // 48 or 64 KB
+  static constexpr uint32_t kTmemCols = 2 * PN;                      // two accumulators
+  static constexpr int kNumBars = 2 * kStages + 5;
+  // 8 KB of slack after the barriers: an operand read one B tile longer than
+  // intended would still stay inside this CTA's shared memory.
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + kNumBars * 8 + 16 + 8192;
+  static_assert(PN == 128 || PN == 256, "pair tiles are 256 x 128 or 256 x 256");
+};
+
+template <int PN>
 __global__ void __launch_bounds__(kTpThreads, 1)
     sgemm_tf32x3_pair_kernel(const __grid_constant__ Tf32x3Params p,
                              const __grid_constant__ CUtensorMap mAhi,
                              const __grid_constant__ CUtensorMap mAlo,
                              const __grid_constant__ CUtensorMap mBhi,
                              const __grid_constant__ CUtensorMap mBlo) {
+  using Cfg = PairCfg<PN>;
+  constexpr int kTpStages = Cfg::kStages;
+  constexpr uint32_t kTpBTile = Cfg::kBTile, kTpStageBytes = Cfg::kStageBytes;
+  constexpr uint32_t kTpTmemCols = Cfg::kTmemCols;
+  constexpr int kTpNumBars = Cfg::kNumBars;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle atoms: 1024-byte aligned
@@ -403,7 +415,7 @@ __global__ void __launch_bounds__(kTpThreads, 1)
         int tm, tn;
         tc_tile_coords(p, tile, tm, tn);
         const int ma = tm * 2 * kTcBM + (int)rank * kTcBM;    // this CTA's rows of A
-        const int nb = tn * kTcBN + (int)rank * (kTcBN / 2);  // this CTA's rows of B^T
+        const int nb = tn * PN + (int)rank * (PN / 2);  // this CTA's rows of B^T
         for (int kt = 0; kt < p.k_tiles; ++kt) {
           if (p.debug_stop_ktile >= 0 && issued >= p.debug_stop_ktile) goto copies_done;
           if (!mbar_wait(empty(s), ph ^ 1u, p.wait_limit_ns, p.status, kStatusTimeoutEmpty))
@@ -435,14 +447,14 @@ __global__ void __launch_bounds__(kTpThreads, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer (even CTA)
     if (even && lane == 0) {
-      constexpr uint32_t idesc = idesc_tf32(2 * kTcBM, kTcBN);
+      constexpr uint32_t idesc = idesc_tf32(2 * kTcBM, PN);
       int s = 0, a = 0;
       uint32_t ph = 0, aph = 0;
       for (int tile = pair; tile < total_tiles; tile += npairs) {
         if (!mbar_wait(tempty(a), aph ^ 1u, p.wait_limit_ns, p.status, kStatusTimeoutTmem))
           goto mma_done;
         tc_fence_after_sync();
-        const uint32_t d = tmem + (uint32_t)(a * kTcBN);
+        const uint32_t d = tmem + (uint32_t)(a * PN);
         for (int kt = 0; kt < p.k_tiles; ++kt) {
           if (!mbar_wait(full(s), ph, p.wait_limit_ns, p.status, kStatusTimeoutFull)) goto mma_done;
           tc_fence_after_sync();
@@ -485,12 +497,12 @@ __global__ void __launch_bounds__(kTpThreads, 1)
       const int r = tm * 2 * kTcBM + (int)rank * kTcBM + 32 * q + lane;
       float* crow = p.C + (long long)r * p.ldc;
 #pragma unroll 1
-      for (int c = 0; c < kTcBN / 32; ++c) {
+      for (int c = 0; c < PN / 32; ++c) {
         uint32_t v[32];
-        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(a * kTcBN + 32 * c), v);
+        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(a * PN + 32 * c), v);
         tmem_ld_wait();
         if (r < p.M) {
-          const int n = tn * kTcBN + 32 * c;
+          const int n = tn * PN + 32 * c;
           if (p.c_vec4 && n + 31 < p.N) {
 #pragma unroll
             for (int j = 0; j < 32; j += 4) {
@@ -585,8 +597,10 @@ cudaError_t launch_tf32x3(const Tf32x3Params& p, const CUtensorMap* maps, int nu
                           dim3(kTcThreads), args, kTcSmemBytes, stream);
 }
 
-cudaError_t launch_tf32x3_pair(const Tf32x3Params& p, const CUtensorMap* maps, int num_sms,
-                               cudaStream_t stream) {
+template <int PN>
+cudaError_t launch_pair(const Tf32x3Params& p, const CUtensorMap* maps, int num_sms,
+                        cudaStream_t stream) {
+  using Cfg = PairCfg<PN>;
   // Per device, once: opt in to the shared memory and ask how many CTA pairs
   // can be resident at once (the persistent grid is that many pairs).
   static std::atomic<int> resident_pairs[kMaxDevices];
@@ -601,15 +615,15 @@ cudaError_t launch_tf32x3_pair(const Tf32x3Params& p, const CUtensorMap* maps, i
   attr[0].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kTpThreads);
-  cfg.dynamicSmemBytes = kTpSmemBytes;
+  cfg.dynamicSmemBytes = Cfg::kSmemBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const void* kern = reinterpret_cast<const void*>(&sgemm_tf32x3_pair_kernel);
+  const void* kern = reinterpret_cast<const void*>(&sgemm_tf32x3_pair_kernel<PN>);
   int pairs = resident_pairs[dev].load(std::memory_order_acquire);
   if (pairs == 0) {
-    e = cudaFuncSetAttribute(sgemm_tf32x3_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kTpSmemBytes);
+    e = cudaFuncSetAttribute(sgemm_tf32x3_pair_kernel<PN>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
     cfg.gridDim = dim3((unsigned)(num_sms & ~1));
     e = cudaOccupancyMaxActiveClusters(&pairs, kern, &cfg);
@@ -623,6 +637,12 @@ cudaError_t launch_tf32x3_pair(const Tf32x3Params& p, const CUtensorMap* maps, i
   CUtensorMap m0 = maps[0], m1 = maps[1], m2 = maps[2], m3 = maps[3];
   void* args[] = {&pc, &m0, &m1, &m2, &m3};
   return cudaLaunchKernelExC(&cfg, kern, args);
+}
+
+cudaError_t launch_tf32x3_pair(const Tf32x3Params& p, const CUtensorMap* maps, int pn,
+                               int num_sms, cudaStream_t stream) {
+  return pn == 256 ? launch_pair<256>(p, maps, num_sms, stream)
+                   : launch_pair<128>(p, maps, num_sms, stream);
 }
 
 }  // namespace b2g

@@ -33,10 +33,11 @@ cudaError_t launch_split_bt(const float* B, int K, int N, long long ldb, float* 
 cudaError_t launch_tf32x3(const Tf32x3Params& p, const CUtensorMap* maps, int num_sms,
                           cudaStream_t stream);
 
-// The same GEMM with a CTA pair per 256 x 128 output tile (a cluster of two
-// CTAs, one tcgen05.mma.cta_group::2 per step).  maps: boxes {32, 128} for
-// A_hi and A_lo, {32, 64} for B_hi^T and B_lo^T.  tiles_m counts 256-row tiles.
-cudaError_t launch_tf32x3_pair(const Tf32x3Params& p, const CUtensorMap* maps, int num_sms,
-                               cudaStream_t stream);
+// The same GEMM with a CTA pair per 256 x pn output tile, pn = 128 or 256 (a
+// cluster of two CTAs, one tcgen05.mma.cta_group::2 per step).  maps: boxes
+// {32, 128} for A_hi and A_lo, {32, pn / 2} for B_hi^T and B_lo^T.  tiles_m
+// counts 256-row tiles, tiles_n pn-column tiles.
+cudaError_t launch_tf32x3_pair(const Tf32x3Params& p, const CUtensorMap* maps, int pn,
+                               int num_sms, cudaStream_t stream);
 
 }  // namespace b2g

@@ -11,7 +11,8 @@ every plan runs exactly one launch per shape and nothing is timed: that is the
 form to run under ncu to compare plans' counters.  --plans keeps only the
 plans whose name matches REGEX (re.search); the table's plan is always kept.
 --tf32x3 times the 3xTF32 tensor-core path instead, each kernel variant
-(0: one CTA per tile, 1: a CTA pair per tile), split kernels included.
+(0: one CTA per 128 x 128 tile, 1 and 2: a CTA pair per 256 x 128 or 256 x 256
+tile), split kernels included.
 """
 from __future__ import annotations
 
@@ -89,7 +90,7 @@ def sweep_tf32x3(shapes, once=False, out=sys.stdout):
         C = torch.rand(M, N, device="cuda") * 2 - 1
         flops = 2.0 * M * N * K
         iters = max(3, min(50, int(2e12 / flops)))
-        for variant in (0, 1):
+        for variant in (0, 1, 2):
             def call():
                 b2g.sgemm_3xtf32(A, B, C, alpha, beta, variant=variant)
 

@@ -276,10 +276,11 @@ int b2g_sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int lda, 
  * b2g_sgemm_3xtf32 with a chosen tensor-core kernel: variant 0 runs one CTA
  * per 128 x 128 output tile; variant 1 runs a CTA pair (a cluster of two CTAs
  * on two SMs) per 256 x 128 tile with tcgen05.mma.cta_group::2, each CTA
- * staging half of A's rows and half of B's columns.  Same arguments, result
- * bound and errors as b2g_sgemm_3xtf32, which runs variant 1 from 2e10
- * multiply-adds (M*N*K) up and variant 0 below; any other variant is
- * B2G_ERR_INVALID_PLAN.  For tests and comparisons.
+ * staging half of A's rows and half of B's columns; variant 2 is the CTA pair
+ * on 256 x 256 tiles.  Same arguments, result
+ * bound and errors as b2g_sgemm_3xtf32, which runs variant 2 from 6e9
+ * multiply-adds (M*N*K) up with M and N at least 512, and variant 0 otherwise;
+ * any other variant is B2G_ERR_INVALID_PLAN.  For tests and comparisons.
  */
 int b2g_sgemm_3xtf32_variant(int variant, int M, int N, int K, float alpha, const float* A,
                              int lda, const float* B, int ldb, float beta, float* C, int ldc,

@@ -1,7 +1,7 @@
 """The 3xTF32 tensor-core path (b2g_sgemm_3xtf32) against the oracle, within
 the same elementwise FP32 bound as the FFMA path, for both tensor-core kernels:
-variant 0 (one CTA per 128 x 128 tile) and variant 1 (a CTA pair per 256 x 128
-tile, tcgen05.mma.cta_group::2)."""
+variant 0 (one CTA per 128 x 128 tile), variant 1 (a CTA pair per 256 x 128
+tile, tcgen05.mma.cta_group::2) and variant 2 (a CTA pair per 256 x 256 tile)."""
 import ctypes
 
 import numpy as np
@@ -19,7 +19,7 @@ def tb():
     return env()
 
 
-VARIANTS = [0, 1]
+VARIANTS = [0, 1, 2]
 
 
 def run3(torch, b2g, A, B, C, alpha, beta, variant=None):
@@ -149,6 +149,6 @@ def test_wait_runs_out_and_context_survives(tb, variant):
 def test_unknown_variant(tb):
     torch, b2g = tb
     C = torch.zeros(4, 4, device="cuda")
-    rc = b2g.b2g_sgemm_3xtf32_variant(2, 4, 4, 4, 1.0, C.data_ptr(), 4, C.data_ptr(), 4, 0.0,
+    rc = b2g.b2g_sgemm_3xtf32_variant(3, 4, 4, 4, 1.0, C.data_ptr(), 4, C.data_ptr(), 4, 0.0,
                                       C.data_ptr(), 4, 0)
     assert rc == b2g.B2G_ERR_INVALID_PLAN
