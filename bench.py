@@ -392,7 +392,7 @@ def run_ours(args, w):
         tc_tensor = 3 * w.flops() / (tc_ms * 1e-3) / 1e12  # three TF32 products per term
         line["tf32x3"] = {
             "value": w.flops() / (tc_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": tc_ms,
-            "launches_per_step": 3, "path": "b2g_sgemm_3xtf32 (split kernels + tcgen05 GEMM, CTA pairs on 256 x 256 tiles)",
+            "launches_per_step": 4, "path": "b2g_sgemm_3xtf32 (2 split kernels + tcgen05 GEMM on CTA pairs, 256 x 256 tiles + split-tail reduction)",
             "accuracy": "same elementwise FP32 bound as the FFMA path",
             "roofline": {"bound": "tensor", "achieved": tc_tensor, "peak": tpeak, "unit": UNIT,
                          "frac": tc_tensor / tpeak, "peak_basis": tbasis},

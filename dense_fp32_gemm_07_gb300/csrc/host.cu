@@ -788,17 +788,51 @@ int run_tf32x3(const Call& c, void* stream, int variant) {
   if (c.transA || c.transB || !aligned16(c.A) || c.lda % 4 || c.K % 4) return B2G_ERR_UNSUPPORTED;
   int dev = 0;
   cudaGetDevice(&dev);
-  float* ws = static_cast<float*>(ws_acquire(dev, st, tf32x3_bytes(c)));
+
+  Tf32x3Params p;
+  p.M = c.M, p.N = c.N, p.K = c.K;
+  p.alpha = c.alpha, p.beta = c.beta;
+  p.C = c.C, p.ldc = c.ldc;
+  p.c_vec4 = aligned16(c.C) && c.ldc % 4 == 0;
+  const int pn = variant == 2 ? 256 : 128;            // a pair's N
+  const int bbox = variant >= 1 ? pn / 2 : kTcBN;     // a pair's CTA stages half of B's columns
+  const int tile_m = variant >= 1 ? 2 * kTcBM : kTcBM;
+  const int tile_n = variant >= 1 ? pn : kTcBN;
+  p.tiles_m = (c.M + tile_m - 1) / tile_m;
+  p.tiles_n = (c.N + tile_n - 1) / tile_n;
+  p.group_m = 8;
+  p.k_tiles = (c.K + kTcBK - 1) / kTcBK;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+  p.debug_stop_ktile = g_debug_stop.load();
+  p.status = d->status;
+  p.work = nullptr, p.tail_first = 0, p.tail_splits = 1;
+  // Split tail of the pair kernels: T tiles over G resident pairs, T = q*G + r;
+  // the last r tiles in S = G / r k slices (at least 16 k tiles each).
+  size_t tail_bytes = 0;
+  if (variant >= 1) {
+    const long long T = (long long)p.tiles_m * p.tiles_n;
+    const long long G = tf32x3_pair_capacity(pn, d->sms);
+    if (G > 0 && T % G) {
+      const long long q = T / G, r = T - q * G;
+      long long S = G / r;
+      if (S > p.k_tiles / 16) S = p.k_tiles / 16;
+      if (S >= 2) {
+        p.tail_first = (int)(q * G), p.tail_splits = (int)S;
+        tail_bytes = (size_t)r * S * (2 * kTcBM) * pn * sizeof(float);
+      }
+    }
+  }
+  const size_t split_bytes = (tf32x3_bytes(c) + 255) / 256 * 256;
+  float* ws = static_cast<float*>(ws_acquire(dev, st, split_bytes + tail_bytes));
   if (!ws) return B2G_ERR_UNSUPPORTED;  // capturing, or the workspace cannot be had
   float* Ahi = ws;
   float* Alo = Ahi + (size_t)c.M * c.K;
   float* Bhi = Alo + (size_t)c.M * c.K;
   float* Blo = Bhi + (size_t)c.N * c.K;
+  if (tail_bytes) p.work = ws + split_bytes / sizeof(float);
   cudaError_t e = launch_split_a(c.A, c.M, c.K, c.lda, Ahi, Alo, d->sms, st);
   if (e == cudaSuccess) e = launch_split_bt(c.B, c.K, c.N, c.ldb, Bhi, Blo, st);
   CUtensorMap maps[4];
-  const int pn = variant == 2 ? 256 : 128;            // a pair's N
-  const int bbox = variant >= 1 ? pn / 2 : kTcBN;     // a pair's CTA stages half of B's columns
   if (e == cudaSuccess) {
     rc = encode_2d_sw128(&maps[0], Ahi, c.K, c.M, c.K, kTcBM);
     if (!rc) rc = encode_2d_sw128(&maps[1], Alo, c.K, c.M, c.K, kTcBM);
@@ -806,22 +840,9 @@ int run_tf32x3(const Call& c, void* stream, int variant) {
     if (!rc) rc = encode_2d_sw128(&maps[3], Blo, c.K, c.N, c.K, bbox);
   }
   if (e == cudaSuccess && !rc) {
-    Tf32x3Params p;
-    p.M = c.M, p.N = c.N, p.K = c.K;
-    p.alpha = c.alpha, p.beta = c.beta;
-    p.C = c.C, p.ldc = c.ldc;
-    p.c_vec4 = aligned16(c.C) && c.ldc % 4 == 0;
-    const int tile_m = variant >= 1 ? 2 * kTcBM : kTcBM;
-    const int tile_n = variant >= 1 ? pn : kTcBN;
-    p.tiles_m = (c.M + tile_m - 1) / tile_m;
-    p.tiles_n = (c.N + tile_n - 1) / tile_n;
-    p.group_m = 8;
-    p.k_tiles = (c.K + kTcBK - 1) / kTcBK;
-    p.wait_limit_ns = g_wait_limit_ns.load();
-    p.debug_stop_ktile = g_debug_stop.load();
-    p.status = d->status;
     e = variant >= 1 ? launch_tf32x3_pair(p, maps, pn, d->sms, st)
                      : launch_tf32x3(p, maps, d->sms, st);
+    if (e == cudaSuccess && p.tail_splits > 1) e = launch_tf32x3_tail_reduce(p, pn, st);
   }
   ws_release(dev, st);
   if (rc) return rc;

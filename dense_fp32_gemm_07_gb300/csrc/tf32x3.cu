@@ -347,6 +347,28 @@ struct PairCfg {
   static_assert(PN == 128 || PN == 256, "pair tiles are 256 x 128 or 256 x 256");
 };
 
+// Work unit u of the pair kernels: the first tail_first units are whole tiles,
+// then (with a split tail) every later tile is tail_splits units, slice s
+// covering k tiles [s*k_tiles/S, (s+1)*k_tiles/S); part is the slice's index
+// among all slices (where its raw sums go), -1 for a whole tile.
+__device__ __forceinline__ void tc_unit(const Tf32x3Params& p, int u, int& tile, int& kt0,
+                                        int& kt1, int& part) {
+  if (p.tail_splits <= 1 || u < p.tail_first) {
+    tile = u, kt0 = 0, kt1 = p.k_tiles, part = -1;
+    return;
+  }
+  const int v = u - p.tail_first, S = p.tail_splits, sl = v % S;
+  tile = p.tail_first + v / S;
+  kt0 = (int)((long long)sl * p.k_tiles / S);
+  kt1 = (int)((long long)(sl + 1) * p.k_tiles / S);
+  part = v;
+}
+
+__device__ __forceinline__ int tc_units(const Tf32x3Params& p) {
+  const int tiles = p.tiles_m * p.tiles_n;
+  return p.tail_splits > 1 ? p.tail_first + (tiles - p.tail_first) * p.tail_splits : tiles;
+}
+
 template <int PN>
 __global__ void __launch_bounds__(kTpThreads, 1)
     sgemm_tf32x3_pair_kernel(const __grid_constant__ Tf32x3Params p,
@@ -399,7 +421,7 @@ __global__ void __launch_bounds__(kTpThreads, 1)
   // The even CTA's base address names the pair's accumulator columns in both.
   const uint32_t tmem =
       even ? *tmem_slot : ld_shared_cluster_u32(mapa_shared(smem_addr(tmem_slot), 0));
-  const int total_tiles = p.tiles_m * p.tiles_n;
+  const int units = tc_units(p);
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
 
   if (warp == 0) {
@@ -411,12 +433,14 @@ __global__ void __launch_bounds__(kTpThreads, 1)
       prefetch_tmap(&mBlo);
       int s = 0, issued = 0;
       uint32_t ph = 0;
-      for (int tile = pair; tile < total_tiles; tile += npairs) {
+      for (int u = pair; u < units; u += npairs) {
+        int tile, kt0, kt1, part;
+        tc_unit(p, u, tile, kt0, kt1, part);
         int tm, tn;
         tc_tile_coords(p, tile, tm, tn);
         const int ma = tm * 2 * kTcBM + (int)rank * kTcBM;    // this CTA's rows of A
         const int nb = tn * PN + (int)rank * (PN / 2);  // this CTA's rows of B^T
-        for (int kt = 0; kt < p.k_tiles; ++kt) {
+        for (int kt = kt0; kt < kt1; ++kt) {
           if (p.debug_stop_ktile >= 0 && issued >= p.debug_stop_ktile) goto copies_done;
           if (!mbar_wait(empty(s), ph ^ 1u, p.wait_limit_ns, p.status, kStatusTimeoutEmpty))
             goto copies_done;
@@ -450,12 +474,14 @@ __global__ void __launch_bounds__(kTpThreads, 1)
       constexpr uint32_t idesc = idesc_tf32(2 * kTcBM, PN);
       int s = 0, a = 0;
       uint32_t ph = 0, aph = 0;
-      for (int tile = pair; tile < total_tiles; tile += npairs) {
+      for (int u = pair; u < units; u += npairs) {
+        int tile, kt0, kt1, part;
+        tc_unit(p, u, tile, kt0, kt1, part);
         if (!mbar_wait(tempty(a), aph ^ 1u, p.wait_limit_ns, p.status, kStatusTimeoutTmem))
           goto mma_done;
         tc_fence_after_sync();
         const uint32_t d = tmem + (uint32_t)(a * PN);
-        for (int kt = 0; kt < p.k_tiles; ++kt) {
+        for (int kt = kt0; kt < kt1; ++kt) {
           if (!mbar_wait(full(s), ph, p.wait_limit_ns, p.status, kStatusTimeoutFull)) goto mma_done;
           tc_fence_after_sync();
           const uint32_t st = base + s * kTpStageBytes;
@@ -466,7 +492,7 @@ __global__ void __launch_bounds__(kTpThreads, 1)
             const uint64_t alo = smem_desc_sw128_kmajor(st + kTpATile + off);
             const uint64_t bhi = smem_desc_sw128_kmajor(st + 2 * kTpATile + off);
             const uint64_t blo = smem_desc_sw128_kmajor(st + 2 * kTpATile + kTpBTile + off);
-            mma_tf32_pair(d, alo, bhi, idesc, (kt > 0 || kk > 0) ? 1u : 0u);
+            mma_tf32_pair(d, alo, bhi, idesc, (kt > kt0 || kk > 0) ? 1u : 0u);
             mma_tf32_pair(d, ahi, blo, idesc, 1u);
             mma_tf32_pair(d, ahi, bhi, idesc, 1u);
           }
@@ -489,19 +515,32 @@ __global__ void __launch_bounds__(kTpThreads, 1)
     int a = 0;
     uint32_t aph = 0;
     const float alpha = p.alpha, beta = p.beta;
-    for (int tile = pair; tile < total_tiles; tile += npairs) {
+    for (int u = pair; u < units; u += npairs) {
+      int tile, kt0, kt1, part;
+      tc_unit(p, u, tile, kt0, kt1, part);
       int tm, tn;
       tc_tile_coords(p, tile, tm, tn);
       if (!mbar_wait(tfull(a), aph, p.wait_limit_ns, p.status, kStatusTimeoutTmem)) break;
       tc_fence_after_sync();
       const int r = tm * 2 * kTcBM + (int)rank * kTcBM + 32 * q + lane;
       float* crow = p.C + (long long)r * p.ldc;
+      // a slice of a split tile: its raw sums, this CTA's 128 rows of the
+      // 256 x PN block, for the tail reduction
+      float* wrow = part >= 0 ? p.work + (size_t)part * (2 * kTcBM * PN) +
+                                    (size_t)((int)rank * kTcBM + 32 * q + lane) * PN
+                              : nullptr;
 #pragma unroll 1
       for (int c = 0; c < PN / 32; ++c) {
         uint32_t v[32];
         tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(a * PN + 32 * c), v);
         tmem_ld_wait();
-        if (r < p.M) {
+        if (wrow) {
+#pragma unroll
+          for (int j = 0; j < 32; j += 4)
+            *reinterpret_cast<float4*>(wrow + 32 * c + j) =
+                make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                            __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+        } else if (r < p.M) {
           const int n = tn * PN + 32 * c;
           if (p.c_vec4 && n + 31 < p.N) {
 #pragma unroll
@@ -643,6 +682,89 @@ cudaError_t launch_tf32x3_pair(const Tf32x3Params& p, const CUtensorMap* maps, i
                                int num_sms, cudaStream_t stream) {
   return pn == 256 ? launch_pair<256>(p, maps, num_sms, stream)
                    : launch_pair<128>(p, maps, num_sms, stream);
+}
+
+int tf32x3_pair_capacity(int pn, int num_sms) {
+  static std::atomic<int> cached[2][kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  const int w = pn == 256 ? 1 : 0;
+  int pairs = cached[w][dev].load(std::memory_order_acquire);
+  if (pairs) return pairs;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kTpThreads);
+  cfg.gridDim = dim3((unsigned)(num_sms & ~1));
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const void* kern = pn == 256 ? reinterpret_cast<const void*>(&sgemm_tf32x3_pair_kernel<256>)
+                               : reinterpret_cast<const void*>(&sgemm_tf32x3_pair_kernel<128>);
+  cfg.dynamicSmemBytes = pn == 256 ? PairCfg<256>::kSmemBytes : PairCfg<128>::kSmemBytes;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)cfg.dynamicSmemBytes) != cudaSuccess ||
+      cudaOccupancyMaxActiveClusters(&pairs, kern, &cfg) != cudaSuccess || pairs < 1)
+    return 0;
+  cached[w][dev].store(pairs, std::memory_order_release);
+  return pairs;
+}
+
+// blockIdx.x: split tile (tail_first + blockIdx.x); blockIdx.y and the threads
+// stride over the tile's 256 x pn / 4 float4 positions; slices added in order.
+__global__ void __launch_bounds__(256) tc_tail_reduce_kernel(const __grid_constant__ Tf32x3Params p,
+                                                             int pn) {
+  int tm, tn;
+  tc_tile_coords(p, p.tail_first + (int)blockIdx.x, tm, tn);
+  const int S = p.tail_splits;
+  const size_t tile_elems = (size_t)2 * kTcBM * pn;
+  const float* __restrict__ P = p.work + (size_t)blockIdx.x * S * tile_elems;
+  const int n4 = pn / 4;
+  const int m0 = tm * 2 * kTcBM, n0 = tn * pn;
+  const float alpha = p.alpha, beta = p.beta;
+  for (int q = blockIdx.y * blockDim.x + threadIdx.x; q < 2 * kTcBM * n4;
+       q += gridDim.y * blockDim.x) {
+    const int r = q / n4, c = (q - r * n4) * 4;
+    const int gr = m0 + r, gc = n0 + c;
+    if (gr >= p.M || gc >= p.N) continue;
+    float4 acc = *reinterpret_cast<const float4*>(P + (size_t)q * 4);
+    for (int s = 1; s < S; ++s) {
+      const float4 v = *reinterpret_cast<const float4*>(P + s * tile_elems + (size_t)q * 4);
+      acc.x += v.x, acc.y += v.y, acc.z += v.z, acc.w += v.w;
+    }
+    const float av[4] = {acc.x, acc.y, acc.z, acc.w};
+    float* crow = p.C + (long long)gr * p.ldc;
+    if (p.c_vec4 && gc + 3 < p.N) {
+      float4 o;
+      if (beta != 0.f) {
+        const float4 cv = *reinterpret_cast<const float4*>(crow + gc);
+        o = make_float4(fmaf(alpha, av[0], beta * cv.x), fmaf(alpha, av[1], beta * cv.y),
+                        fmaf(alpha, av[2], beta * cv.z), fmaf(alpha, av[3], beta * cv.w));
+      } else {
+        o = make_float4(alpha * av[0], alpha * av[1], alpha * av[2], alpha * av[3]);
+      }
+      *reinterpret_cast<float4*>(crow + gc) = o;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (gc + e < p.N) {
+          float* o = crow + gc + e;
+          *o = (beta != 0.f) ? fmaf(alpha, av[e], beta * *o) : alpha * av[e];
+        }
+    }
+  }
+}
+
+cudaError_t launch_tf32x3_tail_reduce(const Tf32x3Params& p, int pn, cudaStream_t stream) {
+  const long long n = (long long)p.tiles_m * p.tiles_n - p.tail_first;
+  if (p.tail_splits <= 1 || n <= 0) return cudaSuccess;
+  const unsigned gy = (unsigned)((2 * kTcBM * pn / 4 + 511) / 512);  // 2 float4 per thread
+  Tf32x3Params pc = p;
+  void* args[] = {&pc, &pn};
+  return cudaLaunchKernel(reinterpret_cast<const void*>(&tc_tail_reduce_kernel),
+                          dim3((unsigned)n, gy), dim3(256), args, 0, stream);
 }
 
 }  // namespace b2g

@@ -15,6 +15,12 @@ struct Tf32x3Params {
   unsigned long long wait_limit_ns;
   int debug_stop_ktile;  // < 0 normally; >= 0 stops the copy issuer (timeout test)
   unsigned int* status;
+  // Split tail (CTA-pair kernels): output tiles tail_first .. tiles-1 are each
+  // cut into tail_splits k slices (1: none); a slice writes its raw sums, a
+  // 256 x pn block, to work + (slice unit index) * 256 * pn, and
+  // launch_tf32x3_tail_reduce adds each tile's slices in order.
+  float* work;
+  int tail_first, tail_splits;
 };
 
 // Tile shape of the tensor-core kernel.
@@ -39,5 +45,12 @@ cudaError_t launch_tf32x3(const Tf32x3Params& p, const CUtensorMap* maps, int nu
 // counts 256-row tiles, tiles_n pn-column tiles.
 cudaError_t launch_tf32x3_pair(const Tf32x3Params& p, const CUtensorMap* maps, int pn,
                                int num_sms, cudaStream_t stream);
+
+// CTA pairs of the pn kernel resident at once on the current device (0 on
+// failure): the persistent grid's size, which the host's split tail needs.
+int tf32x3_pair_capacity(int pn, int num_sms);
+
+// C = alpha * (slice 0 + ... ) + beta * C for every split tile of the pn kernel.
+cudaError_t launch_tf32x3_tail_reduce(const Tf32x3Params& p, int pn, cudaStream_t stream);
 
 }  // namespace b2g

@@ -54,12 +54,14 @@ def test_shapes_within_bound(tb, shape, variant):
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
-def test_small_integers_bit_exact(tb, variant):
+@pytest.mark.parametrize("shape", [(200, 160, 512), (600, 520, 2048)])
+def test_small_integers_bit_exact(tb, variant, shape):
     """Integers up to 2^10 are TF32 values (lo = 0) and every partial sum stays
-    below 2^24, so the tensor-core result must be exact."""
+    below 2^24, so the tensor-core result must be exact -- also when the last
+    tiles are split along k (K = 2048 on the CTA-pair kernels)."""
     torch, b2g = tb
     rng = np.random.default_rng(5)
-    M, N, K = 200, 160, 512
+    M, N, K = shape
     A = rng.integers(-3, 4, size=(M, K)).astype(np.float32)
     B = rng.integers(-3, 4, size=(K, N)).astype(np.float32)
     C = rng.integers(-3, 4, size=(M, N)).astype(np.float32)
