@@ -14,6 +14,7 @@
 #include <mutex>
 
 #include "../../include/b2g_sgemm.h"
+#include "plan_registry.h"
 #include "sgemm_params.h"
 #include "tf32x3.h"
 #include "transpose.h"

@@ -20,6 +20,7 @@
 #include <mutex>
 
 #include "../../include/b2g_sgemm.h"
+#include "plan_registry.h"
 #include "sgemm_params.h"
 
 namespace {

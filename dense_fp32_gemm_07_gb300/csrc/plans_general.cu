@@ -1,5 +1,6 @@
 // plans_general.cu -- the 4-byte cp.async fed FFMA plans: any alignment, any
 // leading dimension, both op() flags.  Same fields as plans_tma.cu.
+#include "plan_registry.h"
 #include "sgemm_ffma.cuh"
 
 namespace b2g {

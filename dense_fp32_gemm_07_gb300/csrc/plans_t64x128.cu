@@ -4,6 +4,7 @@
 // compiled, and the three plans that run it: A stored K x M (tmaT_), row-major
 // A transposed into a workspace first (pre_), both operands packed aligned
 // into a workspace first (pack_).  Fields as in plans_tma.cu.
+#include "plan_registry.h"
 #include "sgemm_ffma.cuh"
 
 namespace b2g {

@@ -2,6 +2,7 @@
 // Each line instantiates one kernel of sgemm_ffma.cuh: name, BM, BN, BK, warps
 // along M, warps along N, per-thread columns TN, stages, A layout, feed,
 // producer warps, FFMA issue order.
+#include "plan_registry.h"
 #include "sgemm_ffma.cuh"
 
 namespace b2g {

@@ -1,6 +1,7 @@
 // plans_tmat.cu -- alternative FFMA issue orders of the transposed-A kernels
 // (A stored K x M), kept for comparison sweeps; the plans the tune table uses
 // live one kernel per file in plans_t*.cu.  Fields as in plans_tma.cu.
+#include "plan_registry.h"
 #include "sgemm_ffma.cuh"
 
 namespace b2g {

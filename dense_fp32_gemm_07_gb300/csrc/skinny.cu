@@ -23,6 +23,7 @@
 
 #include <atomic>
 
+#include "plan_registry.h"
 #include "sgemm_params.h"
 
 namespace b2g {

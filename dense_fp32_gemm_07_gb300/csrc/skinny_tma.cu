@@ -34,6 +34,7 @@
 #include <atomic>
 
 #include "ptx.cuh"
+#include "plan_registry.h"
 #include "sgemm_params.h"
 #include "tcgen05.cuh"
 
