@@ -176,6 +176,7 @@ struct PlanGroup {
 const PlanGroup kGroups[] = {
     {kPlansTMA, &kNumPlansTMA},         {kPlansT, &kNumPlansT},
     {kPlansT64x128, &kNumPlansT64x128}, {kPlansT128x64, &kNumPlansT128x64},
+    {kPlansT128x64k32, &kNumPlansT128x64k32},
     {kPlansT128x128, &kNumPlansT128x128}, {kPlansGeneral, &kNumPlansGeneral},
     {kPlansSkinny, &kNumPlansSkinny},     {kPlansSkinnyTma, &kNumPlansSkinnyTma},
 };
