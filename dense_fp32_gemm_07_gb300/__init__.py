@@ -7,7 +7,8 @@ is no fallback when it is missing.
 
 Low-level names mirror the C ABI one to one (``b2g_sgemm``, ``b2g_sgemm_ex``,
 ``b2g_sgemm_with_plan``, ...) and take raw device pointers; ``sgemm`` is the
-tensor-level convenience: ``C <- alpha * op(A) @ op(B) + beta * C`` in place.
+tensor-level convenience: ``C <- alpha * op(A) @ op(B) + beta * C`` in place;
+``sgemm_colmajor`` is the same for column-major tensors.
 """
 from __future__ import annotations
 
@@ -34,7 +35,8 @@ B2G_ERR_SCRATCH_LIMIT = -11
 
 # every symbol include/b2g_sgemm.h declares
 EXPORTS = (
-    "b2g_sgemm", "b2g_sgemm_ex", "b2g_sgemm_with_plan", "b2g_sgemm_select_plan",
+    "b2g_sgemm", "b2g_sgemm_ex", "b2g_sgemm_colmajor", "b2g_sgemm_with_plan",
+    "b2g_sgemm_select_plan",
     "b2g_sgemm_ws", "b2g_sgemm_workspace_size", "b2g_sgemm_launch_count", "b2g_sgemm_host",
     "b2g_release_workspaces", "b2g_sgemm_noalloc",
     "b2g_sgemm_3xtf32", "b2g_sgemm_3xtf32_variant", "b2g_sgemm_strided_batched",
@@ -66,6 +68,7 @@ def _load():
         gemm = [i, i, i, f, vp, i, vp, i, f, vp, i, vp]
         lib.b2g_sgemm.argtypes = gemm
         lib.b2g_sgemm_ex.argtypes = [i, i] + gemm
+        lib.b2g_sgemm_colmajor.argtypes = [i, i] + gemm
         lib.b2g_sgemm_with_plan.argtypes = [i, i, i] + gemm
         lib.b2g_sgemm_select_plan.argtypes = [i, i, i, i, i, f, vp, i, vp, i, vp, i]
         lib.b2g_sgemm_ws.argtypes = [i, i, i, i, i, f, vp, i, vp, i, f, vp, i, vp, ctypes.c_size_t,
@@ -114,6 +117,12 @@ def b2g_sgemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> int:
 def b2g_sgemm_ex(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> int:
     return _load().b2g_sgemm_ex(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
                                 stream)
+
+
+def b2g_sgemm_colmajor(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                       stream=0) -> int:
+    return _load().b2g_sgemm_colmajor(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C,
+                                      ldc, stream)
 
 
 def b2g_sgemm_with_plan(plan, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
@@ -349,6 +358,41 @@ def sgemm(A, B, C, alpha: float = 1.0, beta: float = 0.0, transA: bool = False,
         rc = b2g_sgemm_ex(int(transA), int(transB), *args)
     else:
         rc = b2g_sgemm_with_plan(int(plan), int(transA), int(transB), *args)
+    if rc:
+        raise B2GError(rc)
+    return C
+
+
+def _check_colmajor(t, name):
+    import torch
+
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or t.dim() != 2:
+        raise TypeError(f"{name} must be a 2-D torch.float32 tensor")
+    if not t.is_cuda:
+        raise TypeError(f"{name} must be on a CUDA device")
+    if t.size(0) > 1 and t.stride(0) != 1:
+        raise ValueError(f"{name} must have unit row stride (column-major columns)")
+    return max(1, t.stride(1)) if t.size(1) > 1 else max(1, t.size(0))
+
+
+def sgemm_colmajor(A, B, C, alpha: float = 1.0, beta: float = 0.0, transA: bool = False,
+                   transB: bool = False, stream=None):
+    """C <- alpha * op(A) @ op(B) + beta * C for column-major tensors.
+
+    A, B, C are 2-D float32 CUDA tensors with unit row stride (for instance
+    ``X.t()`` of a contiguous tensor); their column stride is the leading
+    dimension.  op(A) is A.T when transA, likewise for B.  Runs
+    ``b2g_sgemm_colmajor``; returns C.  Raises B2GError on a library error.
+    """
+    lda, ldb = _check_colmajor(A, "A"), _check_colmajor(B, "B")
+    ldc = _check_colmajor(C, "C")
+    M, K = (A.size(1), A.size(0)) if transA else (A.size(0), A.size(1))
+    Kb, N = (B.size(1), B.size(0)) if transB else (B.size(0), B.size(1))
+    if Kb != K or tuple(C.shape) != (M, N):
+        raise ValueError(f"shape mismatch: op(A) {M}x{K}, op(B) {Kb}x{N}, C {tuple(C.shape)}")
+    rc = b2g_sgemm_colmajor(int(transA), int(transB), M, N, K, float(alpha), A.data_ptr(), lda,
+                            B.data_ptr(), ldb, float(beta), C.data_ptr(), ldc,
+                            _stream_handle(stream))
     if rc:
         raise B2GError(rc)
     return C

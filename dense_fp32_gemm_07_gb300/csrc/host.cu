@@ -884,6 +884,15 @@ int b2g_sgemm_ex(int transA, int transB, int M, int N, int K, float alpha, const
              stream);
 }
 
+// Column-major C = op(A) op(B) is row-major C^T = op(B)^T op(A)^T on the same
+// memory: swap the operands, their op() flags and M with N.
+int b2g_sgemm_colmajor(int transA, int transB, int M, int N, int K, float alpha, const float* A,
+                       int lda, const float* B, int ldb, float beta, float* C, int ldc,
+                       void* stream) {
+  return run(Call{transB != 0, transA != 0, N, M, K, alpha, beta, B, ldb, A, lda, C, ldc}, -1,
+             stream);
+}
+
 int b2g_sgemm_with_plan(int plan, int transA, int transB, int M, int N, int K, float alpha,
                         const float* A, int lda, const float* B, int ldb, float beta, float* C,
                         int ldc, void* stream) {

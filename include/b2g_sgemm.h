@@ -89,6 +89,27 @@ int b2g_sgemm_ex(int transA, int transB, int M, int N, int K, float alpha, const
                  const float* B, int ldb, float beta, float* C, int ldc, void* stream);
 
 /*
+ * The same product for COLUMN-major operands, with BLAS's argument
+ * conventions: C is M x N column-major (element (i, j) at C[i + j*ldc],
+ * ldc >= max(1, M)); transA == 0: A is M x K column-major, lda >= max(1, M);
+ * transA != 0: A is stored K x M column-major (lda >= max(1, K)) and
+ * op(A) = A^T; likewise B (K x N, ldb >= max(1, K); or stored N x K,
+ * ldb >= max(1, N), when transB != 0).
+ *
+ * A column-major matrix is the row-major transpose of the same memory, and
+ * C = op(A) op(B) holds exactly when C^T = op(B)^T op(A)^T ("GEMM 优化之路",
+ * 完整代码: the identity by which the page drives column-major cuBLAS with
+ * row-major data).  So this call is b2g_sgemm_ex(transB, transA, N, M, K,
+ * alpha, B, ldb, A, lda, beta, C, ldc, stream): the same plans, kernels,
+ * workspace behaviour and error bound, with the roles of the two operands
+ * swapped.  Error codes as b2g_sgemm_ex (a leading dimension below the bounds
+ * above is B2G_ERR_INVALID_LD).
+ */
+int b2g_sgemm_colmajor(int transA, int transB, int M, int N, int K, float alpha, const float* A,
+                       int lda, const float* B, int ldb, float beta, float* C, int ldc,
+                       void* stream);
+
+/*
  * `batch` independent products C_b = alpha * op(A_b) * op(B_b) + beta * C_b,
  * b = 0 .. batch-1, with A_b = A + b*strideA, B_b = B + b*strideB and
  * C_b = C + b*strideC (strides in elements, >= 0; C_b must not overlap each
