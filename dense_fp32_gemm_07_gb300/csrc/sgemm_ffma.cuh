@@ -63,18 +63,40 @@ struct FfmaCfg {
   static_assert(BM <= 256 && BN <= 256, "bulk-tensor box dimensions are at most 256");
   static_assert(FEED == kFeedCpAsync ? PWARPS >= 1 : PWARPS == 1, "producer warps");
   static_assert(FEED == kFeedTMA || ALAY == kAKMajor, "4-byte feed writes the transposed layout");
+  // The packed order (5) pairs accumulators in 64-bit registers and needs a
+  // 128-register cap to keep three 160-thread CTAs per SM; its 32-k stage runs
+  // fully unrolled.  The scalar orders unroll at most 16 k (unrolled 32 times
+  // the scalar loop was measured 13% slower).
+  static constexpr int kMinBlocks = ORD == 5 ? 3 : 1;
+  static constexpr int kUnroll = ORD == 5 ? 32 : 16;
 };
 
-// One k step of the register outer product, acc[i][j] += a[i] * b[j], as FP32
-// FFMAs.  ORD picks the issue order (0: row by row, 1: column by column,
-// 2: rows with alternating column direction, 3: 2 x 2 blocks walked as a
-// snake, 4: columns with alternating row direction); every order performs the
-// same FFMAs on the same accumulators, so results are identical, but the order
-// changes which operand consecutive FFMAs share.
+// One k step of the register outer product, acc[i][j] += a[i] * b[j].
+// ORD picks the issue order of the scalar FP32 FMAs (0: row by row, 1: column
+// by column, 2: rows with alternating column direction, 3: 2 x 2 blocks walked
+// as a snake, 4: columns with alternating row direction), or 5: packed FMAs
+// (sm_100's two-lane FP32 FMA, each lane rounded as fmaf), one per pair of
+// columns j, j+1 and row i, walked pair of columns by pair of columns so that
+// consecutive instructions share the B pair.  A packed FMA still occupies the
+// FP32 pipe for both lanes but takes one issue slot instead of two, which
+// leaves the slots for the fragment loads and the loop.  Every order performs
+// the same fused multiply-adds on the same accumulators in the same k order,
+// so results are identical.
 template <int ORD, int TN>
 __device__ __forceinline__ void outer_product(float (&acc)[8][TN], const float (&a)[8],
                                               const float (&b)[TN]) {
-  if constexpr (ORD == 1) {
+  if constexpr (ORD == 5) {
+#pragma unroll
+    for (int j2 = 0; j2 < TN / 2; ++j2) {
+      const float2 bj = make_float2(b[2 * j2], b[2 * j2 + 1]);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float2 r = __ffma2_rn(make_float2(a[i], a[i]), bj,
+                                    make_float2(acc[i][2 * j2], acc[i][2 * j2 + 1]));
+        acc[i][2 * j2] = r.x, acc[i][2 * j2 + 1] = r.y;
+      }
+    }
+  } else if constexpr (ORD == 1) {
 #pragma unroll
     for (int j = 0; j < TN; ++j)
 #pragma unroll
@@ -160,7 +182,9 @@ __device__ __forceinline__ int total_units(const SgemmParams& p) {
 
 template <int BM, int BN, int BK, int WM, int WN, int TN, int STAGES, int ALAY, int FEED,
           int PWARPS, int ORD>
-__global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
+__global__ void __launch_bounds__((WM * WN + PWARPS) * 32,
+                                  (FfmaCfg<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS,
+                                           ORD>::kMinBlocks))
     sgemm_ffma_kernel(const __grid_constant__ SgemmParams p,
                       const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB) {
@@ -391,10 +415,9 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32, 1)
           }
         }
       } else {
-        // at most 16 k unrolled: a 32-k stage (half the barrier round trips
-        // per k of a 16-k stage) runs its loop body twice; unrolled all 32
-        // times the loop was measured 13% slower
-#pragma unroll 16
+        // a 32-k stage (half the barrier round trips per k of a 16-k stage)
+        // runs its scalar loop body twice, its packed loop body once
+#pragma unroll Cfg::kUnroll
         for (int k = 0; k < BK; ++k) {
           const float4 a0 = *reinterpret_cast<const float4*>(As + k * Cfg::kARow);
           const float4 a1 = *reinterpret_cast<const float4*>(As + k * Cfg::kARow + 16);
