@@ -141,11 +141,17 @@ int b2g_sgemm_ws(int transA, int transB, int M, int N, int K, float alpha, const
  * b2g_sgemm on HOST operands: A, B and C are host pointers (same row-major
  * layout and leading-dimension rules as b2g_sgemm; page-locked memory from
  * cudaHostAlloc / cudaHostRegister gives full copy speed, pageable memory
- * works more slowly).  The library copies B to the device, then A and C in
- * row panels of about 1024 rows on its own copy stream while `stream`
- * multiplies the panels that have arrived, and copies each finished panel of
- * C back on a second copy stream; every step is ordered after earlier work on
- * `stream`, and the call's last copy is joined back into `stream`.  C holds
+ * works more slowly).  The copies overlap the multiplication: for K >= 2048
+ * the library copies A's columns and B's rows in three growing K chunks
+ * (K/8, 3K/8, K/2) and then C on its own copy stream, while `stream`
+ * multiplies each chunk into a device accumulator as soon as it has arrived;
+ * the last chunk runs in row panels of about 1024 rows, each finished panel
+ * (plus beta * C) going back to the host on a second copy stream while the
+ * next one multiplies.  For K < 2048 it copies B, then A and C in row panels,
+ * and multiplies each panel as it arrives.  Every step is ordered after
+ * earlier work on `stream`, and the call's last copy is joined back into
+ * `stream`.  Sums split over K chunks are rounded once per chunk, within the
+ * same error bound.  C holds
  * the result once `stream` has completed the call's work (for instance after
  * cudaStreamSynchronize(stream)); until then the host buffers must stay valid
  * and unmodified.  Device staging (A, B and C with rows padded to a multiple

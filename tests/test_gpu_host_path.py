@@ -92,3 +92,18 @@ def test_square4096_sampled(tb):
     got = hC.numpy()[rows, cols]
     ref, bound, _ = oracle.sgemm_entries(A, B, C, w.alpha, w.beta, rows, cols)
     check(got, ref, bound, "square4096 host")
+
+
+@pytest.mark.parametrize("shape,beta", [((1100, 300, 2100), 0.5), ((2100, 300, 2052), -1.0),
+                                        ((600, 1030, 2050), 0.0)])
+def test_k_chunked_schedule(tb, shape, beta):
+    """K >= 2048: three growing K chunks (K/8, 3K/8, K/2 rounded down to 16),
+    the last in row panels; ragged K (K % 4 != 0 included), two panels, and
+    beta = 0 (C not copied in).  Every element against the oracle."""
+    torch, b2g = tb
+    M, N, K = shape
+    A, B, C = _inputs(M * 3 + K, M, N, K)
+    ref, bound, _ = oracle.sgemm(A, B, C, 0.75, beta)
+    hA, hB, hC = (torch.from_numpy(x).pin_memory() for x in (A, B, C))
+    b2g.sgemm_host(hA, hB, hC, 0.75, beta)
+    check(hC.numpy(), ref, bound, f"host chunked {shape} beta={beta}")
