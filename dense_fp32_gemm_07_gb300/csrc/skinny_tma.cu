@@ -90,6 +90,11 @@ __global__ void __launch_bounds__(SkinnyTmaCfg<MR>::kThreads)
   const float alpha = p.alpha, beta = p.beta;
   float* Cb = p.C + (long long)bz * p.strideC;
 
+  // Launched as a programmatic dependent: the next kernel on the stream may
+  // start as soon as every CTA of this one runs (its CTAs then set up while
+  // this grid finishes), and this grid touches global memory only after the
+  // previous grid on the stream has completed and its writes are visible.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStStages; ++i) {
       mbar_init(full0 + 8 * i, 1);
@@ -99,13 +104,16 @@ __global__ void __launch_bounds__(SkinnyTmaCfg<MR>::kThreads)
     fence_proxy_async_smem();
     *failed = 0;
   }
+  if (warp == Cfg::kConsumerWarps && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
   __syncthreads();
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   if (warp == Cfg::kConsumerWarps) {
     // ---------------------------------------------------------- producer
     if (lane == 0) {
-      prefetch_tmap(&tmA);
-      prefetch_tmap(&tmB);
       int st = 0, issued = 0;
       uint32_t ph = 0;
       for (int c = 0; c < nst; ++c) {
@@ -307,18 +315,20 @@ cudaError_t launch_skinny_tma(const SgemmParams& p, const CUtensorMap* tmA, cons
   SgemmParams pc = p;
   CUtensorMap a = *tmA, b = *tmB;
   void* args[] = {&pc, &a, &b};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = (unsigned)p.splits;  // the k slabs of a column slab
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 1;
+  attr[1].val.clusterDim.y = (unsigned)p.splits;  // the k slabs of a column slab
+  attr[1].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)((p.N + kStBN - 1) / kStBN), (unsigned)p.splits, (unsigned)p.batch);
   cfg.blockDim = dim3(SkinnyTmaCfg<MR>::kThreads);
   cfg.dynamicSmemBytes = SkinnyTmaCfg<MR>::kSmemBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = p.splits > 1 ? 1 : 0;
+  cfg.numAttrs = p.splits > 1 ? 2 : 1;
   return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(&skinny_tma_kernel<MR>), args);
 }
 
