@@ -224,12 +224,13 @@ def sgemm_3xtf32(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None,
                  variant: Optional[int] = None):
     """C <- alpha * A @ B + beta * C on the tensor cores (3xTF32 split); see
     b2g_sgemm_3xtf32 in include/b2g_sgemm.h.  variant: None for the default
-    kernel, 0 (one CTA per tile) or 1 (a CTA pair per tile)."""
-    lda, ldb, ldc = _check(A, "A"), _check(B, "B"), _check(C, "C")
-    M, K = A.shape
-    Kb, N = B.shape
-    if Kb != K or tuple(C.shape) != (M, N):
-        raise ValueError("shape mismatch")
+    kernel, 0 (one CTA per 128 x 128 tile), 1 (a CTA pair per 256 x 128 tile)
+    or 2 (a CTA pair per 256 x 256 tile)."""
+    M, K, lda = _check(A, "A")
+    Kb, N, ldb = _check(B, "B")
+    Mc, Nc, ldc = _check(C, "C")
+    if Kb != K or Mc != M or Nc != N:
+        raise ValueError(f"shape mismatch: A {M}x{K}, B {Kb}x{N}, C {Mc}x{Nc}")
     args = (M, N, K, float(alpha), A.data_ptr(), lda, B.data_ptr(), ldb, float(beta),
             C.data_ptr(), ldc, _stream_handle(stream))
     rc = b2g_sgemm_3xtf32(*args) if variant is None else b2g_sgemm_3xtf32_variant(variant, *args)
@@ -318,24 +319,37 @@ def b2g_version() -> str:
 
 # --- tensor-level convenience ----------------------------------------------------
 
-def _stream_handle(stream) -> int:
-    import torch
+_torch = None
 
+
+def _t():
+    """torch, imported on first use (the C-ABI wrappers above need no torch)."""
+    global _torch
+    if _torch is None:
+        import torch
+
+        _torch = torch
+    return _torch
+
+
+def _stream_handle(stream) -> int:
     if stream is None:
-        stream = torch.cuda.current_stream()
+        return _t().cuda.current_stream().cuda_stream
     return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
 
 
 def _check(t, name):
-    import torch
-
-    if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or t.dim() != 2:
+    """(rows, cols, leading dimension) of a row-major float32 CUDA matrix."""
+    torch = _t()
+    if not isinstance(t, torch.Tensor) or t.dtype is not torch.float32 or t.dim() != 2:
         raise TypeError(f"{name} must be a 2-D torch.float32 tensor")
     if not t.is_cuda:
         raise TypeError(f"{name} must be on a CUDA device")
-    if t.size(1) > 1 and t.stride(1) != 1:
+    r, c = t.shape
+    s0, s1 = t.stride()
+    if c > 1 and s1 != 1:
         raise ValueError(f"{name} must have unit column stride (row-major rows)")
-    return max(1, t.stride(0)) if t.size(0) > 1 else max(1, t.size(1))
+    return r, c, (max(1, s0) if r > 1 else max(1, c))
 
 
 def sgemm(A, B, C, alpha: float = 1.0, beta: float = 0.0, transA: bool = False,
@@ -346,18 +360,20 @@ def sgemm(A, B, C, alpha: float = 1.0, beta: float = 0.0, transA: bool = False,
     stride is the leading dimension.  op(A) is A.T when transA (A stored K x M),
     likewise for B.  Returns C.  Raises B2GError on a library error code.
     """
-    lda, ldb, ldc = _check(A, "A"), _check(B, "B"), _check(C, "C")
-    M, K = (A.size(1), A.size(0)) if transA else (A.size(0), A.size(1))
-    Kb, N = (B.size(1), B.size(0)) if transB else (B.size(0), B.size(1))
-    if Kb != K or tuple(C.shape) != (M, N):
-        raise ValueError(f"shape mismatch: op(A) {M}x{K}, op(B) {Kb}x{N}, C {tuple(C.shape)}")
-    s = _stream_handle(stream)
+    ra, ca, lda = _check(A, "A")
+    rb, cb, ldb = _check(B, "B")
+    rc_, cc, ldc = _check(C, "C")
+    M, K = (ca, ra) if transA else (ra, ca)
+    Kb, N = (cb, rb) if transB else (rb, cb)
+    if Kb != K or rc_ != M or cc != N:
+        raise ValueError(f"shape mismatch: op(A) {M}x{K}, op(B) {Kb}x{N}, C {rc_}x{cc}")
+    lib = _lib or _load()
     args = (M, N, K, float(alpha), A.data_ptr(), lda, B.data_ptr(), ldb, float(beta),
-            C.data_ptr(), ldc, s)
+            C.data_ptr(), ldc, _stream_handle(stream))
     if plan is None:
-        rc = b2g_sgemm_ex(int(transA), int(transB), *args)
+        rc = lib.b2g_sgemm_ex(int(transA), int(transB), *args)
     else:
-        rc = b2g_sgemm_with_plan(int(plan), int(transA), int(transB), *args)
+        rc = lib.b2g_sgemm_with_plan(int(plan), int(transA), int(transB), *args)
     if rc:
         raise B2GError(rc)
     return C

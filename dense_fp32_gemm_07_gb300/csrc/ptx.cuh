@@ -1,9 +1,11 @@
 // ptx.cuh -- inline-PTX building blocks for the sm_103a SGEMM kernels:
 // mbarrier phases, bulk-tensor (TMA) loads, 4-byte cp.async with zero fill,
-// and bounded waits that report a timeout instead of spinning forever.
+// bounded waits that report a timeout instead of spinning forever, and
+// programmatic dependent launch.
 #pragma once
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_runtime.h>
 
 namespace b2g {
 
@@ -151,6 +153,34 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
 
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// Programmatic dependent launch.  A grid launched with launch_pdl may start
+// while the previous grid on its stream is still draining, as soon as every
+// CTA of that grid has executed pdl_launch_dependents (or exited); it must
+// execute pdl_wait before its first global-memory access, which returns once
+// the previous grid has completed and its writes are visible.  Without the
+// launch attribute pdl_wait returns at once.  The next grid can only start
+// after every CTA of this one has started, so a waiting grid never holds SM
+// slots that this grid still needs.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+inline cudaError_t launch_pdl(const void* kern, dim3 grid, dim3 block, void** args, size_t smem,
+                              cudaStream_t stream) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, kern, args);
 }
 
 }  // namespace b2g

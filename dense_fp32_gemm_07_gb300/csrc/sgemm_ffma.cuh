@@ -200,6 +200,7 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32,
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  pdl_launch_dependents();  // the next grid may set up while this one runs
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full0 + 8 * s, FEED == kFeedCpAsync ? Cfg::kProducers : 1);
@@ -209,6 +210,7 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32,
     fence_proxy_async_smem();
   }
   __syncthreads();
+  pdl_wait();  // global memory only once the previous grid has completed
 
   const int units = total_units(p);
 
@@ -529,8 +531,8 @@ cudaError_t launch_ffma(const SgemmParams& p, const CUtensorMap* tmA, const CUte
   SgemmParams pc = p;
   CUtensorMap a = tmA ? *tmA : none, b = tmB ? *tmB : none;
   void* args[] = {&pc, &a, &b};
-  return cudaLaunchKernel(reinterpret_cast<const void*>(kern), dim3(grid), dim3(Cfg::kThreads),
-                          args, Cfg::kSmemBytes, stream);
+  return launch_pdl(reinterpret_cast<const void*>(kern), dim3(grid), dim3(Cfg::kThreads), args,
+                    Cfg::kSmemBytes, stream);
 }
 
 #define B2G_FFMA_PLAN(NAME, BM, BN, BK, WM, WN, TN, ST, ALAY, FEED, PW, ORD)                      \

@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(SkinnyTmaCfg<MR>::kThreads)
   // start as soon as every CTA of this one runs (its CTAs then set up while
   // this grid finishes), and this grid touches global memory only after the
   // previous grid on the stream has completed and its writes are visible.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStStages; ++i) {
       mbar_init(full0 + 8 * i, 1);
@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(SkinnyTmaCfg<MR>::kThreads)
     prefetch_tmap(&tmB);
   }
   __syncthreads();
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  pdl_wait();
 
   if (warp == Cfg::kConsumerWarps) {
     // ---------------------------------------------------------- producer

@@ -19,6 +19,8 @@ namespace b2g {
 // threads stride over the tile's BM x BN / 4 float4 positions.
 __global__ void __launch_bounds__(256) tail_reduce_kernel(const __grid_constant__ SgemmParams p,
                                                           int BM, int BN) {
+  pdl_launch_dependents();
+  pdl_wait();  // the partial sums are the previous grid's output
   int b, tm, tn;
   tile_coords(p, p.tail_first + (int)blockIdx.x, b, tm, tn);
   const int S = p.tail_splits;
@@ -72,8 +74,8 @@ cudaError_t launch_tail_reduce(const SgemmParams& p, int BM, int BN, cudaStream_
   const unsigned gy = (unsigned)((BM * BN / 4 + 511) / 512);
   SgemmParams pc = p;
   void* args[] = {&pc, &BM, &BN};
-  return cudaLaunchKernel(reinterpret_cast<const void*>(&tail_reduce_kernel),
-                          dim3((unsigned)n, gy), dim3(256), args, 0, stream);
+  return launch_pdl(reinterpret_cast<const void*>(&tail_reduce_kernel), dim3((unsigned)n, gy),
+                    dim3(256), args, 0, stream);
 }
 
 }  // namespace b2g

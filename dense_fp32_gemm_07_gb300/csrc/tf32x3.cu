@@ -57,6 +57,8 @@ __device__ __forceinline__ void tf32_split(float x, float& hi, float& lo) {
 __global__ void __launch_bounds__(256) split_a_kernel(const float* __restrict__ A, int M, int K,
                                                       long long lda, float* __restrict__ Ahi,
                                                       float* __restrict__ Alo) {
+  pdl_launch_dependents();
+  pdl_wait();
   const long long kv = K / 4;
   const long long total = (long long)M * kv;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
@@ -82,6 +84,8 @@ __global__ void __launch_bounds__(256) split_bt_kernel(const float* __restrict__
                                                        long long ldb, float* __restrict__ Bhi,
                                                        float* __restrict__ Blo) {
   __shared__ __align__(16) float tile[64][68];  // [n][k], rows padded to keep 16-byte reads aligned
+  pdl_launch_dependents();
+  pdl_wait();
   const int k0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   // load: warp w takes rows k = k0 + w + 8j; lanes take 32 consecutive n (twice)
@@ -153,6 +157,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       reinterpret_cast<uint32_t*>(gbase + kTcStages * kTcStageBytes + kTcNumBars * 8);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < kTcStages; ++s) {
       mbar_init(full(s), 1);
@@ -173,6 +178,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
+  pdl_wait();  // operands and C only once the previous grid has completed
   const uint32_t tmem = *tmem_slot;
   const int total_tiles = p.tiles_m * p.tiles_n;
 
@@ -397,6 +403,7 @@ __global__ void __launch_bounds__(kTpThreads, 1)
   const uint32_t rank = cluster_ctarank() & 1u;
   const bool even = rank == 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < kTpStages; ++s) {
       mbar_init(full(s), 1);
@@ -418,6 +425,7 @@ __global__ void __launch_bounds__(kTpThreads, 1)
   tc_fence_before_sync();
   cluster_sync();  // barriers initialised and tensor memory allocated in both CTAs
   tc_fence_after_sync();
+  pdl_wait();  // operands and C only once the previous grid has completed
   // The even CTA's base address names the pair's accumulator columns in both.
   const uint32_t tmem =
       even ? *tmem_slot : ld_shared_cluster_u32(mapa_shared(smem_addr(tmem_slot), 0));
@@ -602,16 +610,16 @@ cudaError_t launch_split_a(const float* A, int M, int K, long long lda, float* A
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   void* args[] = {(void*)&A, (void*)&M, (void*)&K, (void*)&lda, (void*)&Ahi, (void*)&Alo};
-  return cudaLaunchKernel(reinterpret_cast<const void*>(&split_a_kernel), dim3((unsigned)blocks),
-                          dim3(256), args, 0, stream);
+  return launch_pdl(reinterpret_cast<const void*>(&split_a_kernel), dim3((unsigned)blocks),
+                    dim3(256), args, 0, stream);
 }
 
 cudaError_t launch_split_bt(const float* B, int K, int N, long long ldb, float* Bhi, float* Blo,
                             cudaStream_t stream) {
   const dim3 grid((unsigned)((N + 63) / 64), (unsigned)((K + 63) / 64));
   void* args[] = {(void*)&B, (void*)&K, (void*)&N, (void*)&ldb, (void*)&Bhi, (void*)&Blo};
-  return cudaLaunchKernel(reinterpret_cast<const void*>(&split_bt_kernel), grid, dim3(256), args,
-                          0, stream);
+  return launch_pdl(reinterpret_cast<const void*>(&split_bt_kernel), grid, dim3(256), args, 0,
+                    stream);
 }
 
 cudaError_t launch_tf32x3(const Tf32x3Params& p, const CUtensorMap* maps, int num_sms,
@@ -632,8 +640,8 @@ cudaError_t launch_tf32x3(const Tf32x3Params& p, const CUtensorMap* maps, int nu
   Tf32x3Params pc = p;
   CUtensorMap m0 = maps[0], m1 = maps[1], m2 = maps[2], m3 = maps[3];
   void* args[] = {&pc, &m0, &m1, &m2, &m3};
-  return cudaLaunchKernel(reinterpret_cast<const void*>(&sgemm_tf32x3_kernel), dim3(grid),
-                          dim3(kTcThreads), args, kTcSmemBytes, stream);
+  return launch_pdl(reinterpret_cast<const void*>(&sgemm_tf32x3_kernel), dim3(grid),
+                    dim3(kTcThreads), args, kTcSmemBytes, stream);
 }
 
 template <int PN>
@@ -647,11 +655,13 @@ cudaError_t launch_pair(const Tf32x3Params& p, const CUtensorMap* maps, int num_
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kTpThreads);
   cfg.dynamicSmemBytes = Cfg::kSmemBytes;
@@ -672,6 +682,7 @@ cudaError_t launch_pair(const Tf32x3Params& p, const CUtensorMap* maps, int num_
   }
   const long long tiles = (long long)p.tiles_m * p.tiles_n;
   cfg.gridDim = dim3((unsigned)(2 * (tiles < pairs ? tiles : pairs)));
+  cfg.numAttrs = 2;  // the occupancy query above used the cluster shape alone
   Tf32x3Params pc = p;
   CUtensorMap m0 = maps[0], m1 = maps[1], m2 = maps[2], m3 = maps[3];
   void* args[] = {&pc, &m0, &m1, &m2, &m3};
@@ -716,6 +727,8 @@ int tf32x3_pair_capacity(int pn, int num_sms) {
 // stride over the tile's 256 x pn / 4 float4 positions; slices added in order.
 __global__ void __launch_bounds__(256) tc_tail_reduce_kernel(const __grid_constant__ Tf32x3Params p,
                                                              int pn) {
+  pdl_launch_dependents();
+  pdl_wait();  // the partial sums are the previous grid's output
   int tm, tn;
   tc_tile_coords(p, p.tail_first + (int)blockIdx.x, tm, tn);
   const int S = p.tail_splits;
@@ -763,8 +776,8 @@ cudaError_t launch_tf32x3_tail_reduce(const Tf32x3Params& p, int pn, cudaStream_
   const unsigned gy = (unsigned)((2 * kTcBM * pn / 4 + 511) / 512);  // 2 float4 per thread
   Tf32x3Params pc = p;
   void* args[] = {&pc, &pn};
-  return cudaLaunchKernel(reinterpret_cast<const void*>(&tc_tail_reduce_kernel),
-                          dim3((unsigned)n, gy), dim3(256), args, 0, stream);
+  return launch_pdl(reinterpret_cast<const void*>(&tc_tail_reduce_kernel), dim3((unsigned)n, gy),
+                    dim3(256), args, 0, stream);
 }
 
 }  // namespace b2g

@@ -11,6 +11,7 @@
 // are padding and receive zeros.
 #include <cuda_runtime.h>
 
+#include "ptx.cuh"
 #include "transpose.h"
 
 namespace b2g {
@@ -23,6 +24,8 @@ __global__ void __launch_bounds__(256) transpose_a_kernel(const float* __restric
                                                           long long ldat, long long strideA,
                                                           long long strideAt) {
   __shared__ __align__(16) float tile[kTT][kTT];  // [k][m]
+  pdl_launch_dependents();
+  pdl_wait();
   A += (long long)blockIdx.z * strideA;  // problem blockIdx.z of a batch
   At += (long long)blockIdx.z * strideAt;
   const int m0 = blockIdx.x * kTT, k0 = blockIdx.y * kTT;
@@ -68,8 +71,8 @@ cudaError_t launch_transpose_a(const float* A, int M, int K, long long lda, floa
                     (unsigned)nb);
     void* args[] = {(void*)&Ab, (void*)&M, (void*)&K, (void*)&lda, (void*)&Atb, (void*)&ldat,
                     (void*)&strideA, (void*)&strideAt};
-    const cudaError_t e = cudaLaunchKernel(reinterpret_cast<const void*>(&transpose_a_kernel),
-                                           grid, dim3(256), args, 0, stream);
+    const cudaError_t e = launch_pdl(reinterpret_cast<const void*>(&transpose_a_kernel), grid,
+                                     dim3(256), args, 0, stream);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -90,6 +93,8 @@ __global__ void __launch_bounds__(256) pack_kernel(const float* __restrict__ in,
                                                    float* __restrict__ out, long long ldo,
                                                    long long stride_in, long long stride_out) {
   __shared__ float tile[32][33];
+  pdl_launch_dependents();
+  pdl_wait();
   in += (long long)blockIdx.z * stride_in;  // problem blockIdx.z of a batch
   out += (long long)blockIdx.z * stride_out;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
@@ -126,8 +131,8 @@ cudaError_t launch_pack(const float* in, long long ld, int trans, int R, int Cc,
     const dim3 grid((unsigned)((Cc + 31) / 32), (unsigned)((R + 31) / 32), (unsigned)nb);
     void* args[] = {(void*)&ib, (void*)&ld, (void*)&trans, (void*)&R, (void*)&Cc, (void*)&ob,
                     (void*)&ldo, (void*)&stride_in, (void*)&stride_out};
-    const cudaError_t e = cudaLaunchKernel(reinterpret_cast<const void*>(&pack_kernel), grid,
-                                           dim3(256), args, 0, stream);
+    const cudaError_t e =
+        launch_pdl(reinterpret_cast<const void*>(&pack_kernel), grid, dim3(256), args, 0, stream);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
