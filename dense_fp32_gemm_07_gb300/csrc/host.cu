@@ -15,6 +15,7 @@
 
 #include "../../include/b2g_sgemm.h"
 #include "plan_registry.h"
+#include "ptx.cuh"
 #include "sgemm_params.h"
 #include "tf32x3.h"
 #include "transpose.h"
@@ -30,6 +31,8 @@ __device__ unsigned int g_status_word;
 // zeros without reading C).  Used when the product term vanishes.
 __global__ void scale_c_kernel(int M, int N, float beta, float* __restrict__ C, long long ldc,
                                int batch, long long strideC) {
+  pdl_launch_dependents();
+  pdl_wait();
   const long long per = (long long)M * N;
   const long long total = per * batch;
   for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
@@ -45,6 +48,8 @@ __global__ void scale_c_kernel(int M, int N, float beta, float* __restrict__ C, 
 // multiples of 4 with 16-byte aligned bases: float4 throughout).
 __global__ void axpby_rows_kernel(int M, int N4, float b, const float* __restrict__ X,
                                   long long ldx, float* __restrict__ Y, long long ldy) {
+  pdl_launch_dependents();
+  pdl_wait();
   const long long total = (long long)M * N4;
   for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
        idx += (long long)gridDim.x * blockDim.x) {
@@ -438,8 +443,8 @@ int launch_scale(const Call& c, const DeviceState& d, cudaStream_t st) {
   long long ldc = c.ldc, strideC = c.strideC;
   int batch = c.batch;
   void* args[] = {(void*)&c.M, (void*)&c.N, (void*)&c.beta, (void*)&c.C, &ldc, &batch, &strideC};
-  cudaError_t e = cudaLaunchKernel(reinterpret_cast<const void*>(&scale_c_kernel),
-                                   dim3((unsigned)blocks), dim3(256), args, 0, st);
+  cudaError_t e = launch_pdl(reinterpret_cast<const void*>(&scale_c_kernel),
+                             dim3((unsigned)blocks), dim3(256), args, 0, st);
   return e == cudaSuccess ? 0 : B2G_ERR_LAUNCH;
 }
 
@@ -751,8 +756,8 @@ int run_host(const Call& c, void* stream) {
       float beta = c.beta;
       long long ld = (long long)np;
       void* args[] = {&rn_i, (void*)&n4, &beta, (void*)&dCp, &ld, &dDp, &ld};
-      rc = ok(cudaLaunchKernel(reinterpret_cast<const void*>(&axpby_rows_kernel),
-                               dim3((unsigned)blocks), dim3(256), args, 0, st));
+      rc = ok(launch_pdl(reinterpret_cast<const void*>(&axpby_rows_kernel),
+                         dim3((unsigned)blocks), dim3(256), args, 0, st));
     }
     if (!rc) rc = ok(cudaEventRecord(h.gemm[i], st));
     if (!rc) rc = ok(cudaStreamWaitEvent(h.d2h, h.gemm[i], 0));

@@ -24,6 +24,7 @@
 #include <atomic>
 
 #include "plan_registry.h"
+#include "ptx.cuh"
 #include "sgemm_params.h"
 
 namespace b2g {
@@ -40,6 +41,7 @@ struct SkinnyCfg {
 template <int MR, int UNR>
 __global__ void __launch_bounds__(kSkThreads) skinny_kernel(const __grid_constant__ SgemmParams p) {
   extern __shared__ __align__(16) float sm[];
+  pdl_wait();  // after the previous grid on the stream (see launch_pdl)
   float* As = sm;                    // [kSkChunk][MR]
   float* red = sm + kSkChunk * MR;   // [3][MR][kSkCols]: warps 1..3 hand their sums to warp 0
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -97,7 +99,7 @@ __global__ void __launch_bounds__(kSkThreads) skinny_kernel(const __grid_constan
     __syncthreads();  // As is restaged by the next chunk
   }
   // the reduction kernel may launch now; it waits for this grid's results
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  pdl_launch_dependents();
 
   // warps 1..3 -> shared memory; warp 0 adds them in warp order
   if (warp > 0) {
@@ -149,7 +151,7 @@ __global__ void __launch_bounds__(kSkThreads) skinny_kernel(const __grid_constan
 // launched as a programmatic dependent of the split-K kernel it starts early
 // and waits here until that kernel has finished and its writes are visible.
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constant__ SgemmParams p) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  pdl_wait();  // the partial sums are the previous grid's output
   const long long nv = p.N / 4;
   const long long per = (long long)p.M * nv;
   const long long total = per * p.batch;
@@ -252,8 +254,8 @@ cudaError_t launch_skinny(const SgemmParams& p, const CUtensorMap*, const CUtens
                   (unsigned)p.batch);
   SgemmParams pc = p;
   void* args[] = {&pc};
-  e = cudaLaunchKernel(reinterpret_cast<const void*>(kern), grid, dim3(kSkThreads), args,
-                       SkinnyCfg<MR>::kSmemBytes, stream);
+  e = launch_pdl(reinterpret_cast<const void*>(kern), grid, dim3(kSkThreads), args,
+                 SkinnyCfg<MR>::kSmemBytes, stream);
   if (e == cudaSuccess && p.splits > 1) e = launch_splitk_reduce(p, stream, num_sms, true);
   return e;
 }
