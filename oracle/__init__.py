@@ -119,8 +119,10 @@ def sgemm_entries(A: np.ndarray, B: np.ndarray, C: Optional[np.ndarray], alpha: 
     A, B, C = _f32(A), _f32(B), _f32(C)
     if K is None:
         K = _shape(A, B, transA, transB)[2]
-    rows = np.ascontiguousarray(rows, dtype=np.int64)
-    cols = np.ascontiguousarray(cols, dtype=np.int64)
+    rows = np.ascontiguousarray(rows, dtype=np.int64).ravel()
+    cols = np.ascontiguousarray(cols, dtype=np.int64).ravel()
+    if rows.shape != cols.shape:
+        raise ValueError(f"rows and cols differ in length: {rows.size} vs {cols.size}")
     lda, ldb = A.strides[0] // 4, B.strides[0] // 4
     ldc = C.strides[0] // 4 if C is not None else 0
     ref = np.empty(rows.shape[0], dtype=np.float64)
