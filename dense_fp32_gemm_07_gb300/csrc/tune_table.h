@@ -4,7 +4,8 @@
 // and thread tile sizes depend on the GPU and on the matrix shape and that real
 // libraries keep a configuration per shape; this table is that configuration.
 // Rules are tried in order; the first whose class and bounds match names the
-// plan.  "fast" = both operands bulk-tensor eligible (16-byte aligned, lda, ldb
+// plan (for a strided batch whose products have at least 5e7 multiply-adds
+// each, M*N*K counts the whole call: times the batch count).  "fast" = both operands bulk-tensor eligible (16-byte aligned, lda, ldb
 // and K multiples of 4, no op() on B); "general" = anything else.
 #pragma once
 
