@@ -177,6 +177,24 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest value of x over all ranks; every rank receives it (a device
+    tensor for NCCL, a host tensor for gloo)."""
+    if world <= 1:
+        return float(x)
+    import torch
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job rate in units per second: the units every rank processed in a
+    step, over the slowest rank's time per step (ms)."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 def run_reference(args, w):
     """The CPU oracle on host cores: each step computes a bounded block of rows."""
     import numpy as np
@@ -292,12 +310,8 @@ def run_ours(args, w):
     ev1.record(stream)
     barrier()
     clocks = sampler.stop()
-    ms = ev0.elapsed_time(ev1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * w.flops() / (ms * 1e-3) / 1e12
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world, dev)
+    value = job_throughput(w.flops(), world, ms) / 1e12
     rc, launches_per_step = b2g.b2g_sgemm_launch_count(0, 0, w.M, w.N, w.K, w.alpha,
                                                        dA.data_ptr(), w.K, dB.data_ptr(), w.N,
                                                        dC.data_ptr(), w.N)
@@ -393,11 +407,7 @@ def run_ours(args, w):
         e2e_step()
     ev1.record(stream)
     barrier()
-    e2e_ms = ev0.elapsed_time(ev1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(ev0.elapsed_time(ev1) / e2e_steps, world, dev)
     # the result of the last step is still correct (spot check of one row)
     got = out[w.M // 2].numpy()
     if not np.isfinite(got).all():
@@ -428,7 +438,7 @@ def run_ours(args, w):
                          "peak_basis": "152 SMs x 128 FP32 FMA/clk x 2 x 2070 MHz (derived)",
                          "frac_at_sampled_clock": (achieved / fp32_peak_tflops(clocks["sm_mhz"])
                                                    if clocks else None)},
-            "e2e": {"value": world * w.flops() / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+            "e2e": {"value": job_throughput(w.flops(), world, e2e_ms) / 1e12, "unit": UNIT,
                     "h2d_bytes_per_step": int(hA.numel() + hB.numel() + hC.numel()) * 4,
                     "d2h_bytes_per_step": int(out.numel()) * 4},
             "gpu_launches": args.steps * launches_per_step,
