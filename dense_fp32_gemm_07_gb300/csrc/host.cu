@@ -545,11 +545,9 @@ int run(const Call& c, int forced_plan, void* stream, void* user_ws = nullptr,
     const long long sat = (long long)c.K * ldat, sbp = (long long)c.K * ldbp;
     float* At = ws;
     float* Bp = ws + (size_t)c.batch * sat;
-    e = launch_pack(c.A, c.lda, c.transA ? 0 : 1, c.K, c.M, At, ldat, st, c.batch, c.strideA,
-                    sat);
-    if (e == cudaSuccess)
-      e = launch_pack(c.B, c.ldb, c.transB ? 1 : 0, c.K, c.N, Bp, ldbp, st, c.batch, c.strideB,
-                      sbp);
+    e = launch_pack2(pack_job(c.A, c.lda, c.transA ? 0 : 1, c.K, c.M, At, ldat, c.strideA, sat),
+                     pack_job(c.B, c.ldb, c.transB ? 1 : 0, c.K, c.N, Bp, ldbp, c.strideB, sbp),
+                     st, c.batch);
     p.A = At, p.lda = ldat, p.transA = 1, p.strideA = sat;
     p.B = Bp, p.ldb = ldbp, p.transB = 0, p.strideB = sbp;
   }

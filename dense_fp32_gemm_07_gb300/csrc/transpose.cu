@@ -88,51 +88,70 @@ namespace b2g {
 //   trans != 0: out[r][c] = in[c * ld + r]
 // 32 x 32 tiles through shared memory (rows padded to 33: no bank conflicts),
 // coalesced on both sides in either direction.
-__global__ void __launch_bounds__(256) pack_kernel(const float* __restrict__ in, long long ld,
-                                                   int trans, int R, int Cc,
-                                                   float* __restrict__ out, long long ldo,
-                                                   long long stride_in, long long stride_out) {
-  __shared__ float tile[32][33];
-  pdl_launch_dependents();
-  pdl_wait();
-  in += (long long)blockIdx.z * stride_in;  // problem blockIdx.z of a batch
-  out += (long long)blockIdx.z * stride_out;
+__device__ __forceinline__ void pack_tile(const PackJob& j, int bx, int by, int bz,
+                                          float (&tile)[32][33]) {
+  const float* __restrict__ in = j.in + (long long)bz * j.stride_in;  // problem bz of a batch
+  float* __restrict__ out = j.out + (long long)bz * j.stride_out;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
-  const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
-  if (trans) {
+  const int r0 = by * 32, c0 = bx * 32;
+  if (j.trans) {
     // read in rows (c0 + i), columns r0 + tx: coalesced along r
 #pragma unroll
     for (int i = ty; i < 32; i += 8) {
       const int c = c0 + i, r = r0 + tx;
-      tile[i][tx] = (c < Cc && r < R) ? in[(long long)c * ld + r] : 0.f;
+      tile[i][tx] = (c < j.Cc && r < j.R) ? in[(long long)c * j.ld + r] : 0.f;
     }
     __syncthreads();
 #pragma unroll
     for (int i = ty; i < 32; i += 8) {
       const int r = r0 + i, c = c0 + tx;
-      if (r < R && c < Cc) out[(long long)r * ldo + c] = tile[tx][i];
+      if (r < j.R && c < j.Cc) out[(long long)r * j.ldo + c] = tile[tx][i];
     }
   } else {
 #pragma unroll
     for (int i = ty; i < 32; i += 8) {
       const int r = r0 + i, c = c0 + tx;
-      if (r < R && c < Cc) out[(long long)r * ldo + c] = in[(long long)r * ld + c];
+      if (r < j.R && c < j.Cc) out[(long long)r * j.ldo + c] = in[(long long)r * j.ld + c];
     }
   }
 }
 
-cudaError_t launch_pack(const float* in, long long ld, int trans, int R, int Cc, float* out,
-                        long long ldo, cudaStream_t stream, int batch, long long stride_in,
-                        long long stride_out) {
-  for (int b0 = 0; b0 < batch; b0 += 65535) {
+// Both operands in one launch: blocks 0 .. tiles(a)-1 pack job a, the rest
+// job b (a block's job is uniform across its threads, so the barrier in the
+// transposing branch is reached by all of them).
+__global__ void __launch_bounds__(256) pack2_kernel(const __grid_constant__ PackJob a,
+                                                    const __grid_constant__ PackJob b) {
+  __shared__ float tile[32][33];
+  pdl_launch_dependents();
+  pdl_wait();
+  const int ta = a.tiles_x * a.tiles_y;
+  const int t = (int)blockIdx.x;
+  if (t < ta)
+    pack_tile(a, t % a.tiles_x, t / a.tiles_x, (int)blockIdx.z, tile);
+  else
+    pack_tile(b, (t - ta) % b.tiles_x, (t - ta) / b.tiles_x, (int)blockIdx.z, tile);
+}
+
+PackJob pack_job(const float* in, long long ld, int trans, int R, int Cc, float* out,
+                 long long ldo, long long stride_in, long long stride_out) {
+  PackJob j{in, ld, trans, R, Cc, out, ldo, stride_in, stride_out, (Cc + 31) / 32,
+            (R + 31) / 32};
+  return j;
+}
+
+cudaError_t launch_pack2(const PackJob& a, const PackJob& b, cudaStream_t stream, int batch) {
+  const long long tiles = (long long)a.tiles_x * a.tiles_y + (long long)b.tiles_x * b.tiles_y;
+  if (tiles <= 0) return cudaSuccess;
+  if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
+  for (int b0 = 0; b0 < batch; b0 += 65535) {  // grid z is at most 65535
     const int nb = batch - b0 < 65535 ? batch - b0 : 65535;
-    const float* ib = in + (long long)b0 * stride_in;
-    float* ob = out + (long long)b0 * stride_out;
-    const dim3 grid((unsigned)((Cc + 31) / 32), (unsigned)((R + 31) / 32), (unsigned)nb);
-    void* args[] = {(void*)&ib, (void*)&ld, (void*)&trans, (void*)&R, (void*)&Cc, (void*)&ob,
-                    (void*)&ldo, (void*)&stride_in, (void*)&stride_out};
-    const cudaError_t e =
-        launch_pdl(reinterpret_cast<const void*>(&pack_kernel), grid, dim3(256), args, 0, stream);
+    PackJob ja = a, jb = b;
+    ja.in += (long long)b0 * a.stride_in, ja.out += (long long)b0 * a.stride_out;
+    jb.in += (long long)b0 * b.stride_in, jb.out += (long long)b0 * b.stride_out;
+    void* args[] = {&ja, &jb};
+    const cudaError_t e = launch_pdl(reinterpret_cast<const void*>(&pack2_kernel),
+                                     dim3((unsigned)tiles, 1, (unsigned)nb), dim3(256), args, 0,
+                                     stream);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

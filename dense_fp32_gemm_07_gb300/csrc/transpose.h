@@ -12,11 +12,22 @@ cudaError_t launch_transpose_a(const float* A, int M, int K, long long lda, floa
                                long long ldat, cudaStream_t stream, int batch = 1,
                                long long strideA = 0, long long strideAt = 0);
 
-// out (R x Cc, leading dimension ldo) = trans ? in^T : in, in read element by
-// element: any alignment and leading dimension ld.  Grid-limited to R and Cc
-// below 2^31 / 32 tiles.
-cudaError_t launch_pack(const float* in, long long ld, int trans, int R, int Cc, float* out,
-                        long long ldo, cudaStream_t stream, int batch = 1,
-                        long long stride_in = 0, long long stride_out = 0);
+// One packing job: out (R x Cc, leading dimension ldo) = trans ? in^T : in,
+// in read element by element (any alignment and leading dimension ld), in 32 x
+// 32 tiles; `batch` problems advance by stride_in and stride_out elements.
+struct PackJob {
+  const float* in;
+  long long ld;
+  int trans, R, Cc;
+  float* out;
+  long long ldo, stride_in, stride_out;
+  int tiles_x, tiles_y;  // 32 x 32 tiles along Cc and R
+};
+PackJob pack_job(const float* in, long long ld, int trans, int R, int Cc, float* out,
+                 long long ldo, long long stride_in = 0, long long stride_out = 0);
+
+// Both jobs in one launch (the packed plans' A^T and B); at most 2^31 - 1
+// tiles in all.
+cudaError_t launch_pack2(const PackJob& a, const PackJob& b, cudaStream_t stream, int batch = 1);
 
 }  // namespace b2g
