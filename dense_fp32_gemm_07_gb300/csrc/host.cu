@@ -975,7 +975,7 @@ int b2g_sgemm_launch_count(int transA, int transB, int M, int N, int K, float al
   }
   const Plan* pl = plan_at(select_plan(c));
   if (!pl) return B2G_ERR_INVALID_PLAN;
-  int n = 1 + (pl->pretranspose == 1 ? 1 : pl->pretranspose == 2 ? 2 : 0);
+  int n = 1 + (pl->pretranspose ? 1 : 0);  // a transpose, or one launch packing both operands
   if (pl->feed == kFeedSkinny) {
     int kc = 0;
     if (skinny_splits(*pl, c, &kc) > 1) n += 1;  // the split-K reduction

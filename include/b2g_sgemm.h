@@ -181,7 +181,7 @@ int b2g_sgemm_workspace_size(int transA, int transB, int M, int N, int K, float 
  * Number of kernel launches that one b2g_sgemm_ex call with these arguments
  * makes when the workspace can be had, stored in *launches: 0 when M or N is
  * 0, 1 when only C is scaled, else the GEMM kernel plus the plan's prepasses
- * (1 transpose, or 2 packing launches) plus 1 when a split-K or split-tail
+ * (1 transpose, or 1 launch packing both operands) plus 1 when a split-K or split-tail
  * reduction follows.  Depends on the current device like the split itself.
  * Returns 0, a B2G_ERR_* code for invalid arguments, or B2G_ERR_NULL when
  * launches is NULL.  Launches nothing.
