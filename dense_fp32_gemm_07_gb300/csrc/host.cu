@@ -182,6 +182,7 @@ const PlanGroup kGroups[] = {
     {kPlansTMA, &kNumPlansTMA},         {kPlansT, &kNumPlansT},
     {kPlansT64x128, &kNumPlansT64x128}, {kPlansT128x64, &kNumPlansT128x64},
     {kPlansT128x64k32, &kNumPlansT128x64k32},
+    {kPlansT64x128k32, &kNumPlansT64x128k32},
     {kPlansT128x128, &kNumPlansT128x128}, {kPlansGeneral, &kNumPlansGeneral},
     {kPlansSkinny, &kNumPlansSkinny},     {kPlansSkinnyTma, &kNumPlansSkinnyTma},
 };
@@ -266,6 +267,17 @@ bool plan_accepts(const Plan& pl, const Call& c) {
 
 // The tune table's plan; `fallback` receives the plan to use when the chosen
 // one needs a workspace that cannot be had (the same plan when it needs none).
+int tail_split(const Plan& pl, const Call& c, int* first);
+double tile_shape_score(const Plan& pl, const Call& c);
+
+// The packed 128 x 64 plans and their 64 x 128 twins run at the same rate on
+// large products; which one a call gets depends on padding and wave fill.
+const char* const kTileTwins[][2] = {
+    {"pre_128x64x32_s3_o5", "pre_64x128x32_s3_o5"},
+    {"tmaT_128x64x32_s3_o5", "tmaT_64x128x32_s3_o5"},
+    {"pack_128x64x32_s3_o5", "pack_64x128x32_s3_o5"},
+};
+
 int select_plan(const Call& c, int* fallback = nullptr) {
   const int cls = operand_class(c);
   // The work of the whole call: a batch of products amortises a
@@ -277,11 +289,18 @@ int select_plan(const Call& c, int* fallback = nullptr) {
   for (const TuneRule& r : kTuneTable) {
     if (r.cls == cls && c.M >= r.m_min && c.M <= r.m_max && c.N >= r.n_min && c.N <= r.n_max &&
         mnk >= r.mnk_min && mnk < r.mnk_max) {
-      const int i = plan_index(r.plan);
+      int i = plan_index(r.plan);
       if (i >= 0 && plan_accepts(*plan_at(i), c)) {
         if (fallback) {
           const int f = r.fallback ? plan_index(r.fallback) : i;
           *fallback = f >= 0 ? f : i;
+        }
+        for (const auto& tw : kTileTwins) {  // the other tile shape, when clearly better
+          if (strcmp(r.plan, tw[0]) != 0) continue;
+          const int j = plan_index(tw[1]);
+          if (j >= 0 && plan_accepts(*plan_at(j), c) &&
+              tile_shape_score(*plan_at(j), c) > 1.03 * tile_shape_score(*plan_at(i), c))
+            i = j;
         }
         return i;
       }
@@ -349,6 +368,28 @@ int tail_split(const Plan& pl, const Call& c, int* first) {
   if (S < 2) return 1;
   *first = (int)(q * G);
   return (int)S;
+}
+
+// Expected share of the FFMA pipe's work that is useful for plan pl's tile
+// shape: the wave fill of its persistent grid (whole rounds of tiles, the last
+// round shortened to 1/S by the split tail) over the padding of M and N up to
+// whole tiles.  Measured, 128 x 64 vs 64 x 128 tiles at K = 4096: M = 64
+// 0.49 vs 0.98 (28.6 vs 43.0 TFLOP/s), M = 448 0.49 vs 0.98 (34.0 vs 64.2),
+// M = 1088 0.90 vs 0.99 (61.1 vs 66.9), M = 192 x N = 11008 0.57 vs 0.57
+// (39.2 vs 39.2).
+double tile_shape_score(const Plan& pl, const Call& c) {
+  const long long tm = (c.M + pl.BM - 1) / pl.BM, tn = (c.N + pl.BN - 1) / pl.BN;
+  const double pad = (double)(tm * pl.BM) * (double)(tn * pl.BN) / ((double)c.M * c.N);
+  const long long tiles = tm * tn * (c.batch > 0 ? c.batch : 1);
+  int sms = 0, occ = 0;
+  plan_capacity(pl, &sms, &occ);
+  const double G = (double)sms * occ;
+  int first = 0;
+  const int S = tail_split(pl, c, &first);
+  const long long q = (long long)(tiles / G), r = tiles - (long long)(q * G);
+  const double rounds = (double)q + (r > 0 ? (S > 1 ? 1.0 / S : 1.0) : 0.0);
+  const double fill = rounds > 0 ? (double)tiles / G / rounds : 0.0;
+  return fill / pad;
 }
 
 // Bytes of the split tail's partial sums (0 without a split) and where they

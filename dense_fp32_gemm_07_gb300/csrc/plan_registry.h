@@ -43,6 +43,8 @@ extern const Plan kPlansT128x64[];
 extern const int kNumPlansT128x64;
 extern const Plan kPlansT128x64k32[];
 extern const int kNumPlansT128x64k32;
+extern const Plan kPlansT64x128k32[];
+extern const int kNumPlansT64x128k32;
 extern const Plan kPlansT128x128[];
 extern const int kNumPlansT128x128;
 extern const Plan kPlansGeneral[];

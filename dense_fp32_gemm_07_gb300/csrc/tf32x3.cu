@@ -57,7 +57,6 @@ __device__ __forceinline__ void tf32_split(float x, float& hi, float& lo) {
 __global__ void __launch_bounds__(256) split_a_kernel(const float* __restrict__ A, int M, int K,
                                                       long long lda, float* __restrict__ Ahi,
                                                       float* __restrict__ Alo) {
-  pdl_launch_dependents();
   pdl_wait();
   const long long kv = K / 4;
   const long long total = (long long)M * kv;
@@ -73,6 +72,7 @@ __global__ void __launch_bounds__(256) split_a_kernel(const float* __restrict__ 
     *reinterpret_cast<float4*>(Ahi + r * K + c) = h;
     *reinterpret_cast<float4*>(Alo + r * K + c) = l;
   }
+  pdl_launch_dependents();  // after the work, as in the transpose kernel
 }
 
 // B (K x N, ldb) -> Bhi^T, Blo^T (N x K, leading dimension K) in 64 x 64
@@ -84,7 +84,6 @@ __global__ void __launch_bounds__(256) split_bt_kernel(const float* __restrict__
                                                        long long ldb, float* __restrict__ Bhi,
                                                        float* __restrict__ Blo) {
   __shared__ __align__(16) float tile[64][68];  // [n][k], rows padded to keep 16-byte reads aligned
-  pdl_launch_dependents();
   pdl_wait();
   const int k0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -115,6 +114,7 @@ __global__ void __launch_bounds__(256) split_bt_kernel(const float* __restrict__
       *reinterpret_cast<float4*>(Blo + (long long)n * K + k) = l;
     }
   }
+  pdl_launch_dependents();  // after the work, as in the transpose kernel
 }
 
 // ------------------------------------------------------------- the tensor-core GEMM

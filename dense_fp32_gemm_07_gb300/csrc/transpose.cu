@@ -24,7 +24,6 @@ __global__ void __launch_bounds__(256) transpose_a_kernel(const float* __restric
                                                           long long ldat, long long strideA,
                                                           long long strideAt) {
   __shared__ __align__(16) float tile[kTT][kTT];  // [k][m]
-  pdl_launch_dependents();
   pdl_wait();
   A += (long long)blockIdx.z * strideA;  // problem blockIdx.z of a batch
   At += (long long)blockIdx.z * strideAt;
@@ -58,6 +57,11 @@ __global__ void __launch_bounds__(256) transpose_a_kernel(const float* __restric
       *reinterpret_cast<float4*>(At + (long long)k * ldat + m) = v;
     }
   }
+  // The GEMM that reads At may launch once every CTA is here: launched while
+  // this grid still held the SMs, its persistent CTAs were placed unevenly
+  // (up to three on some SMs, none on others: 1536^3 ran at 42 instead of
+  // 60 TFLOP/s).
+  pdl_launch_dependents();
 }
 
 cudaError_t launch_transpose_a(const float* A, int M, int K, long long lda, float* At,
@@ -122,7 +126,6 @@ __device__ __forceinline__ void pack_tile(const PackJob& j, int bx, int by, int 
 __global__ void __launch_bounds__(256) pack2_kernel(const __grid_constant__ PackJob a,
                                                     const __grid_constant__ PackJob b) {
   __shared__ float tile[32][33];
-  pdl_launch_dependents();
   pdl_wait();
   const int ta = a.tiles_x * a.tiles_y;
   const int t = (int)blockIdx.x;
@@ -130,6 +133,7 @@ __global__ void __launch_bounds__(256) pack2_kernel(const __grid_constant__ Pack
     pack_tile(a, t % a.tiles_x, t / a.tiles_x, (int)blockIdx.z, tile);
   else
     pack_tile(b, (t - ta) % b.tiles_x, (t - ta) / b.tiles_x, (int)blockIdx.z, tile);
+  pdl_launch_dependents();  // after the work: the GEMM's CTAs then find the SMs free
 }
 
 PackJob pack_job(const float* in, long long ld, int trans, int R, int Cc, float* out,
