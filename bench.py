@@ -81,12 +81,16 @@ def fp32_peak_tflops(mhz: float) -> float:
 
 
 def kernel_unit(plan: str) -> str:
-    """The csrc/*.cu file that defines `plan` (and compiles its kernel)."""
+    """The csrc/*.cu file that defines `plan` in a plan table (B2G_..._PLAN(...)
+    entry) and so compiles its kernel; other files may name the plan."""
+    import re
+
     csrc = os.path.join(ROOT, "dense_fp32_gemm_07_gb300", "csrc")
+    pat = re.compile(r'B2G_\w*PLAN\w*\(\s*"' + re.escape(plan) + '"')
     for f in sorted(os.listdir(csrc)):
         if f.endswith(".cu"):
             with open(os.path.join(csrc, f)) as fh:
-                if f'"{plan}"' in fh.read():
+                if pat.search(fh.read()):
                     return "csrc/" + f
     raise KeyError(plan)
 

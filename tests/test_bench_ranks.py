@@ -74,3 +74,20 @@ def test_reference_arm_other_ranks_leave_quietly():
                        text=True, timeout=120)
     assert r.returncode == 0, r.stderr
     assert r.stdout.strip() == ""
+
+
+def test_kernel_unit_finds_each_plans_definition():
+    """bench.py ties the recorded DRAM traffic to the sources of the kernel's
+    translation unit: the file that defines the plan, not one that only names
+    it (host.cu names the packed plans in its table of tile-shape twins)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import dense_fp32_gemm_07_gb300 as b2g
+    from dense_fp32_gemm_07_gb300 import build
+
+    build.build()
+    for name in b2g.plans():
+        unit = bench.kernel_unit(name)
+        assert unit.startswith("csrc/") and unit != "csrc/host.cu", (name, unit)
+        src = open(os.path.join(ROOT, "dense_fp32_gemm_07_gb300", unit)).read()
+        assert f'"{name}"' in src and "PLAN" in src
