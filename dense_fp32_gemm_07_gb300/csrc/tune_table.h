@@ -39,12 +39,11 @@ const TuneRule kTuneTable[] = {
     {kClassFast, 0, 8, 0, kInf, 0, "skinny_m8", nullptr},
     {kClassFast, 9, 16, 0, kInf, 0, "skinny_m16", nullptr},
     {kClassFast, 17, 32, 0, kInf, 0, "skinny_m32", nullptr},
-    // other small M: too few row tiles to fill 152 SMs with the tiled plans
-    {kClassFast, 0, 48, 0, kInf, 0, "tma_64x128x16_s6_o1", nullptr},
     // up to ~1e9 multiply-adds the transpose costs about what it saves
-    {kClassFast, 49, kInf, 0, kInf, 0, "tma_64x128x16_s6_o2", nullptr, 1.0e9},
-    // larger: A transposed into the workspace, then the transposed-layout kernel
-    {kClassFast, 49, kInf, 0, kInf, 1.0e9, "pre_128x64x32_s3_o5", "tmaX_128x128x16_s6_o2"},
+    {kClassFast, 0, kInf, 0, kInf, 0, "tma_64x128x16_s6_o2", nullptr, 1.0e9},
+    // larger: A transposed into the workspace, then the transposed-layout
+    // kernel (its 64 x 128 twin when that pads less, e.g. M <= 64)
+    {kClassFast, 0, kInf, 0, kInf, 1.0e9, "pre_128x64x32_s3_o5", "tmaX_128x128x16_s6_o2"},
     {kClassFastTransA, 0, kInf, 0, kInf, 0, "tmaT_128x64x32_s3_o5", nullptr},
     // anything else (misaligned pointers, odd leading dimensions, K % 4 != 0,
     // op(B) = B^T): pack A^T and B aligned into the workspace, then the
