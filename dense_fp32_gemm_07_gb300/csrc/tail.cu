@@ -3,7 +3,7 @@
 // A persistent grid of G CTAs that runs T output tiles finishes when its
 // busiest SM does: with T = q*G + r (0 < r < G) the last round keeps only r
 // CTAs busy.  The host therefore cuts each of the last r tiles into S k slices
-// (S = G / r, at least 128 k per slice), so every CTA gets q whole tiles plus
+// (S = G / r, at least 64 k per slice), so every CTA gets q whole tiles plus
 // at most one slice.  The GEMM kernel writes each slice's raw BM x BN sums to
 // the workspace; this kernel adds a tile's S slices in slice order (a fixed
 // order: results are reproducible run to run) and applies the same epilogue

@@ -71,7 +71,7 @@ extern "C" {
  *
  * Split tail: a persistent grid of G CTAs over T output tiles, T = q*G + r
  * with 0 < r < G, would keep only r CTAs busy in its last round.  The last r
- * tiles are then cut into S = G / r k slices (at least 128 k each) whose
+ * tiles are then cut into S = G / r k slices (at least 64 k each) whose
  * partial sums go to the workspace, after A^T, and a second kernel adds each
  * tile's slices in slice order and applies the epilogue.  The summation order
  * is fixed for given arguments, so results stay reproducible run to run; the

@@ -129,12 +129,12 @@ NO_DEVICE_SLOTS = 152 * 4
 
 def split_tail(M, N, K, BM, BN, slots=NO_DEVICE_SLOTS):
     """(first split tile, slices) of the split-tail rule: T tiles over G slots,
-    T = q*G + r; the last r tiles get S = G // r slices of at least 128 k."""
+    T = q*G + r; the last r tiles get S = G // r slices of at least 64 k."""
     T = -(-M // BM) * -(-N // BN)
     q, r = divmod(T, slots)
     if r == 0:
         return 0, 1
-    S = min(slots // r, K // 128)
+    S = min(slots // r, K // 64)
     return (q * slots, S) if S >= 2 else (0, 1)
 
 
@@ -160,7 +160,7 @@ def test_split_tail_rule_examples():
     assert split_tail(2048, 2048, 2048, 64, 128, slots=456) == (456, 8)
     # whole waves, too little k, or r too large for 2 slices: no split
     assert split_tail(64 * 608, 128, 4096, 64, 128) == (0, 1)
-    assert split_tail(4096, 4096, 255, 128, 64) == (0, 1)
+    assert split_tail(4096, 4096, 127, 128, 64) == (0, 1)
     assert split_tail(4096, 640, 4096, 128, 64) == (0, 1)  # 320 tiles > 608 / 2
 
 

@@ -37,13 +37,13 @@ def test_split_engages_on_these_shapes(tb):
     assert launches(b2g, 300, 260, 1000) == 2
     assert launches(b2g, 1030, 1500, 1400) == 3
     assert launches(b2g, 4096, 4096, 4096) == 3
-    assert launches(b2g, 300, 260, 200) == 1  # under 256 k: no split
+    assert launches(b2g, 300, 260, 100) == 1  # under 128 k: no split
 
 
 @pytest.mark.parametrize("trans", [(False, False), (True, False), (False, True)])
 def test_every_plan_split_ragged(tb, trans):
     """A few tiles and 1000 k (ragged last k tile): every plan splits the
-    tiles into k slices (up to 7 of at least 128 k)."""
+    tiles into k slices (up to 15 of at least 64 k)."""
     torch, b2g = tb
     M, N, K = 300, 260, 1000
     rng = np.random.default_rng(11)
