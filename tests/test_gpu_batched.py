@@ -102,3 +102,28 @@ def test_tensor_api(tb):
     for b in range(3):
         ref, bound, _ = oracle.sgemm(A[b], B[b], None, 1.0, 0.0)
         check(got[b], ref, bound, f"tensor api {b}")
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 16, 16), (17, 19, 13)])
+def test_batch_past_grid_z_limit(tb, M, N, K):
+    """70000 problems (more than the 65535 a grid's z extent holds): the plans
+    that put the batch in z refuse, the table's choice walks the batch in its
+    tile scheduler.  Sampled problems, both sides of 65535, against the oracle."""
+    torch, b2g = tb
+    batch = 70000
+    rng = np.random.default_rng(M * N * K)
+    A = rng.uniform(-1, 1, (batch, M, K)).astype(np.float32)
+    B = rng.uniform(-1, 1, (batch, K, N)).astype(np.float32)
+    C = rng.uniform(-1, 1, (batch, M, N)).astype(np.float32)
+    dA, dB, dC = (torch.from_numpy(x).cuda() for x in (A, B, C))
+    rc = b2g.b2g_sgemm_strided_batched(0, 0, M, N, K, 0.5, dA.data_ptr(), K, M * K, dB.data_ptr(),
+                                       N, K * N, 2.0, dC.data_ptr(), N, M * N, batch,
+                                       torch.cuda.current_stream().cuda_stream)
+    assert rc == 0, b2g.b2g_strerror(rc)
+    torch.cuda.synchronize()
+    out = dC.cpu().numpy()
+    picks = sorted(set([0, 1, 65534, 65535, 65536, 65537, batch - 1] +
+                       list(rng.integers(0, batch, 40))))
+    for b in picks:
+        ref, bound, _ = oracle.sgemm(A[b], B[b], C[b], 0.5, 2.0)
+        check(out[b], ref, bound, f"problem {b} of {batch}")
