@@ -119,6 +119,18 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
       : "memory");
 }
 
+// Fetch the box at (c0, c1, c2) from global memory into L2 only: nothing is
+// written to shared memory and no barrier is signalled.  Reading it cannot go
+// stale (L2 is the device's point of coherence), so it may be issued before
+// the grid's dependencies are met, to overlap the first fetches with the
+// previous grid's last work.
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* m, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, int c0, int c1,
                                             int c2, uint32_t bar) {
   asm volatile(

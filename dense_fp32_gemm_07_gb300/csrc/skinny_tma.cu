@@ -48,6 +48,7 @@ constexpr int kStBK = 32;   // k rows per stage
 constexpr int kStBN = 128;  // columns of C per CTA
 constexpr int kStStages = 4;
 constexpr int kStMaxCluster = 8;  // portable cluster size: at most 8 k slabs per column slab
+constexpr int kStPrefetch = 4;    // stages of B and A fetched into L2 before the dependency wait
 
 template <int MR>
 struct SkinnyTmaCfg {
@@ -107,6 +108,12 @@ __global__ void __launch_bounds__(SkinnyTmaCfg<MR>::kThreads)
   if (warp == Cfg::kConsumerWarps && lane == 0) {
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
+    // the first stages into L2 while the previous grid finishes (its writes,
+    // should it write these operands, still land in L2 before they are read)
+    for (int c = 0; c < nst && c < kStPrefetch; ++c) {
+      tma_prefetch_3d(&tmB, n0, kb + c * kStBK, bz);
+      tma_prefetch_3d(&tmA, kb + c * kStBK, 0, bz);
+    }
   }
   __syncthreads();
   pdl_wait();

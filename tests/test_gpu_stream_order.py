@@ -64,6 +64,41 @@ def test_read_after_write_chain(tb):
     check(dC3.cpu().numpy(), ref3, bound3, "C3 = C1 V + C3")
 
 
+def test_skinny_reads_b_the_previous_kernel_writes(tb):
+    """The skinny cluster kernel fetches its first stages of B into L2 before
+    it waits for the previous grid.  Here that grid writes the very B it reads
+    (a GEMM writes W2 = X Y; the skinny call reads W2), and then a second
+    skinny call reads the first one's output as its B: both must see the
+    finished values, not lines fetched while they were being written."""
+    torch, b2g = tb
+    rng = np.random.default_rng(34)
+    X = rng.uniform(-1, 1, (1024, 256)).astype(np.float32)
+    Y = rng.uniform(-1, 1, (256, 4096)).astype(np.float32)
+    A16 = rng.uniform(-1, 1, (16, 1024)).astype(np.float32)
+    A8 = rng.uniform(-1, 1, (8, 16)).astype(np.float32)
+    dX, dY, dA16, dA8 = (_dev(torch, x) for x in (X, Y, A16, A8))
+    dW2 = torch.full((1024, 4096), float("nan"), device="cuda")
+    dC4 = torch.zeros((16, 4096), device="cuda")
+    dC5 = torch.zeros((8, 4096), device="cuda")
+    torch.cuda.synchronize()
+    b2g.sgemm(dX, dY, dW2, 1.0, 0.0)     # writes B of the next call
+    b2g.sgemm(dA16, dW2, dC4, 1.0, 0.0)  # skinny: B = W2
+    b2g.sgemm(dA8, dC4, dC5, 1.0, 0.0)   # skinny (K = 16): B = the previous output
+    torch.cuda.synchronize()
+    got_w = dW2.cpu().numpy()
+    refw, boundw = _ref(X, Y, None, 1.0, 0.0)
+    check(got_w, refw, boundw, "W2 = X Y")
+    got4 = dC4.cpu().numpy()
+    ref4, bound4 = _ref(A16, got_w, None, 1.0, 0.0)
+    check(got4, ref4, bound4, "C4 = A16 W2")
+    ref5, bound5 = _ref(A8, got4, None, 1.0, 0.0)
+    check(dC5.cpu().numpy(), ref5, bound5, "C5 = A8 C4")
+    for name, (M, N, K) in {"C4": (16, 4096, 1024), "C5": (8, 4096, 16)}.items():
+        plan = b2g.b2g_plan_name(b2g.b2g_sgemm_select_plan(0, 0, M, N, K, 1.0, 1 << 20, K,
+                                                           1 << 20, N, 1 << 20, N))
+        assert plan.startswith("skinnyT"), (name, plan)
+
+
 def test_write_after_read_chain(tb):
     """Call 1 reads A and B; call 2 writes into A's and B's storage at once.
     Call 1's result must be the product of the original A and B."""
