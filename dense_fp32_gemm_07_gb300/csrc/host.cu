@@ -520,7 +520,7 @@ int run(const Call& c, int forced_plan, void* stream, void* user_ws = nullptr,
   if (!plan_accepts(*pl, c)) return B2G_ERR_UNSUPPORTED;
 
   int dev = 0;
-  cudaGetDevice(&dev);
+  if (cudaGetDevice(&dev) != cudaSuccess) return B2G_ERR_DEVICE;
   float* ws = nullptr;
   bool auto_ws = false;
   const size_t base = plan_base_bytes(*pl, c);
@@ -847,7 +847,7 @@ int run_tf32x3(const Call& c, void* stream, int variant) {
   if (!needs_gemm(c)) return launch_scale(c, *d, st);
   if (c.transA || c.transB || !aligned16(c.A) || c.lda % 4 || c.K % 4) return B2G_ERR_UNSUPPORTED;
   int dev = 0;
-  cudaGetDevice(&dev);
+  if (cudaGetDevice(&dev) != cudaSuccess) return B2G_ERR_DEVICE;
 
   Tf32x3Params p;
   p.M = c.M, p.N = c.N, p.K = c.K;
