@@ -334,7 +334,13 @@ def _t():
 
 def _stream_handle(stream) -> int:
     if stream is None:
-        return _t().cuda.current_stream().cuda_stream
+        torch = _t()
+        # the current stream's handle without building a Stream object (2.8 us
+        # a call through torch.cuda.current_stream(), 0.1 us this way)
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        if raw is not None:
+            return raw(torch.cuda.current_device())
+        return torch.cuda.current_stream().cuda_stream
     return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
 
 
