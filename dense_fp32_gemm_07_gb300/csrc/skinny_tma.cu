@@ -115,6 +115,17 @@ __global__ void __launch_bounds__(SkinnyTmaCfg<MR>::kThreads)
       tma_prefetch_3d(&tmA, kb + c * kStBK, 0, bz);
     }
   }
+  if (warp == Cfg::kConsumerWarps && beta != 0.f) {
+    // and the lines of C this CTA will read at the end (its share of the
+    // tile in a cluster, the whole tile alone), in bounds only: one line of
+    // 8 float4 per lane and step
+    constexpr int E = MR * (kStBN / 4);
+    const int S = clustered ? p.splits : 1, r = clustered ? s : 0;
+    for (int e = r * E / S + 8 * lane; e < (r + 1) * E / S; e += 8 * 32) {
+      const int i = e / (kStBN / 4), col = n0 + 4 * (e % (kStBN / 4));
+      if (i < p.M && col < p.N) prefetch_l2(Cb + (long long)i * p.ldc + col);
+    }
+  }
   __syncthreads();
   pdl_wait();
 
