@@ -131,12 +131,6 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* m, int c0, in
                : "memory");
 }
 
-// Fetch the 128-byte line holding `p` into L2 (no register or shared-memory
-// result; the same coherence argument as tma_prefetch_3d).
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
-}
-
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, int c0, int c1,
                                             int c2, uint32_t bar) {
   asm volatile(

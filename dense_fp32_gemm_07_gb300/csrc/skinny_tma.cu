@@ -50,6 +50,12 @@ constexpr int kStStages = 4;
 constexpr int kStMaxCluster = 8;  // portable cluster size: at most 8 k slabs per column slab
 constexpr int kStPrefetch = 4;    // stages of B and A fetched into L2 before the dependency wait
 
+// Fetch the 128-byte line holding `p` into L2 (no register or shared-memory
+// result; like tma_prefetch_3d it cannot read a stale value).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
+}
+
 template <int MR>
 struct SkinnyTmaCfg {
   static constexpr int kGroups = MR / 8;                       // row groups of 8
