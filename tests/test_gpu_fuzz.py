@@ -114,3 +114,58 @@ def test_random_strided_batch(tb, seed):
     prev = before.cpu().numpy()
     assert np.array_equal(out[keep].view(np.uint32), prev[keep].view(np.uint32)), \
         f"{what}: a float outside the C windows changed"
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_tf32x3(tb, seed):
+    """The 3xTF32 path (every kernel variant) on random ragged shapes: row-major
+    operands with K and lda multiples of 4, its documented domain."""
+    torch, b2g = tb
+    rng = np.random.default_rng(3000 + seed)
+    M, N = (int(x) for x in rng.integers(1, 700, size=2))
+    K = 4 * int(rng.integers(1, 400))
+    variant = seed % 3
+    lda = K + 4 * int(rng.integers(0, 3))
+    ldb, ldc = N + int(rng.integers(0, 5)), N + int(rng.integers(0, 5))
+    alpha = float(rng.choice(ALPHAS))
+    beta = float(rng.choice(BETAS))
+    A, B, C = _stored(rng, M, K), _stored(rng, K, N), _stored(rng, M, N)
+    dA = torch.full((M, lda), float("nan"), device="cuda")
+    dA[:, :K] = torch.from_numpy(A).cuda()
+    dB = torch.full((K, ldb), float("nan"), device="cuda")
+    dB[:, :N] = torch.from_numpy(B).cuda()
+    dC = torch.full((M + 1, ldc), float("nan"), device="cuda")
+    dC[:M, :N] = torch.from_numpy(C).cuda()
+    before = dC.clone()
+    s = torch.cuda.current_stream().cuda_stream
+    rc = b2g.b2g_sgemm_3xtf32_variant(variant, M, N, K, alpha, dA.data_ptr(), lda, dB.data_ptr(),
+                                      ldb, beta, dC.data_ptr(), ldc, s)
+    what = f"seed {seed}: variant {variant} {M}x{N}x{K} lds=({lda},{ldb},{ldc}) {alpha} {beta}"
+    assert rc == 0, f"{what}: {b2g.b2g_strerror(rc)}"
+    torch.cuda.synchronize()
+    out, prev = dC.cpu().numpy(), before.cpu().numpy()
+    ref, bound, _ = oracle.sgemm(A, B, C, alpha, beta)
+    check(out[:M, :N], ref, bound, what)
+    outside = np.ones(out.shape, bool)
+    outside[:M, :N] = False
+    assert np.array_equal(out[outside].view(np.uint32), prev[outside].view(np.uint32)), what
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_host_operands(tb, seed):
+    """b2g_sgemm_host on random shapes on both sides of its 2048-k chunking
+    threshold, from page-locked and from pageable host memory."""
+    torch, b2g = tb
+    rng = np.random.default_rng(4000 + seed)
+    M, N = (int(x) for x in rng.integers(1, 600, size=2))
+    K = int(rng.integers(2048, 3000)) if seed % 2 else int(rng.integers(1, 2048))
+    alpha = float(rng.choice(ALPHAS))
+    beta = float(rng.choice(BETAS))
+    A, B, C = _stored(rng, M, K), _stored(rng, K, N), _stored(rng, M, N)
+    pinned = seed % 4 < 2
+    hA, hB, hC = (torch.from_numpy(x.copy()) for x in (A, B, C))
+    if pinned:
+        hA, hB, hC = hA.pin_memory(), hB.pin_memory(), hC.pin_memory()
+    b2g.sgemm_host(hA, hB, hC, alpha, beta)
+    ref, bound, _ = oracle.sgemm(A, B, C, alpha, beta)
+    check(hC.numpy(), ref, bound, f"seed {seed}: {M}x{N}x{K} pinned={pinned} {alpha} {beta}")
