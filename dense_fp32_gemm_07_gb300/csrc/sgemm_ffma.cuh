@@ -200,7 +200,9 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32,
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  pdl_launch_dependents();  // the next grid may set up while this one runs
+  // the next grid may set up while this one runs, unless this grid leaves
+  // slots free for it to land in unevenly (then it launches as CTAs exit)
+  if (!p.pdl_late) pdl_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full0 + 8 * s, FEED == kFeedCpAsync ? Cfg::kProducers : 1);
@@ -529,6 +531,7 @@ cudaError_t launch_ffma(const SgemmParams& p, const CUtensorMap* tmA, const CUte
   CUtensorMap none;
   memset(&none, 0, sizeof(none));
   SgemmParams pc = p;
+  pc.pdl_late = grid < (long long)num_sms * occ ? 1 : 0;
   CUtensorMap a = tmA ? *tmA : none, b = tmB ? *tmB : none;
   void* args[] = {&pc, &a, &b};
   return launch_pdl(reinterpret_cast<const void*>(kern), dim3(grid), dim3(Cfg::kThreads), args,

@@ -35,6 +35,11 @@ struct SgemmParams {
   // then adds each tile's slices in order and applies the epilogue.
   int tail_first;
   int tail_splits;
+  // 1 when the grid leaves resident CTA slots free: the kernel then does not
+  // let the next grid launch early, since an early grid's CTAs would be placed
+  // into those free slots unevenly (some SMs three, others none); they are
+  // placed once this grid's CTAs exit.  Set by the launcher.
+  int pdl_late;
 };
 
 // How A is laid out in one shared-memory stage.
