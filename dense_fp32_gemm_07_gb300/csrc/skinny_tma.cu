@@ -49,6 +49,13 @@ constexpr int kStBN = 128;  // columns of C per CTA
 constexpr int kStStages = 4;
 constexpr int kStMaxCluster = 8;  // portable cluster size: at most 8 k slabs per column slab
 constexpr int kStPrefetch = 4;    // stages of B and A fetched into L2 before the dependency wait
+// Where a CTA lets the next grid on the stream launch (cold-L2 timings at
+// 4096 x 4096, back to back): 8 rows best without an early signal (CTAs launch
+// as these exit: 14.1 us against 16.1 signalling at the start), 16 and 32 rows
+// best after the main loop (18.4 / 29.1 us against 18.7 / 29.4 at the start,
+// 19.2 / 29.8 at exit).
+template <int MR>
+constexpr bool kStSignalAfterLoop = MR > 8;
 
 // Fetch the 128-byte line holding `p` into L2 (no register or shared-memory
 // result; like tma_prefetch_3d it cannot read a stale value).
@@ -97,11 +104,10 @@ __global__ void __launch_bounds__(SkinnyTmaCfg<MR>::kThreads)
   const float alpha = p.alpha, beta = p.beta;
   float* Cb = p.C + (long long)bz * p.strideC;
 
-  // Launched as a programmatic dependent: the next kernel on the stream may
-  // start as soon as every CTA of this one runs (its CTAs then set up while
-  // this grid finishes), and this grid touches global memory only after the
-  // previous grid on the stream has completed and its writes are visible.
-  pdl_launch_dependents();
+  // Launched as a programmatic dependent: this grid touches global memory only
+  // after the previous grid on the stream has completed and its writes are
+  // visible; the next grid may launch once every CTA here has passed its main
+  // loop (kStSignalAfterLoop) or exited.
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStStages; ++i) {
       mbar_init(full0 + 8 * i, 1);
@@ -159,6 +165,7 @@ __global__ void __launch_bounds__(SkinnyTmaCfg<MR>::kThreads)
       }
     }
     __syncwarp();
+    if (kStSignalAfterLoop<MR>) pdl_launch_dependents();
   } else {
     // ---------------------------------------------------------- consumers
     const int rg = warp >> 2, kg = warp & 3;  // row group, k group
@@ -204,6 +211,7 @@ __global__ void __launch_bounds__(SkinnyTmaCfg<MR>::kThreads)
       if (lane == 0) mbar_arrive(empty0 + 8 * st);
       if (++st == kStStages) st = 0, ph ^= 1u;
     }
+    if (kStSignalAfterLoop<MR>) pdl_launch_dependents();
 
     // k groups 1..3 -> shared memory (the drained ring); k group 0 adds them in
     // k-group order and keeps (cluster) or writes (alone) the CTA's sums
