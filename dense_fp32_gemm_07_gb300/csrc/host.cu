@@ -829,9 +829,10 @@ size_t tf32x3_bytes(const Call& c) {
 // variant: 0 one CTA per 128 x 128 tile, 1 a CTA pair per 256 x 128 tile,
 // 2 a CTA pair per 256 x 256 tile.
 // Measured on GB300 (TFLOP/s of FP32 results, variants 0 / 1 / 2): 1536^3
-// 145.8 / 136.0 / 104.0, 2048^3 166.8 / 160.9 / 186.1, 4096^3 232.2 / 236.7 /
-// 275.7, 8192^3 266.1 / 266.7 / 345.9: the 256 x 256 pair (twice the work per
-// MMA instruction) from about 1800^3 up, one CTA per 128 x 128 tile below.
+// 172.7 / 164.0 / 114.1, 2048^3 184.4 / 179.1 / 215.6, 3072^3 219.8 / 224.7 /
+// 281.1, 4096^3 234.9 / 240.2 / 305.0, 8192^3 266.5 / 267.7 / 351.9: the
+// 256 x 256 pair (twice the work per MMA instruction) from about 1800^3 up,
+// one CTA per 128 x 128 tile below.
 int tc_default_variant(const Call& c) {
   return ((double)c.M * c.N * c.K >= 6.0e9 && c.M >= 512 && c.N >= 512) ? 2 : 0;
 }
