@@ -4,9 +4,10 @@
 // (a thread's eight m values in two 16-byte vectors).  Row-major A has k
 // contiguous instead, so the pre-transposed plans first write At (K x ldat,
 // row-major, ldat = M rounded up to 4) into a workspace with this HBM-bound
-// kernel: 64 x 64 tiles, 16-byte loads of A rows, a [64 k][64 m] shared tile
-// written by 32 consecutive m per warp store (no bank conflicts), and 16-byte
-// stores of At rows.  Requires A 16-byte aligned with lda % 4 == 0 and
+// kernel: 64 x 64 tiles, each row of A's tile read by 16 consecutive threads
+// as 16-byte vectors (a warp's load covers two whole 256-byte row segments:
+// one request per line rather than one per thread), a [64 k][65] shared tile,
+// and At rows written the same way.  Requires A 16-byte aligned with lda % 4 == 0 and
 // K % 4 == 0 (the callers check); M is arbitrary.  Columns M .. ldat-1 of At
 // are padding and receive zeros.
 #include <cuda_runtime.h>
@@ -23,38 +24,43 @@ __global__ void __launch_bounds__(256) transpose_a_kernel(const float* __restric
                                                           float* __restrict__ At,
                                                           long long ldat, long long strideA,
                                                           long long strideAt) {
-  __shared__ __align__(16) float tile[kTT][kTT];  // [k][m]
+  // [k][m] with rows of 65 floats: the scalar writes of a warp (16 k chunks x
+  // 2 rows of A) and the scalar reads (2 k rows x 16 m chunks) both meet
+  // bank conflicts of at most two ways.
+  __shared__ float tile[kTT][kTT + 1];
   pdl_wait();
   A += (long long)blockIdx.z * strideA;  // problem blockIdx.z of a batch
   At += (long long)blockIdx.z * strideAt;
   const int m0 = blockIdx.x * kTT, k0 = blockIdx.y * kTT;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  // load: warp w takes 4-k chunks c = w, w+8; lanes take 32 consecutive rows
+  const int q = threadIdx.x & 15, r = threadIdx.x >> 4;  // 16-byte chunk, row (0..15)
+  // load: 16 consecutive threads read one row of A's tile as 16-byte vectors
+  // (a warp takes two whole 256-byte row segments)
+  float4 v[kTT / 16];
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int m = m0 + h * 32 + lane;
+  for (int i = 0; i < kTT / 16; ++i) {
+    const int m = m0 + r + 16 * i, k = k0 + 4 * q;
+    v[i] = (m < M && k < K) ? *reinterpret_cast<const float4*>(A + (long long)m * lda + k)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
 #pragma unroll
-    for (int cc = 0; cc < 2; ++cc) {
-      const int c = warp + 8 * cc;  // 0..15
-      const int k = k0 + 4 * c;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (m < M && k < K) v = *reinterpret_cast<const float4*>(A + (long long)m * lda + k);
-      tile[4 * c + 0][h * 32 + lane] = v.x;
-      tile[4 * c + 1][h * 32 + lane] = v.y;
-      tile[4 * c + 2][h * 32 + lane] = v.z;
-      tile[4 * c + 3][h * 32 + lane] = v.w;
-    }
+  for (int i = 0; i < kTT / 16; ++i) {
+    const int ml = r + 16 * i;
+    tile[4 * q + 0][ml] = v[i].x;
+    tile[4 * q + 1][ml] = v[i].y;
+    tile[4 * q + 2][ml] = v[i].z;
+    tile[4 * q + 3][ml] = v[i].w;
   }
   __syncthreads();
-  // store: 16 threads cover one At row segment of 64 m as 16-byte vectors
-  const int t = threadIdx.x & 15, r = threadIdx.x >> 4;  // r = 0..15
+  // store: 16 consecutive threads write one At row segment of 64 m as 16-byte
+  // vectors; columns M .. ldat-1 receive the zeros loaded for rows past M
 #pragma unroll
-  for (int rr = 0; rr < kTT / 16; ++rr) {
-    const int kl = r + 16 * rr;
-    const int k = k0 + kl, m = m0 + 4 * t;
+  for (int i = 0; i < kTT / 16; ++i) {
+    const int kl = r + 16 * i;
+    const int k = k0 + kl, m = m0 + 4 * q;
     if (k < K && m < ldat) {
-      const float4 v = *reinterpret_cast<const float4*>(&tile[kl][4 * t]);
-      *reinterpret_cast<float4*>(At + (long long)k * ldat + m) = v;
+      const float4 o = make_float4(tile[kl][4 * q], tile[kl][4 * q + 1], tile[kl][4 * q + 2],
+                                   tile[kl][4 * q + 3]);
+      *reinterpret_cast<float4*>(At + (long long)k * ldat + m) = o;
     }
   }
   // The GEMM that reads At may launch once every CTA is here: launched while
