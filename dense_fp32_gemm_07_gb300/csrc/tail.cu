@@ -37,17 +37,20 @@ __global__ void __launch_bounds__(256) tail_reduce_kernel(const __grid_constant_
     const int r = q / n4, c = (q - r * n4) * 4;
     const int gr = m0 + r, gc = n0 + c;
     if (gr >= p.M || gc >= p.N) continue;
+    float* crow = Cb + (long long)gr * p.ldc;
+    const bool vec = p.c_vec4 && gc + 3 < p.N;
+    // C's values first, so that their trip from memory overlaps the slices'
+    float4 cv = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (vec && beta != 0.f) cv = *reinterpret_cast<const float4*>(crow + gc);
     float4 acc = *reinterpret_cast<const float4*>(P + (size_t)q * 4);
     for (int s = 1; s < S; ++s) {
       const float4 v = *reinterpret_cast<const float4*>(P + s * tile_elems + (size_t)q * 4);
       acc.x += v.x, acc.y += v.y, acc.z += v.z, acc.w += v.w;
     }
     const float av[4] = {acc.x, acc.y, acc.z, acc.w};
-    float* crow = Cb + (long long)gr * p.ldc;
-    if (p.c_vec4 && gc + 3 < p.N) {
+    if (vec) {
       float4 o;
       if (beta != 0.f) {
-        const float4 cv = *reinterpret_cast<const float4*>(crow + gc);
         o.x = fmaf(alpha, av[0], beta * cv.x);
         o.y = fmaf(alpha, av[1], beta * cv.y);
         o.z = fmaf(alpha, av[2], beta * cv.z);
@@ -72,8 +75,8 @@ cudaError_t launch_tail_reduce(const SgemmParams& p, int BM, int BN, cudaStream_
   const long long tiles = (long long)p.tiles_m * p.tiles_n * p.batch;
   const long long n = tiles - p.tail_first;
   if (p.tail_splits <= 1 || n <= 0) return cudaSuccess;
-  // two float4 positions per thread
-  const unsigned gy = (unsigned)((BM * BN / 4 + 511) / 512);
+  // one float4 position per thread: every load of a thread in flight at once
+  const unsigned gy = (unsigned)((BM * BN / 4 + 255) / 256);
   SgemmParams pc = p;
   void* args[] = {&pc, &BM, &BN};
   return launch_pdl(reinterpret_cast<const void*>(&tail_reduce_kernel), dim3((unsigned)n, gy),
