@@ -742,17 +742,20 @@ __global__ void __launch_bounds__(256) tc_tail_reduce_kernel(const __grid_consta
     const int r = q / n4, c = (q - r * n4) * 4;
     const int gr = m0 + r, gc = n0 + c;
     if (gr >= p.M || gc >= p.N) continue;
+    float* crow = p.C + (long long)gr * p.ldc;
+    const bool vec = p.c_vec4 && gc + 3 < p.N;
+    // C's values first, so that their trip from memory overlaps the slices'
+    float4 cv = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (vec && beta != 0.f) cv = *reinterpret_cast<const float4*>(crow + gc);
     float4 acc = *reinterpret_cast<const float4*>(P + (size_t)q * 4);
     for (int s = 1; s < S; ++s) {
       const float4 v = *reinterpret_cast<const float4*>(P + s * tile_elems + (size_t)q * 4);
       acc.x += v.x, acc.y += v.y, acc.z += v.z, acc.w += v.w;
     }
     const float av[4] = {acc.x, acc.y, acc.z, acc.w};
-    float* crow = p.C + (long long)gr * p.ldc;
-    if (p.c_vec4 && gc + 3 < p.N) {
+    if (vec) {
       float4 o;
       if (beta != 0.f) {
-        const float4 cv = *reinterpret_cast<const float4*>(crow + gc);
         o = make_float4(fmaf(alpha, av[0], beta * cv.x), fmaf(alpha, av[1], beta * cv.y),
                         fmaf(alpha, av[2], beta * cv.z), fmaf(alpha, av[3], beta * cv.w));
       } else {
@@ -773,7 +776,7 @@ __global__ void __launch_bounds__(256) tc_tail_reduce_kernel(const __grid_consta
 cudaError_t launch_tf32x3_tail_reduce(const Tf32x3Params& p, int pn, cudaStream_t stream) {
   const long long n = (long long)p.tiles_m * p.tiles_n - p.tail_first;
   if (p.tail_splits <= 1 || n <= 0) return cudaSuccess;
-  const unsigned gy = (unsigned)((2 * kTcBM * pn / 4 + 511) / 512);  // 2 float4 per thread
+  const unsigned gy = (unsigned)((2 * kTcBM * pn / 4 + 255) / 256);  // 1 float4 per thread
   Tf32x3Params pc = p;
   void* args[] = {&pc, &pn};
   return launch_pdl(reinterpret_cast<const void*>(&tc_tail_reduce_kernel), dim3((unsigned)n, gy),
