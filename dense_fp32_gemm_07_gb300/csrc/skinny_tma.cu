@@ -48,7 +48,7 @@ constexpr int kStBK = 32;   // k rows per stage
 constexpr int kStBN = 128;  // columns of C per CTA
 constexpr int kStStages = 4;
 constexpr int kStMaxCluster = 8;  // portable cluster size: at most 8 k slabs per column slab
-constexpr int kStPrefetch = 4;    // stages of B and A fetched into L2 before the dependency wait
+constexpr int kStPrefetch = 2;    // stages of B and A fetched into L2 before the dependency wait
 // Where a CTA lets the next grid on the stream launch (cold-L2 timings at
 // 4096 x 4096, back to back): 8 rows best without an early signal (CTAs launch
 // as these exit: 14.1 us against 16.1 signalling at the start), 16 and 32 rows
