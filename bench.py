@@ -18,6 +18,21 @@ bounds, as GB/s of algorithmic bytes against the measured copy bandwidth; its
 calls rotate through four operand sets so that each finds its operands out of
 L2.
 
+After the timed e2e steps, one more call from the original C is checked
+against the oracle on sampled entries (outside the timing).
+
+`configs` reports every workload of workloads.py (512^3, 4096^3, the ragged
+1000 x 1025 x 777 shape, the square sweep 128..8192, 8192 x 11008 x 4096 and
+16 x 4096 x 4096): microseconds per call back to back through the C ABI and
+replayed from a CUDA graph, TFLOP/s, the roofline bound and the fraction of
+min(FP32 peak, AI x HBM bandwidth), with the calls rotating through operand
+copies so that each finds its operands out of L2; beside each, the CPU
+oracle's GFLOP/s on a leading block of rows (all host cores).
+
+Peaks: FP32 = SMs (from the device) x 128 lanes x 2 x the maximum SM clock
+(nvidia-smi); TF32 = SMs x 4096 dense FLOP/clk x the same clock; HBM = the
+measured copy bandwidth in MEASURED_PEAKS.json.
+
 `--impl reference` times the CPU oracle (double i-k-j loops, all host cores)
 on a bounded row sample of the same workload instead.
 """
@@ -40,9 +55,16 @@ import workloads  # noqa: E402
 
 METRIC = "SGEMM TFLOPS (2MNK/t) at M=N=K=4096; % of GB300 FP32 vector peak"
 UNIT = "TFLOP/s"
-# FP32 vector peak from unit counts: 152 SMs x 128 FP32 lanes x 2 FLOP per FMA
-# x clock.  The contract's peak uses the maximum SM clock (2070 MHz).
-SMS, LANES, MAX_MHZ = 152, 128, 2070.0
+# FP32 vector peak from unit counts: SMs x 128 FP32 lanes x 2 FLOP per FMA x
+# clock; the SM count comes from the device, the clock from nvidia-smi's
+# maximum SM clock (MAX_MHZ_FALLBACK when it cannot be read).
+LANES = 128
+MAX_MHZ_FALLBACK = 2070.0
+# Dense TF32 tensor-core rate per SM and clock: half the 8192 dense bf16
+# FLOP/clk/SM of a Blackwell SM (2.25 PFLOP/s bf16 nominal on 152 SMs is
+# 8192 FLOP/clk/SM at about 1.81 GHz; the nominal TF32 figure, 1.1 PFLOP/s, is
+# half of it).
+TF32_FLOP_PER_CLK_SM = 4096
 L2_BYTES = 129e6
 # device code of the dominant kernel: a change here voids the recorded traffic
 # The recorded traffic is valid while these headers and the translation unit
@@ -51,19 +73,27 @@ KERNEL_HEADERS = ("csrc/sgemm_ffma.cuh", "csrc/ptx.cuh", "csrc/sgemm_params.h")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_square4096.txt")
 
 
-def tf32_peak_tflops():
-    """Dense TF32 tensor peak: the measured bf16 GEMM peak x the nominal TF32/bf16
-    ratio (1.1 / 2.25 PFLOP/s); the recipe's 1.9 PFLOP/s bf16 when no
-    measurement is present."""
-    basis = "fallback bf16 1900 TFLOP/s"
-    bf16 = 1900.0
+def device_sms(torch, dev) -> int:
+    return int(torch.cuda.get_device_properties(dev).multi_processor_count)
+
+
+def max_sm_mhz(index: int):
+    """(maximum SM clock in MHz, basis) from nvidia-smi, else the fallback."""
     try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            bf16 = float(json.load(f)["bf16_tflops"])
-            basis = f"measured bf16 {bf16:.1f} TFLOP/s"
-    except (OSError, KeyError, ValueError):
+        out = subprocess.run(["nvidia-smi", f"--id={index}", "--query-gpu=clocks.max.sm",
+                              "--format=csv,noheader,nounits"], capture_output=True, text=True,
+                             timeout=20).stdout.strip()
+        v = float(out.splitlines()[0])
+        if v > 0:
+            return v, "nvidia-smi clocks.max.sm"
+    except (OSError, ValueError, IndexError, subprocess.TimeoutExpired):
         pass
-    return bf16 * 1.1 / 2.25, basis + " x 1.1/2.25 (nominal TF32/bf16)"
+    return MAX_MHZ_FALLBACK, "fallback (nvidia-smi unavailable)"
+
+
+def tf32_peak_tflops(sms: int, mhz: float) -> float:
+    """Dense TF32 tensor peak from unit counts: SMs x 4096 FLOP/clk x clock."""
+    return sms * TF32_FLOP_PER_CLK_SM * mhz * 1e6 / 1e12
 
 
 def hbm_peak_gbs():
@@ -76,8 +106,8 @@ def hbm_peak_gbs():
         return 6800.0, "fallback 6800 GB/s"
 
 
-def fp32_peak_tflops(mhz: float) -> float:
-    return SMS * LANES * 2 * mhz * 1e6 / 1e12
+def fp32_peak_tflops(sms: int, mhz: float) -> float:
+    return sms * LANES * 2 * mhz * 1e6 / 1e12
 
 
 def kernel_unit(plan: str) -> str:
@@ -262,6 +292,158 @@ def cpu_baseline(w):
                       f"({rows}x{w.N}x{w.K} multiply-adds, double accumulation), {dt:.1f} s"}
 
 
+def oracle_rate(w, A, B, C, budget_s: float):
+    """The oracle's GFLOP/s (2 FLOP per multiply-add, double accumulation, all
+    host cores) on a leading block of rows sized to take about budget_s."""
+    import oracle
+
+    lda, ldb, ldc = w.lds
+    probe = min(w.M, 4)
+    t0 = time.perf_counter()
+    oracle.sgemm(A[:probe], B, C[:probe], w.alpha, w.beta, M=probe, N=w.N, K=w.K)
+    per_row = max((time.perf_counter() - t0) / probe, 1e-7)
+    rows = int(max(probe, min(w.M, budget_s / per_row)))
+    t0 = time.perf_counter()
+    oracle.sgemm(A[:rows], B, C[:rows], w.alpha, w.beta, M=rows, N=w.N, K=w.K)
+    dt = time.perf_counter() - t0
+    return {"gflops": 2.0 * rows * w.N * w.K / dt / 1e9, "cores": oracle.max_threads(),
+            "rows": rows, "seconds": round(dt, 3)}
+
+
+def e2e_check(w, A, B, C, got):
+    """Sampled entries of an end-to-end result against the oracle (outside the
+    timed region): every 256 x 256 block's corners and a random interior
+    point, plus 64 random entries.  Raises on a violation."""
+    import numpy as np
+
+    import oracle
+
+    rng = np.random.default_rng(w.seed + 101)
+    rows, cols = [], []
+    for i0 in range(0, w.M, 256):
+        for j0 in range(0, w.N, 256):
+            i1, j1 = min(w.M, i0 + 256) - 1, min(w.N, j0 + 256) - 1
+            rows += [i0, i1, int(rng.integers(i0, i1 + 1))]
+            cols += [j0, j1, int(rng.integers(j0, j1 + 1))]
+    rows += list(rng.integers(0, w.M, 64))
+    cols += list(rng.integers(0, w.N, 64))
+    rows, cols = np.array(rows, np.int64), np.array(cols, np.int64)
+    ref, bound, _ = oracle.sgemm_entries(A, B, C, w.alpha, w.beta, rows, cols)
+    bad = oracle.violations(got[rows, cols], ref, bound)
+    if bad.any():
+        raise RuntimeError(f"e2e result: {int(bad.sum())} of {bad.size} sampled entries "
+                           "outside the FP32 bound")
+    return int(bad.size)
+
+
+def time_config(torch, b2g, w, dev, stream, peak, hbm, budget_s):
+    """One workload: back-to-back calls through the C ABI, timed with CUDA
+    events on the launching stream, and the same calls replayed from a CUDA
+    graph (the GPU's own time per call, without the host's launch cost).
+    Calls rotate through enough copies of the operands that every call finds
+    its own out of L2 (at least 2 x L2 between two uses of a copy).  The
+    graph calls pass a caller workspace (b2g_sgemm_ws), so they run the same
+    plan, split tail included, as the stream calls."""
+    import numpy as np
+
+    A, B, C = w.make()
+    lda, ldb, ldc = w.lds
+    nbytes = w.min_bytes()
+    held = 4.0 * (A.size + B.size + C.size)
+    sets = int(max(1, min(2048, -(-2 * L2_BYTES // held))))
+    dA = torch.from_numpy(A).to(dev)
+    dB = torch.from_numpy(B).to(dev)
+    dC0 = torch.from_numpy(C).to(dev)
+    bufA = dA.unsqueeze(0).repeat(sets, 1, 1) if sets > 1 else dA.unsqueeze(0)
+    bufB = dB.unsqueeze(0).repeat(sets, 1, 1) if sets > 1 else dB.unsqueeze(0)
+    bufC = dC0.unsqueeze(0).repeat(sets, 1, 1)
+    ptrs = [(bufA[i].data_ptr(), bufB[i].data_ptr(), bufC[i].data_ptr()) for i in range(sets)]
+    lib = b2g.library()
+    h = stream.cuda_stream
+    alpha, beta = float(w.alpha), float(w.beta)
+    pa, pb, pc = ptrs[0]
+    plan = b2g.b2g_plan_name(b2g.b2g_sgemm_select_plan(0, 0, w.M, w.N, w.K, alpha, pa, lda, pb,
+                                                        ldb, pc, ldc))
+    _, launches = b2g.b2g_sgemm_launch_count(0, 0, w.M, w.N, w.K, alpha, pa, lda, pb, ldb, pc,
+                                             ldc)
+
+    def call(i):
+        a, b, c = ptrs[i % sets]
+        rc = lib.b2g_sgemm(w.M, w.N, w.K, alpha, a, lda, b, ldb, beta, c, ldc, h)
+        if rc:
+            raise b2g.B2GError(rc)
+
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(max(5, sets if sets < 64 else 8)):
+        call(i)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for i in range(5):
+        call(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    est = max(ev0.elapsed_time(ev1) / 5e3, 1e-6)
+    calls = int(max(20, min(4000, budget_s / est)))
+    ev0.record(stream)
+    for i in range(calls):
+        call(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    us = ev0.elapsed_time(ev1) / calls * 1e3
+
+    # the GPU's own time per call: the same calls captured in a CUDA graph
+    rc, wsb = b2g.b2g_sgemm_workspace_size(0, 0, w.M, w.N, w.K, alpha, pa, lda, pb, ldb, pc, ldc)
+    ws = torch.empty(max(int(wsb), 16) // 4 + 64, dtype=torch.float32, device=dev)
+    gcalls = int(max(20, min(400, calls)))
+    graph_us = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                gh = torch.cuda.current_stream().cuda_stream
+                for i in range(gcalls):
+                    a, b, c = ptrs[i % sets]
+                    rc = lib.b2g_sgemm_ws(0, 0, w.M, w.N, w.K, alpha, a, lda, b, ldb, beta, c,
+                                          ldc, ws.data_ptr(), int(wsb), gh)
+                    if rc:
+                        raise b2g.B2GError(rc)
+        stream.wait_stream(side)
+        g.replay()
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        with torch.cuda.stream(stream):
+            g.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        graph_us = ev0.elapsed_time(ev1) / gcalls * 1e3
+        del g
+    except (RuntimeError, b2g.B2GError):
+        graph_us = None
+    del bufA, bufB, bufC, dA, dB, dC0, ws
+
+    ai = w.flops() / nbytes
+    roof = min(peak, ai * hbm / 1e3)
+    tflops = w.flops() / (us * 1e-6) / 1e12
+    out = {
+        "M": w.M, "N": w.N, "K": w.K, "alpha": w.alpha, "beta": w.beta, "seed": w.seed,
+        "lds": list(w.lds), "plan": plan, "launches_per_call": launches,
+        "us_per_call": round(us, 3), "tflops": round(tflops, 3),
+        "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+        "ai_flop_per_byte": round(ai, 2),
+        "bound": "alu" if ai * hbm / 1e3 >= peak else "hbm",
+        "roofline_tflops": round(roof, 3), "frac": round(tflops / roof, 4),
+        "graph_us_per_call": round(graph_us, 3) if graph_us else None,
+        "graph_tflops": round(w.flops() / (graph_us * 1e-6) / 1e12, 3) if graph_us else None,
+        "graph_frac": round(w.flops() / (graph_us * 1e-6) / 1e12 / roof, 4) if graph_us else None,
+        "calls": calls, "operand_sets": sets,
+        "l2": (f"{sets} operand sets rotated ({sets * held / 1e6:.0f} MB)" if sets > 1
+               else f"operands {held / 1e6:.0f} MB > L2, no flush"),
+    }
+    return out, (A, B, C)
+
+
 def run_ours(args, w):
     import numpy as np
     import torch
@@ -280,6 +462,10 @@ def run_ours(args, w):
     build.build()
     b2g.library()
     dev = torch.device("cuda", torch.cuda.current_device())
+    sms = device_sms(torch, dev)
+    max_mhz, mhz_basis = max_sm_mhz(torch.cuda.current_device())
+    peak = fp32_peak_tflops(sms, max_mhz)
+    hpeak, hbasis = hbm_peak_gbs()
 
     A, B, C = w.make()
     hA, hB, hC = (torch.from_numpy(x).pin_memory() for x in (A, B, C))
@@ -355,11 +541,18 @@ def run_ours(args, w):
     for _ in range(3):
         tc_step()
     barrier()
+    tc_sampler = ClockSampler(torch.cuda.current_device())
+    tc_sampler.start()
+    t_end = time.perf_counter() + 0.3  # load long enough for the sampler
+    while time.perf_counter() < t_end:
+        tc_step()
+        torch.cuda.synchronize()
     ev0.record(stream)
     for _ in range(args.steps):
         tc_step()
     ev1.record(stream)
     barrier()
+    tc_clocks = tc_sampler.stop()
     tc_ms = ev0.elapsed_time(ev1) / args.steps
 
     # The skinny workload (M = 16), bound by HBM: reported as GB/s of
@@ -394,11 +587,10 @@ def run_ours(args, w):
     del sk_sets
 
     # end to end through the public API with host buffers: b2g_sgemm_host
-    # copies A, B and C from page-locked host memory, multiplies (row panels
-    # overlapped with the copies) and copies C back, every step; C is updated
-    # in place, so each step starts from the previous step's C
+    # copies A, B and C from page-locked host memory, multiplies (K chunks and
+    # row panels overlapped with the copies) and copies C back, every step; C
+    # is updated in place, so each step starts from the previous step's C
     e2e_steps = max(3, min(args.steps, 20))
-    out = hC
 
     def e2e_step():
         b2g.sgemm_host(hA, hB, hC, w.alpha, w.beta, stream=stream, sync=False)
@@ -412,18 +604,34 @@ def run_ours(args, w):
     ev1.record(stream)
     barrier()
     e2e_ms = max_over_ranks(ev0.elapsed_time(ev1) / e2e_steps, world, dev)
-    # the result of the last step is still correct (spot check of one row)
-    got = out[w.M // 2].numpy()
-    if not np.isfinite(got).all():
-        raise RuntimeError("non-finite output in the e2e check")
+    # outside the timing: one more call from the original C, checked against
+    # the oracle on sampled entries
+    hC.copy_(torch.from_numpy(C))
+    b2g.sgemm_host(hA, hB, hC, w.alpha, w.beta, stream=stream, sync=True)
+    e2e_checked = e2e_check(w, A, B, C, hC.numpy())
 
     rc, flags = b2g.b2g_status(stream.cuda_stream)
     if rc or flags:
         raise RuntimeError(f"kernel status word {flags:#x}")
 
+    # every configuration of the workload list, each with the oracle beside it
+    configs = {}
+    if not args.no_configs:
+        for name, cw in workloads.WORKLOADS.items():
+            entry, (cA, cB, cC) = time_config(torch, b2g, cw, dev, stream, peak, hpeak,
+                                              args.config_seconds)
+            if rank == 0 and not args.no_cpu_baseline:
+                entry["oracle"] = oracle_rate(cw, cA, cB, cC, args.oracle_seconds)
+                entry["gpu_over_oracle"] = round(entry["tflops"] * 1e3
+                                                 / entry["oracle"]["gflops"], 1)
+            configs[name] = entry
+            del cA, cB, cC
+        rc, flags = b2g.b2g_status(stream.cuda_stream)
+        if rc or flags:
+            raise RuntimeError(f"kernel status word {flags:#x}")
+
     if rank == 0:
         achieved = w.flops() / (kernel_ms * 1e-3) / 1e12
-        peak = fp32_peak_tflops(MAX_MHZ)
         traffic = recorded_traffic(kernel_plan)
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -439,25 +647,33 @@ def run_ours(args, w):
                                                   else ""),
                          "kernel_ms": kernel_ms, "kernel_launches": kernel_launches,
                          "step_frac": value / world / peak,
-                         "peak_basis": "152 SMs x 128 FP32 FMA/clk x 2 x 2070 MHz (derived)",
-                         "frac_at_sampled_clock": (achieved / fp32_peak_tflops(clocks["sm_mhz"])
+                         "peak_basis": (f"{sms} SMs (device) x {LANES} FP32 FMA/clk x 2 x "
+                                        f"{max_mhz:.0f} MHz ({mhz_basis}), derived"),
+                         "frac_at_sampled_clock": (achieved / fp32_peak_tflops(sms, clocks["sm_mhz"])
                                                    if clocks else None)},
             "e2e": {"value": job_throughput(w.flops(), world, e2e_ms) / 1e12, "unit": UNIT,
                     "h2d_bytes_per_step": int(hA.numel() + hB.numel() + hC.numel()) * 4,
-                    "d2h_bytes_per_step": int(out.numel()) * 4},
+                    "d2h_bytes_per_step": int(hC.numel()) * 4,
+                    "checked": f"{e2e_checked} sampled entries against the oracle, in bound"},
             "gpu_launches": args.steps * launches_per_step,
             "clocks": clocks,
         }
-        tpeak, tbasis = tf32_peak_tflops()
+        tpeak = tf32_peak_tflops(sms, max_mhz)
         tc_tensor = 3 * w.flops() / (tc_ms * 1e-3) / 1e12  # three TF32 products per term
         line["tf32x3"] = {
             "value": w.flops() / (tc_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": tc_ms,
             "launches_per_step": 4, "path": "b2g_sgemm_3xtf32 (2 split kernels + tcgen05 GEMM on CTA pairs, 256 x 256 tiles + split-tail reduction)",
             "accuracy": "same elementwise FP32 bound as the FFMA path",
+            "clocks": tc_clocks,
             "roofline": {"bound": "tensor", "achieved": tc_tensor, "peak": tpeak, "unit": UNIT,
-                         "frac": tc_tensor / tpeak, "peak_basis": tbasis},
+                         "frac": tc_tensor / tpeak,
+                         "peak_basis": (f"{sms} SMs x {TF32_FLOP_PER_CLK_SM} dense TF32 FLOP/clk "
+                                        f"x {max_mhz:.0f} MHz, derived from unit counts; "
+                                        "cuBLAS TF32 (one product) measured 1101 TFLOP/s at "
+                                        "8192^3 on this GPU model, below it"),
+                         "frac_at_sampled_clock": (tc_tensor / tf32_peak_tflops(
+                             sms, tc_clocks["sm_mhz"]) if tc_clocks else None)},
         }
-        hpeak, hbasis = hbm_peak_gbs()
         sk_gbs = sk.min_bytes() / (sk_ms * 1e-3) / 1e9
         line["skinny"] = {
             "workload": sk.name, "M": sk.M, "N": sk.N, "K": sk.K, "alpha": sk.alpha,
@@ -468,6 +684,13 @@ def run_ours(args, w):
                          "frac": sk_gbs / hpeak, "algorithmic_bytes": sk.min_bytes(),
                          "peak_basis": hbasis},
         }
+        if configs:
+            line["configs"] = configs
+            line["configs_note"] = (
+                "per workload: us_per_call = back-to-back calls through the C ABI (CUDA events "
+                "on the launching stream); graph_us_per_call = the same calls replayed from a "
+                "CUDA graph (GPU time without host launch cost); frac against min(FP32 peak, "
+                f"AI x {hpeak:.0f} GB/s); oracle = CPU oracle GFLOP/s on a leading row block")
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(w)
         print(json.dumps(line), flush=True)
@@ -483,6 +706,12 @@ def main():
     ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
     ap.add_argument("--workload", default=workloads.HEADLINE, choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-workload table (configs object)")
+    ap.add_argument("--config-seconds", type=float, default=0.25,
+                    help="GPU time per workload in the configs table (about)")
+    ap.add_argument("--oracle-seconds", type=float, default=1.0,
+                    help="oracle time per workload in the configs table (about)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

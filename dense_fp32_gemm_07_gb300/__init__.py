@@ -40,7 +40,8 @@ EXPORTS = (
     "b2g_sgemm_ws", "b2g_sgemm_workspace_size", "b2g_sgemm_launch_count", "b2g_sgemm_host",
     "b2g_release_workspaces", "b2g_sgemm_noalloc",
     "b2g_sgemm_3xtf32", "b2g_sgemm_3xtf32_variant", "b2g_sgemm_strided_batched",
-    "b2g_plan_count", "b2g_plan_name", "b2g_plan_info", "b2g_status", "b2g_set_wait_limit_ns",
+    "b2g_plan_count", "b2g_plan_name", "b2g_plan_info", "b2g_status", "b2g_sgemm_debug_status",
+    "b2g_set_wait_limit_ns",
     "b2g_debug_stop_after", "b2g_strerror", "b2g_version",
 )
 
@@ -90,6 +91,7 @@ def _load():
         lib.b2g_plan_name.restype = ctypes.c_char_p
         lib.b2g_plan_info.argtypes = [i, ctypes.POINTER(ctypes.c_int)]
         lib.b2g_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint), i]
+        lib.b2g_sgemm_debug_status.argtypes = [vp]
         lib.b2g_set_wait_limit_ns.argtypes = [u64]
         lib.b2g_debug_stop_after.argtypes = [i]
         lib.b2g_strerror.argtypes = [i]
@@ -299,6 +301,12 @@ def b2g_status(stream=0, clear: bool = True):
     flags = ctypes.c_uint(0)
     rc = _load().b2g_status(stream, ctypes.byref(flags), int(clear))
     return rc, flags.value
+
+
+def b2g_sgemm_debug_status(stream=0) -> int:
+    """Timeout flags of the status word (>= 0, not cleared) or a negative code;
+    synchronises `stream`."""
+    return _load().b2g_sgemm_debug_status(stream)
 
 
 def b2g_set_wait_limit_ns(ns: int) -> int:

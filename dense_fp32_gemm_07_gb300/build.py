@@ -2,12 +2,16 @@
 
 Each translation unit is compiled in parallel with nvcc, then linked into one
 shared library with the CUDA runtime linked statically.  `-Xptxas -v` output
-(registers, spills, shared memory per kernel) is kept in build/ptxas_<tu>.log.
+(registers, spills, shared memory per kernel) is kept in build/ptxas_<tu>.log,
+and the build fails when ptxas reports a register spill in any kernel: the
+packed FFMA kernels are capped at 128 registers to keep three CTAs per SM, and
+a spill there would otherwise show up only as a quiet loss of speed.
 """
 from __future__ import annotations
 
 import concurrent.futures as cf
 import os
+import re
 import shutil
 import subprocess
 import sys
@@ -46,6 +50,25 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
+_SPILL = re.compile(r"(\d+) bytes spill stores, (\d+) bytes spill loads")
+_ENTRY = re.compile(r"Function properties for (\S+)")
+
+
+def spills(log_text: str):
+    """[(function, spill store bytes, spill load bytes)] for every function
+    whose ptxas report shows a spill."""
+    out, fn = [], None
+    for line in log_text.splitlines():
+        m = _ENTRY.search(line)
+        if m:
+            fn = m.group(1)
+            continue
+        m = _SPILL.search(line)
+        if m and (int(m.group(1)) or int(m.group(2))):
+            out.append((fn, int(m.group(1)), int(m.group(2))))
+    return out
+
+
 def _compile(src: str) -> str:
     obj = os.path.join(BUILD, src[:-3] + ".o")
     log = os.path.join(BUILD, f"ptxas_{src[:-3]}.log")
@@ -55,6 +78,11 @@ def _compile(src: str) -> str:
         f.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed on {src}:\n{r.stderr[-4000:]}")
+    bad = spills(r.stdout + r.stderr)
+    if bad:
+        os.remove(obj)
+        raise RuntimeError(f"ptxas reports register spills in {src}: " +
+                           "; ".join(f"{f}: {st} B stored, {ld} B loaded" for f, st, ld in bad))
     return obj
 
 

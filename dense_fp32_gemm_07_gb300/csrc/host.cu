@@ -1119,6 +1119,13 @@ int b2g_status(void* stream, unsigned int* flags, int clear) {
   return v ? B2G_ERR_TIMEOUT : 0;
 }
 
+int b2g_sgemm_debug_status(void* stream) {
+  unsigned int flags = 0;
+  const int rc = b2g_status(stream, &flags, 0);
+  if (rc && rc != B2G_ERR_TIMEOUT) return rc;
+  return (int)(flags & 0x7fffffffu);
+}
+
 int b2g_set_wait_limit_ns(unsigned long long ns) {
   if (ns == 0) return B2G_ERR_INVALID_DIM;
   g_wait_limit_ns.store(ns);

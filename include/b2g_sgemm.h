@@ -205,10 +205,18 @@ int b2g_release_workspaces(void);
  * (A^T for the plans that transpose A first, then the split tail's partial
  * sums when they fit) is a fixed 64 MiB array that every device loading the
  * library holds until the process exits.
- *   - Calls whose A^T, K x round_up(M, 4) floats for those plans,
- *     exceeds 64 MiB (16,777,216 floats) are rejected with
- *     B2G_ERR_SCRATCH_LIMIT and launch nothing; use b2g_sgemm_ws with your own
- *     buffer for them.
+ *   - A call is rejected with B2G_ERR_SCRATCH_LIMIT, launching nothing, when
+ *     the scratch its tune-table plan cannot do without exceeds 64 MiB
+ *     (16,777,216 floats).  That scratch is: A^T, K x round_up(M, 4) floats,
+ *     for the plans that transpose A first (aligned operands, M*N*K >= 1e9);
+ *     A^T plus an aligned copy of B, K x (round_up(M, 4) + round_up(N, 4))
+ *     floats, for the packing plans (a misaligned pointer, lda or ldb not a
+ *     multiple of 4, or K % 4 != 0, with M*N*K >= 5e7); the k slabs' partial
+ *     sums, S x M x N floats with S <= K / 64, for the skinny split-K plans
+ *     with M <= 32 and N < 2048 (at most about 20 MB on a 152-SM GPU);
+ *     nothing otherwise.  The split tail's partial
+ *     sums are optional: they use the room left, else the plan runs without
+ *     its split.  Use b2g_sgemm_ws with your own buffer for rejected calls.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call
  *     before capturing any stream.
@@ -263,6 +271,19 @@ int b2g_plan_info(int plan, int* info);
  * word.  Returns 0, B2G_ERR_TIMEOUT when a flag is set, or B2G_ERR_CUDA.
  */
 int b2g_status(void* stream, unsigned int* flags, int clear);
+
+/*
+ * The same status word as a return value, without clearing it: synchronises
+ * `stream`, then returns the flags (0 when no bounded wait has run out since
+ * the word was last cleared, else the bit set described at b2g_status), or a
+ * negative B2G_ERR_* code when the current device is unusable or the word
+ * cannot be read.  Exported in every build (the word is only written when a
+ * wait gives up, so reading it costs the normal path nothing).  After a
+ * reported timeout the C of the call that timed out is undefined: tiles whose
+ * consumers gave up were not written, and a split tail may have added partial
+ * sums that were never finished.
+ */
+int b2g_sgemm_debug_status(void* stream);
 
 /*
  * Upper bound, in nanoseconds of GPU wall time, on every mbarrier wait inside

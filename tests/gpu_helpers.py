@@ -8,6 +8,29 @@ import oracle
 
 SENTINEL = np.float32(np.nan)
 
+# Full-size workloads checked by several test files: their inputs and oracle
+# result are computed once per test process (the 4096^3 oracle takes ~4 s on
+# 16 cores, 8192 x 11008 x 4096 ~22 s) and kept for the later files.
+_SHARED = ("square4096", "mlp8192x11008x4096")
+_REF_CACHE = {}
+
+
+def workload_reference(name):
+    """(workload, A, B, C, ref, bound) for a named workload: the seeded inputs
+    and the oracle's result and error budget for EVERY output element."""
+    import workloads
+
+    hit = _REF_CACHE.get(name)
+    if hit is not None:
+        return hit
+    w = workloads.WORKLOADS[name]
+    A, B, C = w.make()
+    ref, bound, _ = oracle.sgemm(A, B, C, w.alpha, w.beta, M=w.M, N=w.N, K=w.K)
+    out = (w, A, B, C, ref, bound)
+    if name in _SHARED:
+        _REF_CACHE[name] = out
+    return out
+
 
 def env():
     import torch

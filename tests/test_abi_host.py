@@ -238,6 +238,20 @@ def test_no_gpu_means_loud_failure(b2g):
     assert rc == b2g.B2G_ERR_DEVICE
 
 
+def test_debug_status_without_device(b2g):
+    """b2g_sgemm_debug_status returns the status word's flags (>= 0) or a
+    negative code; with no usable device it is the device error, never a
+    flag value."""
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert b2g.b2g_sgemm_debug_status(0) == b2g.B2G_ERR_DEVICE
+    lib = ctypes.CDLL(b2g.LIB_PATH)
+    lib.b2g_sgemm_debug_status.argtypes = [ctypes.c_void_p]
+    assert lib.b2g_sgemm_debug_status(None) == b2g.B2G_ERR_DEVICE
+
+
 def test_tensor_api_rejects_cpu_tensors(b2g):
     import torch
 
@@ -286,3 +300,20 @@ def test_colmajor_leading_dims(b2g, tA, tB, M, N, K, lda, ldb, ldc, code):
                                          ldc) >= 0
         assert b2g.b2g_sgemm_colmajor(tA, tB, 0, N, K, 1.0, None, lda, None, ldb, 0.0, None,
                                       ldc, 0) == 0
+
+
+def test_build_rejects_register_spills():
+    """build.spills() finds ptxas's spill report per function, so a kernel that
+    starts spilling fails the build; the current build has none."""
+    from dense_fp32_gemm_07_gb300 import build
+
+    log = ("ptxas info    : Function properties for _Z3fooPf\n"
+           "    0 bytes stack frame, 0 bytes spill stores, 0 bytes spill loads\n"
+           "ptxas info    : Function properties for _Z3barPf\n"
+           "    32 bytes stack frame, 36 bytes spill stores, 44 bytes spill loads\n")
+    assert build.spills(log) == [("_Z3barPf", 36, 44)]
+    build.build()
+    for src in build.sources():
+        path = os.path.join(build.BUILD, f"ptxas_{src[:-3]}.log")
+        if os.path.exists(path):
+            assert build.spills(open(path).read()) == [], src

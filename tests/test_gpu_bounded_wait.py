@@ -41,9 +41,14 @@ def test_wait_runs_out_and_context_survives(tb, plan_name, M, N, K):
         rc = b2g.b2g_sgemm_with_plan(plan, 0, 0, M, N, K, 1.0, dA.data_ptr(), K,
                                      dB.data_ptr(), N, 0.0, dC.data_ptr(), N, stream)
         assert rc == 0
+        # the debug read returns the same flags and leaves them set
+        dbg = b2g.b2g_sgemm_debug_status(stream)
+        assert dbg > 0 and dbg & 1, f"debug status {dbg}"
         rc, flags = b2g.b2g_status(stream, clear=True)
         assert rc == b2g.B2G_ERR_TIMEOUT
         assert flags & 1, f"consumer timeout flag missing: {flags:#x}"
+        assert flags == dbg
+        assert b2g.b2g_sgemm_debug_status(stream) == 0
     finally:
         b2g.b2g_debug_stop_after(-1)
         b2g.b2g_set_wait_limit_ns(2_000_000_000)

@@ -5,8 +5,7 @@ import numpy as np
 import pytest
 
 import oracle
-import workloads
-from gpu_helpers import check, env, sample_entries
+from gpu_helpers import check, env, workload_reference
 
 pytestmark = pytest.mark.gpu
 
@@ -82,16 +81,14 @@ def test_consecutive_calls_and_stream_order(tb):
         check(hC.numpy(), ref, bound, f"call {seed}")
 
 
-def test_square4096_sampled(tb):
+def test_square4096_full(tb):
+    """The bench's e2e workload through b2g_sgemm_host (three K chunks, the
+    last in row panels), every output element against the oracle."""
     torch, b2g = tb
-    w = workloads.WORKLOADS["square4096"]
-    A, B, C = w.make()
+    w, A, B, C, ref, bound = workload_reference("square4096")
     hA, hB, hC = (torch.from_numpy(x).pin_memory() for x in (A, B, C))
     b2g.sgemm_host(hA, hB, hC, w.alpha, w.beta)
-    rows, cols = sample_entries(w.M, w.N, seed=w.seed)
-    got = hC.numpy()[rows, cols]
-    ref, bound, _ = oracle.sgemm_entries(A, B, C, w.alpha, w.beta, rows, cols)
-    check(got, ref, bound, "square4096 host")
+    check(hC.numpy(), ref, bound, "square4096 host")
 
 
 @pytest.mark.parametrize("shape,beta", [((1100, 300, 2100), 0.5), ((2100, 300, 2052), -1.0),

@@ -12,7 +12,7 @@ import pytest
 
 import oracle
 import workloads
-from gpu_helpers import check, env, gemm, sample_entries
+from gpu_helpers import check, env, gemm, workload_reference
 
 pytestmark = pytest.mark.gpu
 
@@ -24,7 +24,7 @@ def tb():
 
 FULL = ["square512", "ragged1000x1025x777", "sweep128", "sweep256", "sweep512", "sweep1024",
         "skinny16x4096x4096"]
-SAMPLED = ["square4096", "sweep2048", "sweep4096", "sweep8192", "mlp8192x11008x4096"]
+FULL_SIZE = ["square4096", "sweep2048", "sweep4096", "sweep8192", "mlp8192x11008x4096"]
 
 
 @pytest.mark.parametrize("name", FULL)
@@ -39,23 +39,19 @@ def test_workload_full(tb, name):
     check(got, ref, bound, name)
 
 
-@pytest.mark.parametrize("name", SAMPLED)
-def test_workload_sampled(tb, name):
-    """Full-size problems in the launch configuration the bench times (the tune
-    table's plan, device-resident operands); the oracle computes a sample of
-    entries covering every 128 x 128 tile, its corners and the last row/column."""
+@pytest.mark.parametrize("name", FULL_SIZE)
+def test_workload_full_size(tb, name):
+    """The large workloads in the launch configuration the bench times (the
+    tune table's plan with its transpose and split tail, device-resident
+    contiguous operands), every output element against the oracle."""
     torch, b2g = tb
-    w = workloads.WORKLOADS[name]
-    A, B, C = w.make()
+    w, A, B, C, ref, bound = workload_reference(name)
     dA = torch.from_numpy(A).cuda()
     dB = torch.from_numpy(B).cuda()
     dC = torch.from_numpy(C).cuda()
     b2g.sgemm(dA, dB, dC, w.alpha, w.beta)
     torch.cuda.synchronize()
-    rows, cols = sample_entries(w.M, w.N, seed=w.seed)
-    got = dC[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()].cpu().numpy()
-    ref, bound, _ = oracle.sgemm_entries(A, B, C, w.alpha, w.beta, rows, cols)
-    check(got, ref, bound, name)
+    check(dC.cpu().numpy(), ref, bound, name)
 
 
 SHAPES = [(1, 1, 4), (1, 37, 8), (37, 1, 12), (5, 7, 3), (37, 45, 52), (130, 257, 68),

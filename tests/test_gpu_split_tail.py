@@ -8,7 +8,6 @@ import numpy as np
 import pytest
 
 import oracle
-import workloads
 from gpu_helpers import check, env, gemm
 
 pytestmark = pytest.mark.gpu
@@ -108,42 +107,3 @@ def test_batched_split(tb):
     for b in range(batch):
         ref, bound, _ = oracle.sgemm(A[b], B[b], C[b], 0.5, 1.5)
         check(got[b], ref, bound, f"problem {b}")
-
-
-def tile_order(tiles_m, tiles_n, group_m=8):
-    """(tm, tn) of every output tile in the persistent loop's order: down a
-    group of group_m tile rows, then one tile column right."""
-    out = []
-    for t in range(tiles_m * tiles_n):
-        per_group = group_m * tiles_n
-        g, r = divmod(t, per_group)
-        first_m = g * group_m
-        gsize = min(tiles_m - first_m, group_m)
-        out.append((first_m + r % gsize, r // gsize))
-    return out
-
-
-def test_square4096_last_tiles_sampled(tb):
-    """The bench workload: entries of the last quarter of the tiles in
-    scheduler order (the split tail is among them) against the oracle."""
-    torch, b2g = tb
-    w = workloads.WORKLOADS["square4096"]
-    A, B, C = w.make()
-    pi = b2g.b2g_sgemm_select_plan(0, 0, w.M, w.N, w.K, w.alpha, FAKE, w.K, FAKE, w.N, FAKE, w.N)
-    info = b2g.b2g_plan_info(pi)
-    BM, BN = info["BM"], info["BN"]
-    order = tile_order(-(-w.M // BM), -(-w.N // BN))
-    last = order[-len(order) // 4:]
-    rng = np.random.default_rng(2)
-    rows, cols = [], []
-    for tm, tn in last:
-        for _ in range(2):
-            rows.append(tm * BM + int(rng.integers(0, BM)))
-            cols.append(tn * BN + int(rng.integers(0, BN)))
-    rows, cols = np.array(rows), np.array(cols)
-    dA, dB, dC = (torch.from_numpy(x).cuda() for x in (A, B, C))
-    b2g.sgemm(dA, dB, dC, w.alpha, w.beta)
-    torch.cuda.synchronize()
-    got = dC[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()].cpu().numpy()
-    ref, bound, _ = oracle.sgemm_entries(A, B, C, w.alpha, w.beta, rows, cols)
-    check(got, ref, bound, "square4096 last tiles")

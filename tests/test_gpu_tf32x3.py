@@ -2,14 +2,13 @@
 the same elementwise FP32 bound as the FFMA path, for both tensor-core kernels:
 variant 0 (one CTA per 128 x 128 tile), variant 1 (a CTA pair per 256 x 128
 tile, tcgen05.mma.cta_group::2) and variant 2 (a CTA pair per 256 x 256 tile)."""
-import ctypes
 
 import numpy as np
 import pytest
 
 import oracle
 import workloads
-from gpu_helpers import check, env, sample_entries
+from gpu_helpers import check, env, workload_reference
 
 pytestmark = pytest.mark.gpu
 
@@ -84,18 +83,17 @@ def test_workloads_full(tb, name, variant):
 
 
 @pytest.mark.parametrize("name", ["square4096", "mlp8192x11008x4096"])
-@pytest.mark.parametrize("variant", VARIANTS)
-def test_workloads_sampled(tb, name, variant):
+@pytest.mark.parametrize("variant", [None] + VARIANTS)
+def test_workloads_full_size(tb, name, variant):
+    """Full-size workloads on every kernel variant and on the default choice
+    (the 256 x 256 CTA pair with its split tail at these sizes), every output
+    element against the oracle."""
     torch, b2g = tb
-    w = workloads.WORKLOADS[name]
-    A, B, C = w.make()
+    w, A, B, C, ref, bound = workload_reference(name)
     dA, dB, dC = (torch.from_numpy(x).cuda() for x in (A, B, C))
     b2g.sgemm_3xtf32(dA, dB, dC, w.alpha, w.beta, variant=variant)
     torch.cuda.synchronize()
-    rows, cols = sample_entries(w.M, w.N, seed=w.seed)
-    got = dC[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()].cpu().numpy()
-    ref, bound, _ = oracle.sgemm_entries(A, B, C, w.alpha, w.beta, rows, cols)
-    check(got, ref, bound, name)
+    check(dC.cpu().numpy(), ref, bound, f"{name} variant {variant}")
 
 
 def test_unsupported_operands(tb):

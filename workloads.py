@@ -23,8 +23,10 @@ All matrices are row-major float32.  ``ld`` values default to the row width.
 """
 from __future__ import annotations
 
+import concurrent.futures
 import dataclasses
 import math
+import os
 from typing import Dict, Optional, Tuple
 
 import numpy as np
@@ -50,32 +52,65 @@ def stream_key(seed: int, stream: int) -> np.uint64:
     return _mix64(np.array([base], dtype=np.uint64))[0]
 
 
+def _bits(key: np.uint64, start: int, count: int) -> np.ndarray:
+    """The 24-bit draws ``x_i >> 40`` of stream key ``key`` for i in
+    [start, start + count), as uint32 (one chunk, one thread)."""
+    idx = np.arange(start + 1, start + count + 1, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        z = key + idx * _GAMMA
+    return (_mix64(z) >> np.uint64(40)).astype(np.uint32)
+
+
+def _chunked(count: int, step: int, fill) -> None:
+    """Call fill(lo, hi) over [0, count) in chunks of ``step``.  Element i of a
+    stream depends only on i (the generator is counter-based), so the chunks
+    run on a thread pool (numpy releases the interpreter lock in its array
+    loops) and the values do not depend on the chunking.  The pool lives only
+    for this call, so a process forked later inherits no worker threads."""
+    spans = [(lo, min(count, lo + step)) for lo in range(0, count, step)]
+    if len(spans) <= 1:
+        for lo, hi in spans:
+            fill(lo, hi)
+        return
+    workers = max(1, min(len(spans), os.cpu_count() or 1, 32))
+    with concurrent.futures.ThreadPoolExecutor(max_workers=workers) as ex:
+        for f in [ex.submit(fill, lo, hi) for lo, hi in spans]:
+            f.result()
+
+
 def raw_bits(seed: int, stream: int, start: int, count: int) -> np.ndarray:
     """The 24-bit draws ``x_i >> 40`` for i in [start, start + count) as uint32."""
     key = stream_key(seed, stream)
     out = np.empty(count, dtype=np.uint32)
-    for lo in range(0, count, _CHUNK):
-        hi = min(count, lo + _CHUNK)
-        idx = np.arange(start + lo + 1, start + hi + 1, dtype=np.uint64)
-        with np.errstate(over="ignore"):
-            z = key + idx * _GAMMA
-        out[lo:hi] = (_mix64(z) >> np.uint64(40)).astype(np.uint32)
+
+    def fill(lo, hi):
+        out[lo:hi] = _bits(key, start + lo, hi - lo)
+
+    _chunked(count, _CHUNK, fill)
     return out
 
 
 def uniform_pm1(seed: int, stream: int, count: int) -> np.ndarray:
     """``count`` float32 values in [-1, 1), each an exact multiple of 2**-23."""
-    j = raw_bits(seed, stream, 0, count).astype(np.int64) - (1 << 23)
-    return (j.astype(np.float64) * 2.0 ** -23).astype(np.float32)
+    key = stream_key(seed, stream)
+    out = np.empty(count, dtype=np.float32)
+
+    def fill(lo, hi):
+        j = _bits(key, lo, hi - lo).astype(np.int64) - (1 << 23)
+        out[lo:hi] = (j.astype(np.float64) * 2.0 ** -23).astype(np.float32)
+
+    _chunked(count, _CHUNK, fill)
+    return out
 
 
 def normal(seed: int, stream: int, count: int, mean: float = 0.0, std: float = 1.0) -> np.ndarray:
     """``count`` float32 normal(mean, std) draws by Box-Muller on draw pairs."""
+    key = stream_key(seed, stream)
     pairs = (count + 1) // 2
     out = np.empty(2 * pairs, dtype=np.float32)
-    for lo in range(0, pairs, _CHUNK):
-        hi = min(pairs, lo + _CHUNK)
-        bits = raw_bits(seed, stream, 2 * lo, 2 * (hi - lo)).astype(np.float64)
+
+    def fill(lo, hi):  # pairs lo .. hi-1, draws 2*lo .. 2*hi-1
+        bits = _bits(key, 2 * lo, 2 * (hi - lo)).astype(np.float64)
         u1 = (bits[0::2] + 1.0) * 2.0 ** -24
         u2 = bits[1::2] * 2.0 ** -24
         r = np.sqrt(-2.0 * np.log(u1))
@@ -84,6 +119,8 @@ def normal(seed: int, stream: int, count: int, mean: float = 0.0, std: float = 1
         blk[0::2] = r * np.cos(t)
         blk[1::2] = r * np.sin(t)
         out[2 * lo:2 * hi] = (mean + std * blk).astype(np.float32)
+
+    _chunked(pairs, _CHUNK, fill)
     return out[:count]
 
 
