@@ -69,7 +69,7 @@ L2_BYTES = 129e6
 # device code of the dominant kernel: a change here voids the recorded traffic
 # The recorded traffic is valid while these headers and the translation unit
 # that compiles the plan's kernel are unchanged.
-KERNEL_HEADERS = ("csrc/sgemm_ffma.cuh", "csrc/ptx.cuh", "csrc/sgemm_params.h")
+KERNEL_HEADERS = ("csrc/sgemm_ffma.cuh", "csrc/ptx.cuh", "csrc/sgemm_params.h", "csrc/tcgen05.cuh")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_square4096.txt")
 
 

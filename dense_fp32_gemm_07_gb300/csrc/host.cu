@@ -185,6 +185,7 @@ const PlanGroup kGroups[] = {
     {kPlansT64x128k32, &kNumPlansT64x128k32},
     {kPlansT128x128, &kNumPlansT128x128}, {kPlansGeneral, &kNumPlansGeneral},
     {kPlansSkinny, &kNumPlansSkinny},     {kPlansSkinnyTma, &kNumPlansSkinnyTma},
+    {kPlansCs, &kNumPlansCs},
 };
 
 int num_plans() {
@@ -249,7 +250,8 @@ bool needs_gemm(const Call& c) {
 int operand_class(const Call& c) {
   const bool ab_aligned = aligned16(c.A) && aligned16(c.B) && c.lda % 4 == 0 && c.ldb % 4 == 0 &&
                           (c.batch <= 1 || (c.strideA % 4 == 0 && c.strideB % 4 == 0));
-  if (!ab_aligned || c.transB) return kClassGeneral;
+  if (!ab_aligned) return kClassGeneral;
+  if (c.transB) return c.K % 4 == 0 ? kClassFastTransB : kClassGeneral;
   if (c.transA) return kClassFastTransA;
   return c.K % 4 == 0 ? kClassFast : kClassGeneral;
 }
@@ -261,6 +263,7 @@ bool plan_accepts(const Plan& pl, const Call& c) {
     return cls == kClassFast && c.M <= pl.BM && c.N % 4 == 0 && c.batch <= 65535;
   if (pl.pretranspose == 2) return true;  // packing accepts any operands
   if (pl.pretranspose == 1) return cls == kClassFast;
+  if (pl.pretranspose == 3) return cls == kClassFastTransB;
   if (pl.feed == kFeedTMATrans || pl.alayout == kAKChunk) return cls == kClassFast;
   return cls == kClassFastTransA;
 }
@@ -276,6 +279,7 @@ const char* const kTileTwins[][2] = {
     {"pre_128x64x32_s3_o5", "pre_64x128x32_s3_o5"},
     {"tmaT_128x64x32_s3_o5", "tmaT_64x128x32_s3_o5"},
     {"pack_128x64x32_s3_o5", "pack_64x128x32_s3_o5"},
+    {"pret_128x64x32_s3_o5", "pret_64x128x32_s3_o5"},
 };
 
 int select_plan(const Call& c, int* fallback = nullptr) {
@@ -355,7 +359,7 @@ constexpr int kMinSliceK = 64;
 
 int tail_split(const Plan& pl, const Call& c, int* first) {
   *first = 0;
-  if (is_skinny(pl) || !pl.occupancy) return 1;
+  if (is_skinny(pl) || !pl.occupancy || pl.cluster_max) return 1;
   const long long tiles =
       (long long)((c.M + pl.BM - 1) / pl.BM) * ((c.N + pl.BN - 1) / pl.BN) * c.batch;
   int sms = 0, occ = 0;
@@ -369,6 +373,22 @@ int tail_split(const Plan& pl, const Call& c, int* first) {
   if (S > smax) S = smax;
   if (S < 2) return 1;
   *first = (int)(q * G);
+  return (int)S;
+}
+
+// k slices per tile of a cluster-split plan: as many as fill the resident CTA
+// slots once (S = slots / tiles), at most the plan's largest cluster, and at
+// least two k stages per slice.
+int cs_splits(const Plan& pl, const Call& c) {
+  const long long tiles =
+      (long long)((c.M + pl.BM - 1) / pl.BM) * ((c.N + pl.BN - 1) / pl.BN) * c.batch;
+  int sms = 0, occ = 0;
+  plan_capacity(pl, &sms, &occ);
+  long long S = tiles > 0 ? (long long)sms * occ / tiles : 1;
+  const long long k_tiles = (c.K + pl.BK - 1) / pl.BK;
+  if (S > pl.cluster_max) S = pl.cluster_max;
+  if (S > k_tiles / 2) S = k_tiles / 2;
+  if (S < 1) S = 1;
   return (int)S;
 }
 
@@ -410,6 +430,8 @@ size_t plan_base_bytes(const Plan& pl, const Call& c) {
   if (pl.pretranspose == 1) return nb * (size_t)c.K * (size_t)pre_ld(c.M) * sizeof(float);
   if (pl.pretranspose == 2)
     return nb * (size_t)c.K * (size_t)(pre_ld(c.M) + pre_ld(c.N)) * sizeof(float);
+  if (pl.pretranspose == 3)  // B^T transposed, and A unless it comes stored K x M
+    return nb * (size_t)c.K * (size_t)((c.transA ? 0 : pre_ld(c.M)) + pre_ld(c.N)) * sizeof(float);
   if (pl.feed == kFeedSkinny) {  // partial sums per k slab (the cluster plans keep them on chip)
     int kc = 0;
     const int S = skinny_splits(pl, c, &kc);
@@ -573,6 +595,8 @@ int run(const Call& c, int forced_plan, void* stream, void* user_ws = nullptr,
   } else if (pl->feed == kFeedSkinny && ws) {
     p.splits = skinny_splits(*pl, c, &p.kc);
     p.work = ws;
+  } else if (pl->cluster_max) {  // k slices summed inside clusters: no workspace
+    p.tail_first = 0, p.tail_splits = cs_splits(*pl, c);
   } else if (ws && tail_S > 1) {
     p.tail_first = tail_first, p.tail_splits = tail_S;
     p.work = ws + tail_offset(base) / sizeof(float);
@@ -592,6 +616,21 @@ int run(const Call& c, int forced_plan, void* stream, void* user_ws = nullptr,
                      pack_job(c.B, c.ldb, c.transB ? 1 : 0, c.K, c.N, Bp, ldbp, c.strideB, sbp),
                      st, c.batch);
     p.A = At, p.lda = ldat, p.transA = 1, p.strideA = sat;
+    p.B = Bp, p.ldb = ldbp, p.transB = 0, p.strideB = sbp;
+  } else if (ws && pl->pretranspose == 3) {
+    // B stored N x K -> Bp (K x ldbp), and row-major A -> At (K x ldat), both
+    // with 16-byte vectors; A stored K x M is read in place
+    const long long ldbp = pre_ld(c.N), sbp = (long long)c.K * ldbp;
+    float* Bp = ws;
+    if (!c.transA) {
+      const long long ldat = pre_ld(c.M), sat = (long long)c.K * ldat;
+      float* At = ws;
+      Bp = ws + (size_t)c.batch * sat;
+      e = launch_transpose_a(c.A, c.M, c.K, c.lda, At, ldat, st, c.batch, c.strideA, sat);
+      p.A = At, p.lda = ldat, p.transA = 1, p.strideA = sat;
+    }
+    if (e == cudaSuccess)
+      e = launch_transpose_a(c.B, c.N, c.K, c.ldb, Bp, ldbp, st, c.batch, c.strideB, sbp);
     p.B = Bp, p.ldb = ldbp, p.transB = 0, p.strideB = sbp;
   }
 
@@ -613,7 +652,7 @@ int run(const Call& c, int forced_plan, void* stream, void* user_ws = nullptr,
     pA = &tmA, pB = &tmB;
   }
   if (e == cudaSuccess && !rc) e = pl->launch(p, pA, pB, d->sms, st);
-  if (e == cudaSuccess && !rc && p.tail_splits > 1)
+  if (e == cudaSuccess && !rc && p.tail_splits > 1 && !pl->cluster_max)
     e = launch_tail_reduce(p, pl->BM, pl->BN, st);
   if (auto_ws) ws_release(dev, st);
   if (rc) return rc;
@@ -1019,11 +1058,12 @@ int b2g_sgemm_launch_count(int transA, int transB, int M, int N, int K, float al
   }
   const Plan* pl = plan_at(select_plan(c));
   if (!pl) return B2G_ERR_INVALID_PLAN;
-  int n = 1 + (pl->pretranspose ? 1 : 0);  // a transpose, or one launch packing both operands
+  // a transpose, or one launch packing both operands, or a transpose per operand
+  int n = 1 + (pl->pretranspose == 3 ? (c.transA ? 1 : 2) : pl->pretranspose ? 1 : 0);
   if (pl->feed == kFeedSkinny) {
     int kc = 0;
     if (skinny_splits(*pl, c, &kc) > 1) n += 1;  // the split-K reduction
-  } else if (pl->feed == kFeedSkinnyTMA) {
+  } else if (pl->feed == kFeedSkinnyTMA || pl->cluster_max) {
     // the split-K sums are added inside the kernel's clusters
   } else {
     int first = 0;

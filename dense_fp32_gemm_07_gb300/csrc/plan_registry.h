@@ -49,5 +49,7 @@ extern const Plan kPlansT128x128[];
 extern const int kNumPlansT128x128;
 extern const Plan kPlansGeneral[];
 extern const int kNumPlansGeneral;
+extern const Plan kPlansCs[];
+extern const int kNumPlansCs;
 
 }  // namespace b2g

@@ -35,11 +35,12 @@
 
 #include "ptx.cuh"
 #include "sgemm_params.h"
+#include "tcgen05.cuh"
 
 namespace b2g {
 
 template <int BM, int BN, int BK, int WM, int WN, int TN, int STAGES, int ALAY, int FEED,
-          int PWARPS, int ORD = 0>
+          int PWARPS, int ORD = 0, int CS = 0>
 struct FfmaCfg {
   static constexpr int TM = 8;
   static constexpr int kConsumerWarps = WM * WN;
@@ -55,8 +56,14 @@ struct FfmaCfg {
   static constexpr int kPrivate = kStaged ? kConsumerWarps * 2 * BK * 32 : 0;  // per-warp A
   static constexpr int kARow = kStaged ? 32 : BM;  // row stride of the transposed A a warp reads
   static constexpr int kStageBytes = (BM * BK + kBStage) * 4;  // bytes one stage's copies land
+  // Cluster split (CS = 1): one work unit per CTA, the k slices of a tile
+  // summed in a cluster through distributed shared memory; each slice's sums
+  // wait in the drained ring, and a flag word follows the barriers.
+  static constexpr int kCsFlagBytes = CS ? 16 : 0;
   static constexpr int kSmemBytes =
-      (STAGES * (kAStage + kBStage + kStaging) + kPrivate) * 4 + 2 * STAGES * 8;
+      (STAGES * (kAStage + kBStage + kStaging) + kPrivate) * 4 + 2 * STAGES * 8 + kCsFlagBytes;
+  static_assert(!CS || BM * BN <= STAGES * (kAStage + kBStage), "a slice's sums fit in the ring");
+  static_assert(!CS || (FEED == kFeedTMA && !kStaged), "cluster split: bulk-tensor feed");
   static_assert(BM == WM * 32, "a warp tile is 32 rows");
   static_assert(BN == WN * 8 * TN, "a warp tile is 8*TN columns");
   static_assert(TN % 4 == 0 && BK % 4 == 0, "16-byte fragments");
@@ -180,15 +187,86 @@ __device__ __forceinline__ int total_units(const SgemmParams& p) {
   return p.tail_splits > 1 ? p.tail_first + (tiles - p.tail_first) * p.tail_splits : tiles;
 }
 
+// Cluster split: the S = p.tail_splits CTAs of a cluster are the k slices
+// of one output tile (blockIdx.x = tile * S + slice, the slice being the
+// CTA's rank in the cluster), and each has left its raw BM x BN sums in its
+// own shared memory at `part` (rows of BN floats).  After a cluster barrier
+// the CTA of rank r takes 1/S of the tile's float4 positions, adds their S
+// partial sums in rank (= slice) order through distributed shared memory,
+// applies C = alpha * sum + beta * C (C read only when beta != 0) and writes
+// C.  A second barrier keeps every CTA until all have read.  When any CTA of
+// the cluster gave up on a wait (its flag word), C is left alone; the status
+// word says why.  Every thread of the CTA calls this, on every path.
+template <int BM, int BN, int NT>
+__device__ __forceinline__ void cs_finish(const SgemmParams& p, const float* part,
+                                          const volatile int* failed) {
+  const int S = p.tail_splits;
+  if (S <= 1) return;  // no cluster: the CTA wrote C itself
+  // Not the .aligned barrier forms: the producer warp's lanes arrive from two
+  // places (lane 0 after its copies, the others at once).
+  // Every CTA's sums (or its failure flag) are in its shared memory after this.
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+  const uint32_t rank = cluster_ctarank();
+  bool any_failed = false;
+  for (int r = 0; r < S; ++r)
+    any_failed |=
+        ld_shared_cluster_u32(mapa_shared(smem_addr((const void*)failed), (uint32_t)r)) != 0;
+  if (!any_failed) {
+    int bt, tm, tn;
+    tile_coords(p, (int)blockIdx.x / S, bt, tm, tn);
+    float* Cb = p.C + (long long)bt * p.strideC;
+    constexpr int E = BM * BN / 4;  // float4 positions of the tile
+    const int e0 = (int)rank * E / S, e1 = ((int)rank + 1) * E / S;
+    const uint32_t part0 = smem_addr(part);
+    const float alpha = p.alpha, beta = p.beta;
+    for (int e = e0 + (int)threadIdx.x; e < e1; e += NT) {
+      const int gr = tm * BM + e / (BN / 4), gc = tn * BN + 4 * (e % (BN / 4));
+      if (gr >= p.M || gc >= p.N) continue;
+      float4 v[16];
+#pragma unroll
+      for (int r = 0; r < 16; ++r)
+        if (r < S) v[r] = ld_shared_cluster_f4(mapa_shared(part0 + 16u * e, (uint32_t)r));
+      float4 sum = v[0];
+#pragma unroll
+      for (int r = 1; r < 16; ++r)
+        if (r < S) sum.x += v[r].x, sum.y += v[r].y, sum.z += v[r].z, sum.w += v[r].w;
+      const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
+      float* crow = Cb + (long long)gr * p.ldc;
+      if (p.c_vec4 && gc + 3 < p.N) {
+        float4 o;
+        if (beta != 0.f) {
+          const float4 cv = *reinterpret_cast<const float4*>(crow + gc);
+          o = make_float4(fmaf(alpha, sv[0], beta * cv.x), fmaf(alpha, sv[1], beta * cv.y),
+                          fmaf(alpha, sv[2], beta * cv.z), fmaf(alpha, sv[3], beta * cv.w));
+        } else {
+          o = make_float4(alpha * sv[0], alpha * sv[1], alpha * sv[2], alpha * sv[3]);
+        }
+        *reinterpret_cast<float4*>(crow + gc) = o;
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (gc + q < p.N) {
+            float* o = crow + gc + q;
+            *o = (beta != 0.f) ? fmaf(alpha, sv[q], beta * *o) : alpha * sv[q];
+          }
+      }
+    }
+  }
+  // the others keep their shared memory until every CTA has read it; the
+  // arrive is relaxed (the loads it follows have been consumed, and the
+  // stores of C need no order with it)
+  asm volatile("barrier.cluster.arrive.relaxed;\n\tbarrier.cluster.wait;" ::: "memory");
+}
+
 template <int BM, int BN, int BK, int WM, int WN, int TN, int STAGES, int ALAY, int FEED,
-          int PWARPS, int ORD>
+          int PWARPS, int ORD, int CS>
 __global__ void __launch_bounds__((WM * WN + PWARPS) * 32,
                                   (FfmaCfg<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS,
                                            ORD>::kMinBlocks))
     sgemm_ffma_kernel(const __grid_constant__ SgemmParams p,
                       const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB) {
-  using Cfg = FfmaCfg<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS, ORD>;
+  using Cfg = FfmaCfg<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS, ORD, CS>;
   extern __shared__ __align__(1024) unsigned char smem[];
   float* sA = reinterpret_cast<float*>(smem);
   float* sB = sA + STAGES * Cfg::kAStage;
@@ -197,6 +275,7 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32,
   uint64_t* bars = reinterpret_cast<uint64_t*>(sAp + Cfg::kPrivate);
   const uint32_t full0 = smem_addr(bars);
   const uint32_t empty0 = smem_addr(bars + STAGES);
+  volatile int* cs_failed = reinterpret_cast<volatile int*>(bars + 2 * STAGES);  // CS only
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
@@ -210,6 +289,7 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32,
     }
     fence_mbar_init();
     fence_proxy_async_smem();
+    if constexpr (CS) *cs_failed = 0;
   }
   __syncthreads();
   pdl_wait();  // global memory only once the previous grid has completed
@@ -223,7 +303,10 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32,
     uint32_t phase = 0;
     int issued = 0;
     if constexpr (FEED == kFeedTMA || FEED == kFeedTMATrans) {
-      if (lane != 0) return;
+      if (lane != 0) {
+        if constexpr (CS) cs_finish<BM, BN, Cfg::kThreads>(p, sA, cs_failed);
+        return;
+      }
       prefetch_tmap(&tmA);
       prefetch_tmap(&tmB);
       for (int u = blockIdx.x; u < units; u += gridDim.x) {
@@ -311,6 +394,7 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32,
     drain_cp:
       cp_async_wait_all();
     }
+    if constexpr (CS) cs_finish<BM, BN, Cfg::kThreads>(p, sA, cs_failed);
     return;
   }
 
@@ -390,8 +474,18 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32,
         }
         As = priv + (int)(t_all & 1) * BK * 32 + 4 * tr;
       } else {
-        if (!mbar_wait(full0 + 8 * stage, phase, p.wait_limit_ns, p.status, kStatusTimeoutFull))
-          return;  // the status word says why; the producer drains and leaves too
+        if constexpr (CS) {
+          // the whole warp gives up together, and still reaches the barriers below
+          const bool landed =
+              mbar_wait(full0 + 8 * stage, phase, p.wait_limit_ns, p.status, kStatusTimeoutFull);
+          if (!__all_sync(0xffffffffu, landed)) {
+            if (lane == 0) *cs_failed = 1;
+            break;
+          }
+        } else {
+          if (!mbar_wait(full0 + 8 * stage, phase, p.wait_limit_ns, p.status, kStatusTimeoutFull))
+            return;  // the status word says why; the producer drains and leaves too
+        }
         As = sA + stage * Cfg::kAStage + a_off;
       }
       const float* Bs = sB + stage * Cfg::kBStage + b_off;
@@ -449,7 +543,13 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32,
     // split tile instead stores its raw sums (alpha 1, beta 0: exact) as a
     // whole BM x BN block with leading dimension BN for the tail reduction.
     const bool slice = part >= 0;
-    float* const cb = slice ? p.work + (size_t)part * (BM * BN) : p.C + (long long)bt * p.strideC;
+    if constexpr (CS) {
+      // every consumer warp has left the ring before a slice's sums overwrite it
+      asm volatile("bar.sync 1, %0;" ::"n"(Cfg::kConsumers) : "memory");
+      if (*cs_failed) break;
+    }
+    float* const cb = slice ? (CS ? sA : p.work + (size_t)part * (BM * BN))
+                            : p.C + (long long)bt * p.strideC;
     const long long ldc = slice ? BN : p.ldc;
     const int m0 = slice ? 0 : tm * BM, n0 = slice ? 0 : tn * BN;
     const int mlim = slice ? BM : p.M, nlim = slice ? BN : p.N;
@@ -489,15 +589,16 @@ __global__ void __launch_bounds__((WM * WN + PWARPS) * 32,
       }
     }
   }
+  if constexpr (CS) cs_finish<BM, BN, Cfg::kThreads>(p, sA, cs_failed);
 }
 
 // CTAs of one plan resident per SM on the current device, queried once per
 // device (after opting in to the plan's dynamic shared memory); 0 on failure.
 template <int BM, int BN, int BK, int WM, int WN, int TN, int STAGES, int ALAY, int FEED,
-          int PWARPS, int ORD>
+          int PWARPS, int ORD, int CS = 0>
 int ffma_occupancy() {
-  using Cfg = FfmaCfg<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS, ORD>;
-  auto kern = sgemm_ffma_kernel<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS, ORD>;
+  using Cfg = FfmaCfg<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS, ORD, CS>;
+  auto kern = sgemm_ffma_kernel<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS, ORD, CS>;
   static std::atomic<int> resident[kMaxDevices];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
@@ -505,6 +606,10 @@ int ffma_occupancy() {
   if (occ == 0) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Cfg::kSmemBytes) != cudaSuccess)
+      return 0;
+    // clusters of up to 16 k slices (more than the portable 8)
+    if (CS && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+                  cudaSuccess)
       return 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, Cfg::kThreads,
                                                       Cfg::kSmemBytes) != cudaSuccess ||
@@ -516,24 +621,44 @@ int ffma_occupancy() {
 }
 
 template <int BM, int BN, int BK, int WM, int WN, int TN, int STAGES, int ALAY, int FEED,
-          int PWARPS, int ORD>
+          int PWARPS, int ORD, int CS = 0>
 cudaError_t launch_ffma(const SgemmParams& p, const CUtensorMap* tmA, const CUtensorMap* tmB,
                         int num_sms, cudaStream_t stream) {
-  using Cfg = FfmaCfg<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS, ORD>;
-  auto kern = sgemm_ffma_kernel<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS, ORD>;
-  // The persistent grid is SMs x resident CTAs, or one CTA per work unit.
-  const int occ = ffma_occupancy<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS, ORD>();
+  using Cfg = FfmaCfg<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS, ORD, CS>;
+  auto kern = sgemm_ffma_kernel<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS, ORD, CS>;
+  // The persistent grid is SMs x resident CTAs, or one CTA per work unit;
+  // a cluster-split grid is always one CTA per work unit.
+  const int occ = ffma_occupancy<BM, BN, BK, WM, WN, TN, STAGES, ALAY, FEED, PWARPS, ORD, CS>();
   if (occ < 1) return cudaErrorInvalidConfiguration;
   const long long tiles = (long long)p.tiles_m * p.tiles_n * p.batch;
   const long long units =
       p.tail_splits > 1 ? p.tail_first + (tiles - p.tail_first) * p.tail_splits : tiles;
-  const int grid = (int)std::min<long long>(units, (long long)num_sms * occ);
+  if (CS && (p.tail_first != 0 || p.tail_splits > 16 || units > 0x7fffffffLL))
+    return cudaErrorInvalidConfiguration;
+  const int grid = CS ? (int)units : (int)std::min<long long>(units, (long long)num_sms * occ);
   CUtensorMap none;
   memset(&none, 0, sizeof(none));
   SgemmParams pc = p;
   pc.pdl_late = grid < (long long)num_sms * occ ? 1 : 0;
   CUtensorMap a = tmA ? *tmA : none, b = tmB ? *tmB : none;
   void* args[] = {&pc, &a, &b};
+  if (CS && p.tail_splits > 1) {  // the k slices of a tile form one cluster
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)p.tail_splits;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(Cfg::kThreads);
+    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(kern), args);
+  }
   return launch_pdl(reinterpret_cast<const void*>(kern), dim3(grid), dim3(Cfg::kThreads), args,
                     Cfg::kSmemBytes, stream);
 }
@@ -545,6 +670,18 @@ cudaError_t launch_ffma(const SgemmParams& p, const CUtensorMap* tmA, const CUte
         FfmaCfg<BM, BN, BK, WM, WN, TN, ST, ALAY, FEED, PW, ORD>::kSmemBytes,                    \
         &launch_ffma<BM, BN, BK, WM, WN, TN, ST, ALAY, FEED, PW, ORD>, 0,                        \
         &ffma_occupancy<BM, BN, BK, WM, WN, TN, ST, ALAY, FEED, PW, ORD>                         \
+  }
+
+// The kernel in its cluster-split form: one CTA per (tile, k slice), the k
+// slices of a tile (at most SMAX, one cluster) summed through distributed
+// shared memory; one launch, no workspace.
+#define B2G_FFMA_PLAN_CS(NAME, BM, BN, BK, WM, WN, TN, ST, ALAY, PW, ORD, SMAX)                   \
+  Plan {                                                                                         \
+    NAME, BM, BN, BK, ST, TN, ALAY, kFeedTMA,                                                    \
+        FfmaCfg<BM, BN, BK, WM, WN, TN, ST, ALAY, kFeedTMA, PW, ORD, 1>::kThreads,               \
+        FfmaCfg<BM, BN, BK, WM, WN, TN, ST, ALAY, kFeedTMA, PW, ORD, 1>::kSmemBytes,             \
+        &launch_ffma<BM, BN, BK, WM, WN, TN, ST, ALAY, kFeedTMA, PW, ORD, 1>, 0,                 \
+        &ffma_occupancy<BM, BN, BK, WM, WN, TN, ST, ALAY, kFeedTMA, PW, ORD, 1>, SMAX            \
   }
 
 // The same kernel behind a transpose of row-major A (PRE = 1) or a packing of

@@ -76,9 +76,13 @@ struct Plan {
   int pretranspose;  // 1: row-major A is first transposed into a workspace, then this
                      // plan's kernel (which reads A stored K x M) runs on it; 2: both
                      // operands are packed into a workspace first (A^T and B, aligned,
-                     // from any alignment, leading dimension or op() flags)
+                     // from any alignment, leading dimension or op() flags); 3: B stored
+                     // N x K (op(B) = B^T) is transposed into the workspace, and A too
+                     // unless it comes stored K x M (aligned operands, 16-byte vectors)
   int (*occupancy)();  // CTAs of this plan resident per SM on the current device (0 on
                        // failure); the host sizes split-K and split tails by it
+  int cluster_max = 0;  // > 0: cluster-split kernel, one CTA per (tile, k slice), at most
+                        // this many k slices of a tile summed inside one cluster
 };
 
 }  // namespace b2g

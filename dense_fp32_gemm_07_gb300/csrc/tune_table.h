@@ -5,13 +5,20 @@
 // libraries keep a configuration per shape; this table is that configuration.
 // Rules are tried in order; the first whose class and bounds match names the
 // plan (for a strided batch whose products have at least 5e7 multiply-adds
-// each, M*N*K counts the whole call: times the batch count).  "fast" = both operands bulk-tensor eligible (16-byte aligned, lda, ldb
-// and K multiples of 4, no op() on B); "general" = anything else.
+// each, M*N*K counts the whole call: times the batch count).  "fast" = both
+// operands bulk-tensor eligible (16-byte aligned, lda, ldb and K multiples of
+// 4, no op() on B); "fast, B transposed" = the same alignment with op(B) = B^T;
+// "general" = anything else.
 #pragma once
 
 namespace b2g {
 
-enum OperandClass : int { kClassFast = 0, kClassFastTransA = 1, kClassGeneral = 2 };
+enum OperandClass : int {
+  kClassFast = 0,        // row-major A and B, bulk-tensor eligible
+  kClassFastTransA = 1,  // A stored K x M, B row-major, bulk-tensor eligible
+  kClassGeneral = 2,     // anything else
+  kClassFastTransB = 3,  // B stored N x K (A either way), 16-byte aligned, lda, ldb, K % 4 == 0
+};
 
 struct TuneRule {
   int cls;
@@ -45,6 +52,12 @@ const TuneRule kTuneTable[] = {
     // kernel (its 64 x 128 twin when that pads less, e.g. M <= 64)
     {kClassFast, 0, kInf, 0, kInf, 1.0e9, "pre_128x64x32_s3_o5", "tmaX_128x128x16_s6_o2"},
     {kClassFastTransA, 0, kInf, 0, kInf, 0, "tmaT_128x64x32_s3_o5", nullptr},
+    // op(B) = B^T on aligned operands: B^T (and A, unless it comes stored
+    // K x M) transposed into the workspace by the 16-byte-vector transpose,
+    // then the transposed-layout kernel (4096^3: packing both operands with
+    // 4-byte moves cost 3.5% of the call); small calls take the 4-byte feed
+    {kClassFastTransB, 0, kInf, 0, kInf, 5.0e7, "pret_128x64x32_s3_o5", "gen_64x64x16_s4"},
+    {kClassFastTransB, 0, kInf, 0, kInf, 0, "gen_64x64x16_s4", nullptr},
     // anything else (misaligned pointers, odd leading dimensions, K % 4 != 0,
     // op(B) = B^T): pack A^T and B aligned into the workspace, then the
     // transposed-layout kernel; the 4-byte feed needs no workspace

@@ -16,7 +16,7 @@ bench's skinny measurement does, and adds the algorithmic bytes' rate
 (4(MK + KN + MN(1 + [beta != 0])) per call) to each line.
 --tf32x3 times the 3xTF32 tensor-core path instead, each kernel variant
 (0: one CTA per 128 x 128 tile, 1 and 2: a CTA pair per 256 x 128 or 256 x 256
-tile), split kernels included.
+tile), split kernels included; --variants picks which.
 """
 from __future__ import annotations
 
@@ -98,7 +98,7 @@ def sweep(shapes, once=False, out=sys.stdout, pattern=None, cold=False):
                   file=out, flush=True)
 
 
-def sweep_tf32x3(shapes, once=False, out=sys.stdout):
+def sweep_tf32x3(shapes, once=False, out=sys.stdout, variants=(0, 1, 2)):
     import torch
 
     from dense_fp32_gemm_07_gb300 import build
@@ -110,7 +110,7 @@ def sweep_tf32x3(shapes, once=False, out=sys.stdout):
         C = torch.rand(M, N, device="cuda") * 2 - 1
         flops = 2.0 * M * N * K
         iters = max(3, min(50, int(2e12 / flops)))
-        for variant in (0, 1, 2):
+        for variant in variants:
             def call():
                 b2g.sgemm_3xtf32(A, B, C, alpha, beta, variant=variant)
 
@@ -139,12 +139,15 @@ def main():
     ap.add_argument("--once", action="store_true")
     ap.add_argument("--plans", default=None, help="regex: time only the matching plans")
     ap.add_argument("--tf32x3", action="store_true", help="time the 3xTF32 kernel variants")
+    ap.add_argument("--variants", default="0,1,2",
+                    help="3xTF32 kernel variants to run, comma-separated (with --tf32x3)")
     ap.add_argument("--cold", action="store_true",
                     help="rotate operand copies so that every call reads them from HBM")
     args = ap.parse_args()
     shapes = [parse_shape(s) for s in args.shapes]
     if args.tf32x3:
-        sweep_tf32x3(shapes, once=args.once)
+        sweep_tf32x3(shapes, once=args.once,
+                     variants=tuple(int(v) for v in args.variants.split(",")))
     else:
         sweep(shapes, once=args.once, pattern=args.plans, cold=args.cold)
 

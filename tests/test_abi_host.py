@@ -53,7 +53,7 @@ def test_version_and_plans(b2g):
         info = b2g.b2g_plan_info(i)
         assert info["BM"] > 0 and info["BN"] > 0 and info["BK"] % 4 == 0
         assert info["threads"] % 32 == 0 and info["smem_bytes"] <= 227 * 1024
-        assert n.startswith(("tma", "gen", "pre", "pack", "skinny"))
+        assert n.startswith(("tma", "gen", "pre", "pack", "skinny", "cs"))
     assert b2g.b2g_plan_name(len(names)) is None
     with pytest.raises(b2g.B2GError):
         b2g.b2g_plan_info(-1)
@@ -118,9 +118,16 @@ def test_tune_table_classes(b2g):
     assert _plan(b2g, 0, 0, 512, 512, 510, 1.0, FAKE, 512, FAKE, 512, FAKE, 512).startswith("pack_")
     # small general problems -> 4-byte feed (no workspace)
     assert _plan(b2g, 0, 0, 64, 64, 63, 1.0, FAKE, 64, FAKE, 64, FAKE, 64).startswith("gen_")
-    # op(A) = A^T aligned -> transposed-layout bulk-tensor plan; op(B) = B^T -> packed
+    # op(A) = A^T aligned -> transposed-layout bulk-tensor plan; op(B) = B^T
+    # aligned -> B^T (and A) transposed with 16-byte vectors, then that plan
     assert _plan(b2g, 1, 0, 512, 512, 512, 1.0, FAKE, 512, FAKE, 512, FAKE, 512).startswith("tmaT_")
-    assert _plan(b2g, 0, 1, 512, 512, 512, 1.0, FAKE, 512, FAKE, 512, FAKE, 512).startswith("pack_")
+    assert _plan(b2g, 0, 1, 512, 512, 512, 1.0, FAKE, 512, FAKE, 512, FAKE, 512).startswith("pret_")
+    assert _plan(b2g, 1, 1, 512, 512, 512, 1.0, FAKE, 512, FAKE, 512, FAKE, 512).startswith("pret_")
+    # op(B) = B^T with K % 4 != 0 or an odd leading dimension -> packed
+    assert _plan(b2g, 0, 1, 512, 512, 510, 1.0, FAKE, 512, FAKE, 510, FAKE, 512).startswith("pack_")
+    assert _plan(b2g, 0, 1, 512, 512, 512, 1.0, FAKE, 512, FAKE, 513, FAKE, 512).startswith("pack_")
+    # small op(B) = B^T calls -> 4-byte feed
+    assert _plan(b2g, 0, 1, 64, 64, 64, 1.0, FAKE, 64, FAKE, 64, FAKE, 64).startswith("gen_")
 
 
 # With no device answering, the host sizes splits for 152 SMs x 4 resident CTAs.
@@ -212,6 +219,25 @@ def test_launch_count_query(b2g):
     assert count(1000, 1025, 777, lda=777) == 3      # one packing launch, GEMM, tail
     rc, _ = b2g.b2g_sgemm_launch_count(0, 0, 64, 64, 64, 1.0, FAKE, 63, FAKE, 64, FAKE, 64)
     assert rc == -2
+    # op(B) = B^T at 4096^3: transposes of A and of B^T, GEMM, tail reduction;
+    # with A stored K x M only B^T is transposed
+    for tA, n in ((0, 4), (1, 3)):
+        rc, got = b2g.b2g_sgemm_launch_count(tA, 1, 4096, 4096, 4096, 1.0, FAKE, 4096, FAKE, 4096,
+                                             FAKE, 4096)
+        assert rc == 0 and got == n, (tA, got)
+
+
+def test_workspace_of_transposed_b(b2g):
+    """pret_ plans: B^T transposed (K x round_up(N, 4)), plus A^T unless A
+    comes stored K x M, then the split tail's room."""
+    M, N, K = 4096, 4092, 4096
+    for tA in (0, 1):
+        pi = b2g.b2g_sgemm_select_plan(tA, 1, M, N, K, 1.0, FAKE, 4096, FAKE, 4096, FAKE, N)
+        info = b2g.b2g_plan_info(pi)
+        assert b2g.b2g_plan_name(pi).startswith("pret_")
+        rc, n = b2g.b2g_sgemm_workspace_size(tA, 1, M, N, K, 1.0, FAKE, 4096, FAKE, 4096, FAKE, N)
+        base = K * ((0 if tA else M) + N) * 4
+        assert rc == 0 and n == want_bytes(base, M, N, K, info["BM"], info["BN"]), (tA, n)
 
 
 def test_forced_plan_range(b2g):

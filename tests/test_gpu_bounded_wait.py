@@ -23,6 +23,8 @@ def tb():
     ("pre_128x64x32_s3_o5", 64, 64, 128),   # packed kernels, both tile shapes
     ("pre_64x128x32_s3_o5", 64, 64, 128),
     ("skinnyT_m16", 16, 512, 1024),         # k slabs summed in a cluster of 8 CTAs
+    ("cs8_64x128x16_s6_o2", 64, 128, 256),  # one tile's 8 k slices in one cluster
+    ("cs16_64x128x16_s6_o2", 128, 256, 512),  # four clusters of 16 k slices
 ])
 def test_wait_runs_out_and_context_survives(tb, plan_name, M, N, K):
     torch, b2g = tb

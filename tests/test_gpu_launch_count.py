@@ -79,3 +79,30 @@ def test_reported_launches_match(tb, M, N, K, lda, alpha, beta):
 
     got, nodes = _kernel_nodes(cu, stream.cuda_stream, call)
     assert got == expected, (expected, got, nodes)
+
+
+@pytest.mark.parametrize("transA,expected_transposes", [(0, 2), (1, 1)])
+def test_reported_launches_match_transposed_b(tb, transA, expected_transposes):
+    """op(B) = B^T at 2048^3: one transpose per operand not in the kernel's
+    layout, the GEMM and its split-tail reduction."""
+    torch, b2g, cu = tb
+    M = N = K = 2048
+    rng = np.random.default_rng(7 + transA)
+    A = torch.from_numpy(rng.uniform(-1, 1, (M, K)).astype(np.float32)).cuda()
+    B = torch.from_numpy(rng.uniform(-1, 1, (N, K)).astype(np.float32)).cuda()
+    C = torch.from_numpy(rng.uniform(-1, 1, (M, N)).astype(np.float32)).cuda()
+    args = (transA, 1, M, N, K, 1.0, A.data_ptr(), 2048, B.data_ptr(), 2048)
+    rc, expected = b2g.b2g_sgemm_launch_count(*args, C.data_ptr(), N)
+    assert rc == 0 and expected == expected_transposes + 2
+    rc, need = b2g.b2g_sgemm_workspace_size(*args, C.data_ptr(), N)
+    assert rc == 0
+    ws = torch.empty(max(16, need), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+
+    def call():
+        assert b2g.b2g_sgemm_ws(*args, 0.5, C.data_ptr(), N, ws.data_ptr(), need,
+                                stream.cuda_stream) == 0
+
+    got, nodes = _kernel_nodes(cu, stream.cuda_stream, call)
+    assert got == expected, (expected, got, nodes)

@@ -229,3 +229,44 @@ def test_status_word_clean(tb):
     torch, b2g = tb
     rc, flags = b2g.b2g_status(torch.cuda.current_stream().cuda_stream)
     assert rc == 0 and flags == 0
+
+
+@pytest.mark.parametrize("trans", [(False, True), (True, True), (True, False)])
+def test_square4096_transposed_operands_full(tb, trans):
+    """The headline product with A and/or B handed over transposed (A stored
+    K x M, B stored N x K): the same result, every element against the oracle.
+    op(B) = B^T takes the plan that transposes B^T (and A) with 16-byte
+    vectors before the GEMM."""
+    torch, b2g = tb
+    transA, transB = trans
+    w, A, B, C, ref, bound = workload_reference("square4096")
+    dA = torch.from_numpy(np.ascontiguousarray(A.T) if transA else A).cuda()
+    dB = torch.from_numpy(np.ascontiguousarray(B.T) if transB else B).cuda()
+    dC = torch.from_numpy(C).cuda()
+    plan = b2g.b2g_plan_name(b2g.b2g_sgemm_select_plan(
+        int(transA), int(transB), w.M, w.N, w.K, w.alpha, dA.data_ptr(), dA.stride(0),
+        dB.data_ptr(), dB.stride(0), dC.data_ptr(), w.N))
+    assert plan.startswith("pret_" if transB else "tmaT_"), plan
+    b2g.sgemm(dA, dB, dC, w.alpha, w.beta, transA=transA, transB=transB)
+    torch.cuda.synchronize()
+    check(dC.cpu().numpy(), ref, bound, f"square4096 trans {trans}")
+
+
+@pytest.mark.parametrize("shape", [(600, 520, 1024), (1000, 1028, 776), (64, 4096, 512)])
+@pytest.mark.parametrize("transA", [False, True])
+def test_transposed_b_plans(tb, shape, transA):
+    """op(B) = B^T on aligned operands above 5e7 multiply-adds: the pret_
+    plans (both tile shapes), split tail included."""
+    torch, b2g = tb
+    M, N, K = shape
+    rng = np.random.default_rng(M + N + K + transA)
+    A = rng.uniform(-1, 1, size=(K, M) if transA else (M, K)).astype(np.float32)
+    B = rng.uniform(-1, 1, size=(N, K)).astype(np.float32)
+    C = rng.uniform(-1, 1, size=(M, N)).astype(np.float32)
+    ref, bound, _ = oracle.sgemm(A, B, C, 0.5, 1.5, transA=transA, transB=True)
+    plan = b2g.b2g_plan_name(b2g.b2g_sgemm_select_plan(int(transA), 1, M, N, K, 0.5, 1 << 20,
+                                                        A.shape[1], 1 << 20, K, 1 << 20, N))
+    assert plan.startswith("pret_"), plan
+    got, rc, guard = gemm(b2g, torch, A, B, C, 0.5, 1.5, transA, True)
+    assert rc == 0 and guard
+    check(got, ref, bound, f"{shape} transA={transA} {plan}")
