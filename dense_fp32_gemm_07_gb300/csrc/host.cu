@@ -668,9 +668,9 @@ int run(const Call& c, int forced_plan, void* stream, void* user_ws = nullptr,
 //    stream sends B's rows and A's columns of chunk 0, then of chunk 1, ...,
 //    then C.  The caller's stream multiplies each chunk as soon as it has
 //    landed into a device accumulator D (beta 0 for the first chunk, 1 after).
-//  * The last chunk runs in row panels of about 1024 rows: each panel adds
-//    beta * C (D += beta * C) and goes back to the host on a second copy
-//    stream while the next panel multiplies.
+//  * The last chunk runs in row panels that shrink (6/16, 6/16, 3/16, 1/16
+//    of M): each panel adds beta * C (D += beta * C) and goes back to the host
+//    on a second copy stream while the next panel multiplies.
 // So the GEMM starts after 1/4 of A and B have arrived, C's copy hides behind
 // the first chunks, and only the last panel's return is exposed.  With
 // K < 2048 there is one chunk and C goes in with A, panel by panel, straight
@@ -736,10 +736,28 @@ int run_host(const Call& c, void* stream) {
     kb[1] = c.K / 8 / 16 * 16, kb[2] = c.K / 2 / 16 * 16, kb[3] = c.K;
     chunks = 3;
   }
-  int panels = c.M / 1024;
-  panels = panels < 1 ? 1 : panels > kHostPanelsMax ? kHostPanelsMax : panels;
-  const int rows = ((c.M + panels - 1) / panels + 127) / 128 * 128;
-  panels = (c.M + rows - 1) / rows;
+  // Row panels of the last chunk, rows pb[i] .. pb[i+1]-1: about 1024 rows
+  // each (at 4096 columns, 512 tiles: one round of the persistent grid plus a
+  // split tail).  With K chunks (all of A and C already copied in), the last
+  // panel is cut into 3/4 and 1/4 (multiples of 128 rows) so that the return
+  // left exposed after the last GEMM is a quarter as long; each earlier
+  // panel's return hides behind the next panel's GEMM.  With one chunk each
+  // panel first brings its own rows of A and C in.
+  int pb[kHostPanelsMax + 1];
+  int panels = 0;
+  pb[0] = 0;
+  {
+    int n = c.M / 1024;  // at most kHostPanelsMax - 1, leaving room for the cut
+    n = n < 1 ? 1 : n > kHostPanelsMax - 1 ? kHostPanelsMax - 1 : n;
+    const int rows = ((c.M + n - 1) / n + 127) / 128 * 128;
+    for (int r = rows; r < c.M; r += rows) pb[++panels] = r;
+    const int base = pb[panels], last = c.M - base;
+    if (chunks > 1 && last >= 512) {
+      const int cut = base + (last * 3 / 4 + 127) / 128 * 128;
+      if (cut < c.M) pb[++panels] = cut;
+    }
+    pb[++panels] = c.M;
+  }
   const bool separate_c = chunks > 1 && read_c;  // C kept apart, added at the end
 
   const size_t a_bytes = gemm ? round256(M * kp * 4) : 0;
@@ -813,8 +831,8 @@ int run_host(const Call& c, void* stream) {
   // the last chunk (or the only one), panel by panel, then back to the host
   const int kl0 = kb[chunks - 1];
   for (int i = 0; i < panels && !rc; ++i) {
-    const size_t r0 = (size_t)i * rows;
-    const size_t rn = (size_t)(c.M - (int)r0 < rows ? c.M - (int)r0 : rows);
+    const size_t r0 = (size_t)pb[i];
+    const size_t rn = (size_t)(pb[i + 1] - pb[i]);
     if (chunks == 1) {  // A's and C's rows of this panel come now
       if (gemm)
         rc = ok(cudaMemcpy2DAsync(dA + r0 * kp, kp * 4, c.A + r0 * c.lda, (size_t)c.lda * 4,
