@@ -40,8 +40,18 @@ __global__ void __launch_bounds__(256) tail_reduce_kernel(const __grid_constant_
     float* crow = Cb + (long long)gr * p.ldc;
     const bool vec = p.c_vec4 && gc + 3 < p.N;
     // C's values first, so that their trip from memory overlaps the slices'
+    // (element by element where C's rows are not 16-byte aligned)
     float4 cv = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (vec && beta != 0.f) cv = *reinterpret_cast<const float4*>(crow + gc);
+    if (beta != 0.f) {
+      if (vec) {
+        cv = *reinterpret_cast<const float4*>(crow + gc);
+      } else {
+        cv.x = crow[gc];
+        if (gc + 1 < p.N) cv.y = crow[gc + 1];
+        if (gc + 2 < p.N) cv.z = crow[gc + 2];
+        if (gc + 3 < p.N) cv.w = crow[gc + 3];
+      }
+    }
     float4 acc = *reinterpret_cast<const float4*>(P + (size_t)q * 4);
     for (int s = 1; s < S; ++s) {
       const float4 v = *reinterpret_cast<const float4*>(P + s * tile_elems + (size_t)q * 4);
@@ -60,12 +70,11 @@ __global__ void __launch_bounds__(256) tail_reduce_kernel(const __grid_constant_
       }
       *reinterpret_cast<float4*>(crow + gc) = o;
     } else {
+      const float cs[4] = {cv.x, cv.y, cv.z, cv.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        if (gc + e < p.N) {
-          float* o = crow + gc + e;
-          *o = (beta != 0.f) ? fmaf(alpha, av[e], beta * *o) : alpha * av[e];
-        }
+        if (gc + e < p.N)
+          crow[gc + e] = (beta != 0.f) ? fmaf(alpha, av[e], beta * cs[e]) : alpha * av[e];
       }
     }
   }

@@ -107,3 +107,21 @@ def test_batched_split(tb):
     for b in range(batch):
         ref, bound, _ = oracle.sgemm(A[b], B[b], C[b], 0.5, 1.5)
         check(got[b], ref, bound, f"problem {b}")
+
+
+@pytest.mark.parametrize("lds,mis", [((1000, 260, 261), (0, 0, 0)), ((1000, 260, 260), (0, 0, 1))])
+def test_split_tail_unaligned_c(tb, lds, mis):
+    """C whose rows are not 16-byte aligned (odd ldc, or a base one float off):
+    the split tail's reduction then moves C element by element; same bound,
+    beta != 0 so C is read."""
+    torch, b2g = tb
+    M, N, K = 300, 260, 1000
+    rng = np.random.default_rng(17)
+    A = rng.uniform(-1, 1, size=(M, K)).astype(np.float32)
+    B = rng.uniform(-1, 1, size=(K, N)).astype(np.float32)
+    C = rng.uniform(-1, 1, size=(M, N)).astype(np.float32)
+    ref, bound, _ = oracle.sgemm(A, B, C, 0.5, 1.5)
+    assert launches(b2g, M, N, K) == 2  # the GEMM and the split tail's reduction
+    got, rc, guard = gemm(b2g, torch, A, B, C, 0.5, 1.5, lds=lds, misalign=mis)
+    assert rc == 0 and guard
+    check(got, ref, bound, f"ldc {lds[2]} misalign {mis}")
