@@ -1,6 +1,7 @@
 """Strided-batched SGEMM: every problem of the batch against the oracle,
 across the plan families the tune table reaches (k-chunked, pre-transposed,
-packed, skinny split-K) and with padded strides and op() flags."""
+packed, B^T transposed first, skinny split-K) and with padded strides and op()
+flags."""
 import numpy as np
 import pytest
 
@@ -52,6 +53,8 @@ CASES = [
     (16, 512, 256, 5, False, False, 0),     # skinny split-K
     (1024, 1024, 2048, 2, False, False, 0),  # pre-transposed A (workspace x batch)
     (1000, 1025, 777, 2, False, False, 0),   # packed operands
+    (400, 384, 512, 3, False, True, 0),      # op(B) = B^T: B^T and A transposed first (pret_)
+    (400, 384, 512, 3, True, True, 4),       # the same with A stored K x M, padded strides
     (64, 64, 64, 1, False, False, 0),
 ]
 
