@@ -185,7 +185,7 @@ const PlanGroup kGroups[] = {
     {kPlansT64x128k32, &kNumPlansT64x128k32},
     {kPlansT128x128, &kNumPlansT128x128}, {kPlansGeneral, &kNumPlansGeneral},
     {kPlansSkinny, &kNumPlansSkinny},     {kPlansSkinnyTma, &kNumPlansSkinnyTma},
-    {kPlansCs, &kNumPlansCs},
+    {kPlansCs, &kNumPlansCs},           {kPlansTmaO5, &kNumPlansTmaO5},
 };
 
 int num_plans() {

@@ -51,5 +51,7 @@ extern const Plan kPlansGeneral[];
 extern const int kNumPlansGeneral;
 extern const Plan kPlansCs[];
 extern const int kNumPlansCs;
+extern const Plan kPlansTmaO5[];
+extern const int kNumPlansTmaO5;
 
 }  // namespace b2g

@@ -74,7 +74,9 @@ struct FfmaCfg {
   // 128-register cap to keep three 160-thread CTAs per SM; its 32-k stage runs
   // fully unrolled.  The scalar orders unroll at most 16 k (unrolled 32 times
   // the scalar loop was measured 13% slower).
-  static constexpr int kMinBlocks = ORD == 5 ? 3 : 1;
+  // With A k-chunked the packed order keeps eight float4 fragments and would
+  // spill under that cap, so those kernels ask for two CTAs per SM instead.
+  static constexpr int kMinBlocks = ORD == 5 ? (ALAY == kAKChunk ? 2 : 3) : 1;
   static constexpr int kUnroll = ORD == 5 ? 32 : 16;
 };
 

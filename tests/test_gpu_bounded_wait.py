@@ -18,6 +18,7 @@ def tb():
 
 @pytest.mark.parametrize("plan_name,M,N,K", [
     ("tma_64x128x16_s6_o2", 64, 64, 64),
+    ("tma_64x128x16_s6_o5", 64, 64, 64),      # the small-problem plan: packed, k-chunked A
     ("tmaX_64x128x16_s6_o1", 64, 64, 64),
     ("gen_64x64x16_s4", 64, 64, 64),
     ("pre_128x64x32_s3_o5", 64, 64, 128),   # packed kernels, both tile shapes
