@@ -664,15 +664,16 @@ int run(const Call& c, int forced_plan, void* stream, void* user_ws = nullptr,
 // b2g_sgemm_host: A, B and C live in host memory; the host link (about 210 GB/s
 // in, 190 GB/s out on GB300) is much slower than the GEMM, so the copies are
 // overlapped with it:
-//  * K is cut into chunks (for K >= 2048: four chunks, 16-aligned); the copy
-//    stream sends B's rows and A's columns of chunk 0, then of chunk 1, ...,
-//    then C.  The caller's stream multiplies each chunk as soon as it has
-//    landed into a device accumulator D (beta 0 for the first chunk, 1 after).
-//  * The last chunk runs in row panels that shrink (6/16, 6/16, 3/16, 1/16
-//    of M): each panel adds beta * C (D += beta * C) and goes back to the host
-//    on a second copy stream while the next panel multiplies.
-// So the GEMM starts after 1/4 of A and B have arrived, C's copy hides behind
-// the first chunks, and only the last panel's return is exposed.  With
+//  * K is cut into chunks (for K >= 2048: three growing chunks, K/8, 3K/8 and
+//    K/2, 16-aligned); the copy stream sends B's rows and A's columns of chunk
+//    0, then of chunk 1, then of chunk 2, then C.  The caller's stream
+//    multiplies each chunk as soon as it has landed into a device accumulator
+//    D (beta 0 for the first chunk, 1 after).
+//  * The last chunk runs in row panels of about 1024 rows, the last of them
+//    cut into 3/4 and 1/4: each panel adds beta * C (D += beta * C) and goes
+//    back to the host on a second copy stream while the next panel multiplies.
+// So the GEMM starts after 1/8 of A and B have arrived, C's copy hides behind
+// the first chunks, and only the last, short panel's return is exposed.  With
 // K < 2048 there is one chunk and C goes in with A, panel by panel, straight
 // into D.  Chunked sums are rounded once per chunk, which the FP32 bound
 // covers.  Device copies are packed with rows padded to a multiple of 4 floats.

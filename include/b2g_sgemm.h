@@ -145,11 +145,12 @@ int b2g_sgemm_ws(int transA, int transB, int M, int N, int K, float alpha, const
  * the library copies A's columns and B's rows in three growing K chunks
  * (K/8, 3K/8, K/2) and then C on its own copy stream, while `stream`
  * multiplies each chunk into a device accumulator as soon as it has arrived;
- * the last chunk runs in row panels that shrink (6/16, 6/16, 3/16 and 1/16
- * of M, in multiples of 128 rows; one panel below M = 2048), each finished
- * panel (plus beta * C) going back to the host on a second copy stream while
- * the next one multiplies, so that only the last, small return is exposed.  For K < 2048 it copies B, then A and C in row panels,
- * and multiplies each panel as it arrives.  Every step is ordered after
+ * the last chunk runs in row panels of about 1024 rows (multiples of 128
+ * rows, at most 16 panels), the last panel cut into 3/4 and 1/4 when it has
+ * 512 rows or more; each finished panel (plus beta * C) goes back to the host
+ * on a second copy stream while the next one multiplies, so that only the
+ * last, short return is exposed.  For K < 2048 it copies B, then A and C in
+ * the same row panels (no cut), and multiplies each panel as it arrives.  Every step is ordered after
  * earlier work on `stream`, and the call's last copy is joined back into
  * `stream`.  Sums split over K chunks are rounded once per chunk, within the
  * same error bound.  C holds
