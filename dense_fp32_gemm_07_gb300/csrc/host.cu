@@ -44,21 +44,32 @@ __global__ void scale_c_kernel(int M, int N, float beta, float* __restrict__ C, 
   }
 }
 
-// Y += b * X over an M x N window (row-major, leading dimensions ldx, ldy, both
-// multiples of 4 with 16-byte aligned bases: float4 throughout).
-__global__ void axpby_rows_kernel(int M, int N4, float b, const float* __restrict__ X,
-                                  long long ldx, float* __restrict__ Y, long long ldy) {
+// Y = (P0 + P1) + Y, then Y += b * X when X is given, over an M x N window of
+// row-major matrices that share the leading dimension ld (a multiple of 4, all
+// bases 16-byte aligned: float4 throughout).  Rows go to blockIdx.y, float4
+// columns to the threads of blockIdx.x.
+__global__ void combine_rows_kernel(int M, int N4, long long ld, const float* __restrict__ P0,
+                                    const float* __restrict__ P1, float b,
+                                    const float* __restrict__ X, float* __restrict__ Y) {
   pdl_launch_dependents();
   pdl_wait();
-  const long long total = (long long)M * N4;
-  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-       idx += (long long)gridDim.x * blockDim.x) {
-    const long long i = idx / N4, j = (idx - i * N4) * 4;
-    const float4 x = *reinterpret_cast<const float4*>(X + i * ldx + j);
-    float4* yp = reinterpret_cast<float4*>(Y + i * ldy + j);
-    float4 y = *yp;
-    y.x = fmaf(b, x.x, y.x), y.y = fmaf(b, x.y, y.y), y.z = fmaf(b, x.z, y.z), y.w = fmaf(b, x.w, y.w);
-    *yp = y;
+  for (int i = blockIdx.y; i < M; i += gridDim.y) {
+    const long long row = (long long)i * ld;
+    for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < N4; j += gridDim.x * blockDim.x) {
+      const long long o = row + 4LL * j;
+      const float4 p0 = *reinterpret_cast<const float4*>(P0 + o);
+      const float4 p1 = *reinterpret_cast<const float4*>(P1 + o);
+      float4* yp = reinterpret_cast<float4*>(Y + o);
+      float4 y = *yp;
+      y.x = (p0.x + p1.x) + y.x, y.y = (p0.y + p1.y) + y.y;
+      y.z = (p0.z + p1.z) + y.z, y.w = (p0.w + p1.w) + y.w;
+      if (X) {
+        const float4 x = *reinterpret_cast<const float4*>(X + o);
+        y.x = fmaf(b, x.x, y.x), y.y = fmaf(b, x.y, y.y);
+        y.z = fmaf(b, x.z, y.z), y.w = fmaf(b, x.w, y.w);
+      }
+      *yp = y;
+    }
   }
 }
 
@@ -667,11 +678,14 @@ int run(const Call& c, int forced_plan, void* stream, void* user_ws = nullptr,
 //  * K is cut into chunks (for K >= 2048: three growing chunks, K/8, 3K/8 and
 //    K/2, 16-aligned); the copy stream sends B's rows and A's columns of chunk
 //    0, then of chunk 1, then of chunk 2, then C.  The caller's stream
-//    multiplies each chunk as soon as it has landed into a device accumulator
-//    D (beta 0 for the first chunk, 1 after).
+//    multiplies each chunk as soon as it has landed, into a product of its
+//    own (P0, P1, D: every GEMM runs with beta 0 and never reads C, which
+//    saves the epilogue's waits for C; at 4096 x 4096 x 1536 a beta-1 pass
+//    takes 782 us against 752).
 //  * The last chunk runs in row panels of about 1024 rows, the last of them
-//    cut into 3/4 and 1/4: each panel adds beta * C (D += beta * C) and goes
-//    back to the host on a second copy stream while the next panel multiplies.
+//    cut into 3/4 and 1/4: each panel is combined, D = (P0 + P1) + D + beta * C,
+//    and goes back to the host on a second copy stream while the next panel
+//    multiplies.
 // So the GEMM starts after 1/8 of A and B have arrived, C's copy hides behind
 // the first chunks, and only the last, short panel's return is exposed.  With
 // K < 2048 there is one chunk and C goes in with A, panel by panel, straight
@@ -764,7 +778,8 @@ int run_host(const Call& c, void* stream) {
   const size_t a_bytes = gemm ? round256(M * kp * 4) : 0;
   const size_t b_bytes = gemm ? round256(K * np * 4) : 0;
   const size_t d_bytes = round256(M * np * 4);
-  const size_t need = a_bytes + b_bytes + d_bytes + (separate_c ? d_bytes : 0);
+  const size_t p_bytes = chunks > 1 ? 2 * d_bytes : 0;  // P0, P1: the first chunks' products
+  const size_t need = a_bytes + b_bytes + d_bytes + p_bytes + (separate_c ? d_bytes : 0);
 
   HostPath& h = g_hostpath[dev];
   std::lock_guard<std::mutex> lk(h.mu);
@@ -790,7 +805,10 @@ int run_host(const Call& c, void* stream) {
   float* dA = reinterpret_cast<float*>(base);
   float* dB = reinterpret_cast<float*>(base + a_bytes);
   float* dD = reinterpret_cast<float*>(base + a_bytes + b_bytes);
-  float* dC = separate_c ? reinterpret_cast<float*>(base + a_bytes + b_bytes + d_bytes) : dD;
+  float* dP0 = reinterpret_cast<float*>(base + a_bytes + b_bytes + d_bytes);
+  float* dP1 = reinterpret_cast<float*>(base + a_bytes + b_bytes + 2 * d_bytes);
+  float* dC = separate_c ? reinterpret_cast<float*>(base + a_bytes + b_bytes + d_bytes + p_bytes)
+                         : dD;
 
   auto ok = [](cudaError_t e) { return e == cudaSuccess ? 0 : B2G_ERR_CUDA; };
   const int lda_d = (int)(kp > 0 ? kp : 1);
@@ -811,13 +829,13 @@ int run_host(const Call& c, void* stream) {
                                 cudaMemcpyHostToDevice, h.h2d));
       if (!rc) rc = ok(cudaEventRecord(h.c_in, h.h2d));
     }
-    // all chunks but the last, over all rows, into D
+    // all chunks but the last, over all rows, each into its own product
     for (int j = 0; j + 1 < chunks && !rc; ++j) {
       const int k0 = kb[j], k1 = kb[j + 1];
       rc = ok(cudaStreamWaitEvent(st, h.chunk[j], 0));
       if (!rc) {
-        Call pc{0, 0, c.M, c.N, k1 - k0, c.alpha, j == 0 ? 0.f : 1.f, dA + k0, lda_d,
-                dB + (size_t)k0 * np, (int)np, dD, (int)np};
+        Call pc{0, 0, c.M, c.N, k1 - k0, c.alpha, 0.f, dA + k0, lda_d,
+                dB + (size_t)k0 * np, (int)np, j == 0 ? dP0 : dP1, (int)np};
         rc = run(pc, -1, st);
       }
     }
@@ -845,23 +863,26 @@ int run_host(const Call& c, void* stream) {
       if (!rc) rc = ok(cudaStreamWaitEvent(st, h.panel_in[i], 0));
     }
     if (!rc) {
-      const float beta = chunks == 1 ? c.beta : 1.f;
+      const float beta = chunks == 1 ? c.beta : 0.f;
       Call pc{0, 0, (int)rn, c.N, c.K - kl0, c.alpha, beta, dA + r0 * kp + kl0, lda_d,
               dB + (size_t)kl0 * np, (int)np, dD + r0 * np, (int)np};
       rc = run(pc, -1, st);
     }
-    if (!rc && separate_c) {  // D += beta * C over the panel
-      const int n4 = (int)(np / 4);
-      long long blocks = ((long long)rn * n4 + 255) / 256;
-      if (blocks > (long long)d->sms * 8) blocks = (long long)d->sms * 8;
-      float* dDp = dD + r0 * np;
-      const float* dCp = dC + r0 * np;
-      int rn_i = (int)rn;
-      float beta = c.beta;
+    if (!rc && chunks > 1) {  // D = (P0 + P1) + D + beta * C over the panel
+      int n4 = (int)(np / 4), rn_i = (int)rn;
+      const unsigned bx = (unsigned)((n4 + 255) / 256);
+      unsigned by = (unsigned)rn;
+      const unsigned cap = (unsigned)d->sms * 8 / bx;
+      if (by > cap) by = cap > 0 ? cap : 1;
       long long ld = (long long)np;
-      void* args[] = {&rn_i, (void*)&n4, &beta, (void*)&dCp, &ld, &dDp, &ld};
-      rc = ok(launch_pdl(reinterpret_cast<const void*>(&axpby_rows_kernel),
-                         dim3((unsigned)blocks), dim3(256), args, 0, st));
+      const float* p0 = dP0 + r0 * np;
+      const float* p1 = dP1 + r0 * np;
+      const float* x = separate_c ? dC + r0 * np : nullptr;
+      float* y = dD + r0 * np;
+      float beta = c.beta;
+      void* args[] = {&rn_i, &n4, &ld, (void*)&p0, (void*)&p1, &beta, (void*)&x, &y};
+      rc = ok(launch_pdl(reinterpret_cast<const void*>(&combine_rows_kernel), dim3(bx, by),
+                         dim3(256), args, 0, st));
     }
     if (!rc) rc = ok(cudaEventRecord(h.gemm[i], st));
     if (!rc) rc = ok(cudaStreamWaitEvent(h.d2h, h.gemm[i], 0));

@@ -144,20 +144,21 @@ int b2g_sgemm_ws(int transA, int transB, int M, int N, int K, float alpha, const
  * works more slowly).  The copies overlap the multiplication: for K >= 2048
  * the library copies A's columns and B's rows in three growing K chunks
  * (K/8, 3K/8, K/2) and then C on its own copy stream, while `stream`
- * multiplies each chunk into a device accumulator as soon as it has arrived;
- * the last chunk runs in row panels of about 1024 rows (multiples of 128
- * rows, at most 16 panels), the last panel cut into 3/4 and 1/4 when it has
- * 512 rows or more; each finished panel (plus beta * C) goes back to the host
- * on a second copy stream while the next one multiplies, so that only the
- * last, short return is exposed.  For K < 2048 it copies B, then A and C in
- * the same row panels (no cut), and multiplies each panel as it arrives.  Every step is ordered after
- * earlier work on `stream`, and the call's last copy is joined back into
- * `stream`.  Sums split over K chunks are rounded once per chunk, within the
- * same error bound.  C holds
- * the result once `stream` has completed the call's work (for instance after
- * cudaStreamSynchronize(stream)); until then the host buffers must stay valid
- * and unmodified.  Device staging (A, B and C with rows padded to a multiple
- * of 4 floats) is a library-owned buffer per device, grown when needed and
+ * multiplies each chunk, as soon as it has arrived, into a device product of
+ * its own; the last chunk runs in row panels of about 1024 rows (multiples of
+ * 128 rows, at most 16 panels), the last panel cut into 3/4 and 1/4 when it
+ * has 512 rows or more; each finished panel is added up, (P0 + P1) + P2 +
+ * beta * C, and goes back to the host on a second copy stream while the next
+ * one multiplies, so that only the last, short return is exposed.  For
+ * K < 2048 it copies B, then A and C in the same row panels (no cut), and
+ * multiplies each panel as it arrives.  Every step is ordered after earlier
+ * work on `stream`, and the call's last copy is joined back into `stream`.
+ * Sums split over K chunks are rounded once per chunk, within the same error
+ * bound.  C holds the result once `stream` has completed the call's work (for
+ * instance after cudaStreamSynchronize(stream)); until then the host buffers
+ * must stay valid and unmodified.  Device staging (A, B and C with rows padded
+ * to a multiple of 4 floats, and for K >= 2048 two more M x N products) is a
+ * library-owned buffer per device, grown when needed and
  * freed by b2g_release_workspaces; calls on different streams are ordered one
  * after the other.  Same return codes as b2g_sgemm, plus B2G_ERR_UNSUPPORTED
  * while `stream` is being captured into a graph and B2G_ERR_CUDA when a copy
