@@ -10,6 +10,7 @@
 
 #include <atomic>
 #include <cstdint>
+#include <cmath>
 #include <cstring>
 #include <mutex>
 
@@ -197,6 +198,7 @@ const PlanGroup kGroups[] = {
     {kPlansT128x128, &kNumPlansT128x128}, {kPlansGeneral, &kNumPlansGeneral},
     {kPlansSkinny, &kNumPlansSkinny},     {kPlansSkinnyTma, &kNumPlansSkinnyTma},
     {kPlansCs, &kNumPlansCs},           {kPlansTmaO5, &kNumPlansTmaO5},
+    {kPlansWarpk, &kNumPlansWarpk},
 };
 
 int num_plans() {
@@ -293,6 +295,40 @@ const char* const kTileTwins[][2] = {
     {"pret_128x64x32_s3_o5", "pret_64x128x32_s3_o5"},
 };
 
+// The one-launch small-problem plans (wk_*: one CTA per output tile, its k
+// range split between the CTA's warps) against the split-tail plan that the
+// next rule names, by a model fitted to GB300 timings of back-to-back calls:
+// a wk call takes 2.0 + waves x (2.4 + BM x BN x K x 4.6e-6) us (waves of one
+// CTA per SM; each wave pays its CTAs' start, first copies and reduction),
+// the split-tail plan 7.4 + (M N K of the whole call) x 3.7e-8 us, and a wk
+// plan is taken when its estimate is 3% lower.  Measured (us; split tail /
+// wk_32x64x16_g8 / wk_64x64x16_g4): 128^3 10.4 / 8.4 / 7.2, 256^3 10.2 / 7.2
+// / 8.1, 384^3 9.9 / 7.9 / 10.5, 512^3 12.4 / 9.2 / 13.2, 768^3 23.7 / 24.0 /
+// 18.6, 1024^3 47.6 / 59.2 / 47.0; strided batches (split tail / the wk plan
+// the model picks): 128 x 128^3 14.6 / 27.2, 64 x 256^3 48.4 / 53.2,
+// 16 x 384^3 35.6 / 41.0, 4 x 512^3 29.6 / 26.2, 2 x 768^3 40.4 / 36.8.
+// Returns the wk plan with the smaller estimate (the larger tile on a tie:
+// fewer waves), or -1 when the split-tail plan should run (many waves of
+// small tiles, or few tiles over a long k range such as 128 x 128 x 32768).
+int warpk_choice(const Call& c) {
+  int sms = 152;
+  DeviceState* d = nullptr;
+  if (device_state(&d) == 0) sms = d->sms;
+  const double b = c.batch > 0 ? c.batch : 1;
+  double best = 0.97 * (7.4 + (double)c.M * c.N * (double)c.K * b * 3.7e-8);
+  int pick = -1;
+  for (const char* name : {"wk_32x64x16_g8", "wk_64x64x16_g4"}) {
+    const int i = plan_index(name);
+    if (i < 0 || !plan_accepts(*plan_at(i), c)) continue;
+    const Plan& pl = *plan_at(i);
+    const double tiles = (double)((c.M + pl.BM - 1) / pl.BM) * ((c.N + pl.BN - 1) / pl.BN) * b;
+    const double waves = std::ceil(tiles / sms);
+    const double t = 2.0 + waves * (2.4 + pl.BM * pl.BN * (double)c.K * 4.6e-6);
+    if (t <= best) best = t, pick = i;
+  }
+  return pick;
+}
+
 int select_plan(const Call& c, int* fallback = nullptr) {
   const int cls = operand_class(c);
   // The work of the whole call: a batch of products amortises a
@@ -305,6 +341,10 @@ int select_plan(const Call& c, int* fallback = nullptr) {
     if (r.cls == cls && c.M >= r.m_min && c.M <= r.m_max && c.N >= r.n_min && c.N <= r.n_max &&
         mnk >= r.mnk_min && mnk < r.mnk_max) {
       int i = plan_index(r.plan);
+      if (std::strncmp(r.plan, "wk_", 3) == 0) {  // the wk plans, or the next rule
+        i = warpk_choice(c);
+        if (i < 0) continue;
+      }
       if (i >= 0 && plan_accepts(*plan_at(i), c)) {
         if (fallback) {
           const int f = r.fallback ? plan_index(r.fallback) : i;

@@ -53,5 +53,7 @@ extern const Plan kPlansCs[];
 extern const int kNumPlansCs;
 extern const Plan kPlansTmaO5[];
 extern const int kNumPlansTmaO5;
+extern const Plan kPlansWarpk[];
+extern const int kNumPlansWarpk;
 
 }  // namespace b2g

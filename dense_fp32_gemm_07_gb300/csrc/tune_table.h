@@ -46,10 +46,15 @@ const TuneRule kTuneTable[] = {
     {kClassFast, 0, 8, 0, kInf, 0, "skinny_m8", nullptr},
     {kClassFast, 9, 16, 0, kInf, 0, "skinny_m16", nullptr},
     {kClassFast, 17, 32, 0, kInf, 0, "skinny_m32", nullptr},
-    // up to ~1e9 multiply-adds the transpose costs about what it saves; the
-    // packed-FMA form of the k-chunked kernel (two CTAs per SM) beats the
-    // scalar one by 0.35-0.9 us a call (128^3 8.52 -> 7.71 us, 512^3 13.66 ->
-    // 13.31, 1000 x 1024 x 776 43.5 -> 42.1; CUDA-graph replay)
+    // up to ~1e9 multiply-adds: one launch, one CTA per small output tile
+    // with its k range split between the CTA's warps (wk_32x64x16_g8 or
+    // wk_64x64x16_g4, whichever a wave model expects faster), unless the
+    // split-tail plan of the next rule is expected faster (few tiles, long k)
+    {kClassFast, 0, kInf, 0, kInf, 0, "wk_32x64x16_g8", nullptr, 1.0e9},
+    // the transpose costs about what it saves here; the packed-FMA form of
+    // the k-chunked kernel (two CTAs per SM) beats the scalar one by 0.35-0.9
+    // us a call (128^3 8.52 -> 7.71 us, 512^3 13.66 -> 13.31, 1000 x 1024 x
+    // 776 43.5 -> 42.1; CUDA-graph replay)
     {kClassFast, 0, kInf, 0, kInf, 0, "tma_64x128x16_s6_o5", nullptr, 1.0e9},
     // larger: A transposed into the workspace, then the transposed-layout
     // kernel (its 64 x 128 twin when that pads less, e.g. M <= 64)

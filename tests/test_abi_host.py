@@ -53,7 +53,7 @@ def test_version_and_plans(b2g):
         info = b2g.b2g_plan_info(i)
         assert info["BM"] > 0 and info["BN"] > 0 and info["BK"] % 4 == 0
         assert info["threads"] % 32 == 0 and info["smem_bytes"] <= 227 * 1024
-        assert n.startswith(("tma", "gen", "pre", "pack", "skinny", "cs"))
+        assert n.startswith(("tma", "gen", "pre", "pack", "skinny", "cs", "wk"))
     assert b2g.b2g_plan_name(len(names)) is None
     with pytest.raises(b2g.B2GError):
         b2g.b2g_plan_info(-1)
@@ -109,7 +109,12 @@ def test_tune_table_classes(b2g):
     assert _plan(b2g, 0, 0, 16, 1024, 8192, 1.0, FAKE, 8192, FAKE, 1024, FAKE, 1024) == "skinny_m16"
     # skinny M with N % 4 != 0 takes a tiled plan
     assert _plan(b2g, 0, 0, 16, 4095, 4096, 1.0, FAKE, 4096, FAKE, 4096, FAKE, 4096).startswith("tma_")
-    assert _plan(b2g, 0, 0, 64, 64, 64, 1.0, FAKE, 64, FAKE, 64, FAKE, 64).startswith("tma_")
+    # small products: one launch, the k range split between a CTA's warps;
+    # few tiles over a long k range keep the split-tail plan
+    assert _plan(b2g, 0, 0, 64, 64, 64, 1.0, FAKE, 64, FAKE, 64, FAKE, 64) == "wk_32x64x16_g8"
+    assert _plan(b2g, 0, 0, 512, 512, 512, 1.0, FAKE, 512, FAKE, 512, FAKE, 512) == "wk_32x64x16_g8"
+    assert _plan(b2g, 0, 0, 768, 768, 768, 1.0, FAKE, 768, FAKE, 768, FAKE, 768) == "wk_64x64x16_g4"
+    assert _plan(b2g, 0, 0, 128, 128, 32768, 1.0, FAKE, 32768, FAKE, 128, FAKE, 128).startswith("tma_")
     # odd leading dimension -> operands packed into the workspace first
     assert _plan(b2g, 0, 0, 1000, 1025, 777, 0.75, FAKE, 777, FAKE, 1025, FAKE, 1025).startswith("pack_")
     # misaligned base pointer -> packed
