@@ -301,23 +301,36 @@ const char* const kTileTwins[][2] = {
 // a wk call takes 2.0 + waves x (2.4 + BM x BN x K x 4.6e-6) us (waves of one
 // CTA per SM; each wave pays its CTAs' start, first copies and reduction),
 // the split-tail plan 7.4 + (M N K of the whole call) x 3.7e-8 us, and a wk
-// plan is taken when its estimate is 3% lower.  Measured (us; split tail /
+// plan is taken when its estimate is 3% lower (near a tie the wk plan's
+// second wave made it the slower one with operands out of L2: the ragged
+// 1000 x 1025 x 777, packed first, 50.9 us against 47.4).  Measured (us; split tail /
 // wk_32x64x16_g8 / wk_64x64x16_g4): 128^3 10.4 / 8.4 / 7.2, 256^3 10.2 / 7.2
 // / 8.1, 384^3 9.9 / 7.9 / 10.5, 512^3 12.4 / 9.2 / 13.2, 768^3 23.7 / 24.0 /
 // 18.6, 1024^3 47.6 / 59.2 / 47.0; strided batches (split tail / the wk plan
 // the model picks): 128 x 128^3 14.6 / 27.2, 64 x 256^3 48.4 / 53.2,
-// 16 x 384^3 35.6 / 41.0, 4 x 512^3 29.6 / 26.2, 2 x 768^3 40.4 / 36.8.
-// Returns the wk plan with the smaller estimate (the larger tile on a tie:
-// fewer waves), or -1 when the split-tail plan should run (many waves of
-// small tiles, or few tiles over a long k range such as 128 x 128 x 32768).
-int warpk_choice(const Call& c) {
+// 16 x 384^3 35.6 / 41.0, 4 x 512^3 29.6 / 26.2, 2 x 768^3 40.4 / 36.8;
+// 1000 x 1024 x 776 (split tail / wk 64 x 64) 42.2 / 37.0, with A stored
+// K x M 38.7 / 33.9, with B stored N x K 42.8 / 39.1.
+// Returns the plan of the family `rule_plan` names (wk_, wkT_, wkP_, wkR_:
+// the same kernel for each operand class) with the smaller estimate (the
+// larger tile on a tie: fewer waves), or -1 when the split-tail plan should
+// run (many waves of small tiles, or few tiles over a long k range such as
+// 128 x 128 x 32768).  A family's packing or transposing pass is the same as
+// its split-tail counterpart's, so the estimates leave it out.
+int warpk_choice(const Call& c, const char* rule_plan) {
   int sms = 152;
   DeviceState* d = nullptr;
   if (device_state(&d) == 0) sms = d->sms;
   const double b = c.batch > 0 ? c.batch : 1;
   double best = 0.97 * (7.4 + (double)c.M * c.N * (double)c.K * b * 3.7e-8);
   int pick = -1;
-  for (const char* name : {"wk_32x64x16_g8", "wk_64x64x16_g4"}) {
+  const char* us = std::strchr(rule_plan, '_');
+  const size_t fam = us ? (size_t)(us - rule_plan) : 0;
+  for (const char* tile : {"_32x64x16_g8", "_64x64x16_g4"}) {
+    char name[32];
+    if (fam == 0 || fam + std::strlen(tile) >= sizeof(name)) break;
+    std::memcpy(name, rule_plan, fam);
+    std::strcpy(name + fam, tile);
     const int i = plan_index(name);
     if (i < 0 || !plan_accepts(*plan_at(i), c)) continue;
     const Plan& pl = *plan_at(i);
@@ -341,8 +354,8 @@ int select_plan(const Call& c, int* fallback = nullptr) {
     if (r.cls == cls && c.M >= r.m_min && c.M <= r.m_max && c.N >= r.n_min && c.N <= r.n_max &&
         mnk >= r.mnk_min && mnk < r.mnk_max) {
       int i = plan_index(r.plan);
-      if (std::strncmp(r.plan, "wk_", 3) == 0) {  // the wk plans, or the next rule
-        i = warpk_choice(c);
+      if (std::strncmp(r.plan, "wk", 2) == 0) {  // a wk family's plan, or the next rule
+        i = warpk_choice(c, r.plan);
         if (i < 0) continue;
       }
       if (i >= 0 && plan_accepts(*plan_at(i), c)) {

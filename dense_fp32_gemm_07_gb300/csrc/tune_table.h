@@ -59,16 +59,23 @@ const TuneRule kTuneTable[] = {
     // larger: A transposed into the workspace, then the transposed-layout
     // kernel (its 64 x 128 twin when that pads less, e.g. M <= 64)
     {kClassFast, 0, kInf, 0, kInf, 1.0e9, "pre_128x64x32_s3_o5", "tmaX_128x128x16_s6_o2"},
+    // op(A) = A^T: small products in one launch (the wk kernel reading A
+    // stored K x M), larger ones on the transposed-layout kernel
+    {kClassFastTransA, 0, kInf, 0, kInf, 0, "wkT_32x64x16_g8", nullptr, 1.0e9},
     {kClassFastTransA, 0, kInf, 0, kInf, 0, "tmaT_128x64x32_s3_o5", nullptr},
     // op(B) = B^T on aligned operands: B^T (and A, unless it comes stored
     // K x M) transposed into the workspace by the 16-byte-vector transpose,
-    // then the transposed-layout kernel (4096^3: packing both operands with
-    // 4-byte moves cost 3.5% of the call); small calls take the 4-byte feed
+    // then the wk kernel (one launch) or the transposed-layout kernel
+    // (4096^3: packing both operands with 4-byte moves cost 3.5% of the
+    // call); small calls take the 4-byte feed
+    {kClassFastTransB, 0, kInf, 0, kInf, 5.0e7, "wkR_32x64x16_g8", "gen_64x64x16_s4", 1.0e9},
     {kClassFastTransB, 0, kInf, 0, kInf, 5.0e7, "pret_128x64x32_s3_o5", "gen_64x64x16_s4"},
     {kClassFastTransB, 0, kInf, 0, kInf, 0, "gen_64x64x16_s4", nullptr},
     // anything else (misaligned pointers, odd leading dimensions, K % 4 != 0,
-    // op(B) = B^T): pack A^T and B aligned into the workspace, then the
-    // transposed-layout kernel; the 4-byte feed needs no workspace
+    // op(B) = B^T): pack A^T and B aligned into the workspace, then the wk
+    // kernel (one launch) or the transposed-layout kernel; the 4-byte feed
+    // needs no workspace
+    {kClassGeneral, 0, kInf, 0, kInf, 5.0e7, "wkP_32x64x16_g8", "gen_64x64x16_s4", 1.0e9},
     {kClassGeneral, 0, kInf, 0, kInf, 5.0e7, "pack_128x64x32_s3_o5", "gen_64x64x16_s4"},
     {kClassGeneral, 0, kInf, 0, kInf, 0, "gen_64x64x16_s4", nullptr},
 };

@@ -9,7 +9,8 @@
 // takes one small output tile (BM x 64, BM = 32 * WM) and KG groups of WM
 // consumer warps take its k tiles in turn (k tile t goes to group t % KG),
 // each warp with the 8 x 8 register outer product of the FFMA plans (packed
-// two-lane FMAs, A k-chunked by a 3-D bulk-tensor view, B row-major).  When
+// two-lane FMAs, B row-major; A either row-major, k-chunked by a 3-D
+// bulk-tensor view, or stored K x M, landing transposed).  When
 // the groups are done, their partial tiles meet in the drained shared-memory
 // ring and are added in group order, then C = alpha * sum + beta * C is
 // written: one launch, no workspace.  Every output element is a fixed-order
@@ -25,7 +26,7 @@
 
 namespace b2g {
 
-template <int WM, int KG, int BK, int STAGES>
+template <int WM, int KG, int BK, int STAGES, int ALAY>
 struct WarpkCfg {
   static constexpr int BM = 32 * WM, BN = 64, TN = 8;
   static constexpr int kConsumerWarps = WM * KG;
@@ -38,17 +39,18 @@ struct WarpkCfg {
   static_assert(STAGES % KG == 0, "a ring slot always serves the same k group");
   static_assert(KG * BM * BN <= kRingFloats, "the groups' partial tiles fit in the ring");
   static_assert(BK % 4 == 0, "A is k-chunked by 4");
+  static_assert(ALAY == kAKChunk || ALAY == kAKMajor, "A's shared-memory layout");
 };
 
-template <int WM, int KG, int BK, int STAGES>
-__global__ void __launch_bounds__(WarpkCfg<WM, KG, BK, STAGES>::kThreads, 1)
+template <int WM, int KG, int BK, int STAGES, int ALAY>
+__global__ void __launch_bounds__(WarpkCfg<WM, KG, BK, STAGES, ALAY>::kThreads, 1)
     sgemm_warpk_kernel(const __grid_constant__ SgemmParams p,
                        const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB) {
-  using Cfg = WarpkCfg<WM, KG, BK, STAGES>;
+  using Cfg = WarpkCfg<WM, KG, BK, STAGES, ALAY>;
   constexpr int BM = Cfg::BM, BN = Cfg::BN, TN = Cfg::TN;
   extern __shared__ __align__(1024) unsigned char smem[];
-  float* sA = reinterpret_cast<float*>(smem);          // [STAGES][BK/4][BM][4]
+  float* sA = reinterpret_cast<float*>(smem);          // [STAGES][BK/4][BM][4] or [STAGES][BK][BM]
   float* sB = sA + STAGES * Cfg::kAStage;              // [STAGES][BK][BN]
   uint64_t* bars = reinterpret_cast<uint64_t*>(sA + Cfg::kRingFloats);
   const uint32_t full0 = smem_addr(bars);
@@ -88,7 +90,10 @@ __global__ void __launch_bounds__(WarpkCfg<WM, KG, BK, STAGES>::kThreads, 1)
         break;
       const uint32_t fb = full0 + 8 * stage;
       mbar_arrive_expect_tx(fb, Cfg::kStageBytes);
-      tma_load_4d(smem_addr(sA + stage * Cfg::kAStage), &tmA, 0, m0, kt * (BK / 4), bt, fb);
+      if constexpr (ALAY == kAKChunk)  // view {4, M, K/4, batch}
+        tma_load_4d(smem_addr(sA + stage * Cfg::kAStage), &tmA, 0, m0, kt * (BK / 4), bt, fb);
+      else  // A stored K x M: {M, K, batch}
+        tma_load_3d(smem_addr(sA + stage * Cfg::kAStage), &tmA, m0, kt * BK, bt, fb);
       tma_load_3d(smem_addr(sB + stage * Cfg::kBStage), &tmB, n0, kt * BK, bt, fb);
       ++issued;
       if (++stage == STAGES) stage = 0, phase ^= 1u;
@@ -106,10 +111,11 @@ __global__ void __launch_bounds__(WarpkCfg<WM, KG, BK, STAGES>::kThreads, 1)
   const int cw = warp - 1;
   const int g = cw / WM, wm = cw % WM;  // k group, warp row
   const int tr = lane >> 3, tc = lane & 7;
-  // thread rows wm*32 + tr + 4i (the 4 thread rows of a warp read 4
-  // consecutive 16-byte vectors of the k-chunked A); thread columns
-  // 4tc + 32(j >> 2) + (j & 3)
-  const int a_off = (wm * 32 + tr) * 4;
+  // Thread rows: wm*32 + tr + 4i with A k-chunked (the 4 thread rows of a
+  // warp read 4 consecutive 16-byte vectors), wm*32 + 4tr + (i & 3) + 16(i >> 2)
+  // with A transposed (one 16-byte load gives 4 rows at one k).  Thread
+  // columns 4tc + 32(j >> 2) + (j & 3).
+  const int a_off = ALAY == kAKChunk ? (wm * 32 + tr) * 4 : wm * 32 + 4 * tr;
   const int b_off = 4 * tc;
   float acc[8][TN];
 #pragma unroll
@@ -128,6 +134,21 @@ __global__ void __launch_bounds__(WarpkCfg<WM, KG, BK, STAGES>::kThreads, 1)
     }
     const float* As = sA + stage * Cfg::kAStage + a_off;
     const float* Bs = sB + stage * Cfg::kBStage + b_off;
+    if constexpr (ALAY == kAKMajor) {
+#pragma unroll
+      for (int k = 0; k < BK; ++k) {
+        const float4 a0 = *reinterpret_cast<const float4*>(As + k * BM);
+        const float4 a1 = *reinterpret_cast<const float4*>(As + k * BM + 16);
+        const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        float b[TN];
+#pragma unroll
+        for (int j4 = 0; j4 < TN / 4; ++j4) {
+          const float4 v = *reinterpret_cast<const float4*>(Bs + k * BN + 32 * j4);
+          b[4 * j4 + 0] = v.x, b[4 * j4 + 1] = v.y, b[4 * j4 + 2] = v.z, b[4 * j4 + 3] = v.w;
+        }
+        outer_product<5, TN>(acc, a, b);
+      }
+    } else {
 #pragma unroll
     for (int q = 0; q < BK / 4; ++q) {
       float4 a4[8];
@@ -149,6 +170,7 @@ __global__ void __launch_bounds__(WarpkCfg<WM, KG, BK, STAGES>::kThreads, 1)
         outer_product<5, TN>(acc, a, b);
       }
     }
+    }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * stage);
   }
@@ -160,7 +182,9 @@ __global__ void __launch_bounds__(WarpkCfg<WM, KG, BK, STAGES>::kThreads, 1)
   float* part = sA;  // [KG][BM][BN]: group g's partial tile
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    float* row = part + (g * BM + wm * 32 + tr + 4 * i) * BN + b_off;
+    const int r = ALAY == kAKChunk ? wm * 32 + tr + 4 * i
+                                   : wm * 32 + 4 * tr + (i & 3) + 16 * (i >> 2);
+    float* row = part + (g * BM + r) * BN + b_off;
 #pragma unroll
     for (int j4 = 0; j4 < TN / 4; ++j4)
       *reinterpret_cast<float4*>(row + 32 * j4) =
@@ -220,11 +244,11 @@ __global__ void __launch_bounds__(WarpkCfg<WM, KG, BK, STAGES>::kThreads, 1)
 }
 
 // One CTA per output tile (of every problem of a batch).
-template <int WM, int KG, int BK, int STAGES>
+template <int WM, int KG, int BK, int STAGES, int ALAY>
 cudaError_t launch_warpk(const SgemmParams& p, const CUtensorMap* tmA, const CUtensorMap* tmB,
                          int /*num_sms*/, cudaStream_t stream) {
-  using Cfg = WarpkCfg<WM, KG, BK, STAGES>;
-  auto kern = sgemm_warpk_kernel<WM, KG, BK, STAGES>;
+  using Cfg = WarpkCfg<WM, KG, BK, STAGES, ALAY>;
+  auto kern = sgemm_warpk_kernel<WM, KG, BK, STAGES, ALAY>;
   static std::atomic<int> opted[kMaxDevices];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
@@ -244,18 +268,32 @@ cudaError_t launch_warpk(const SgemmParams& p, const CUtensorMap* tmA, const CUt
                     dim3(Cfg::kThreads), args, Cfg::kSmemBytes, stream);
 }
 
-#define B2G_WARPK_PLAN(NAME, WM, KG, BK, ST)                                                     \
+#define B2G_WARPK_PLAN(NAME, WM, KG, BK, ST, ALAY, PRE)                                         \
   Plan {                                                                                         \
-    NAME, WarpkCfg<WM, KG, BK, ST>::BM, WarpkCfg<WM, KG, BK, ST>::BN, BK, ST,                    \
-        WarpkCfg<WM, KG, BK, ST>::TN, kAKChunk, kFeedTMA, WarpkCfg<WM, KG, BK, ST>::kThreads,    \
-        WarpkCfg<WM, KG, BK, ST>::kSmemBytes, &launch_warpk<WM, KG, BK, ST>, 0, nullptr         \
+    NAME, WarpkCfg<WM, KG, BK, ST, ALAY>::BM, WarpkCfg<WM, KG, BK, ST, ALAY>::BN, BK, ST,        \
+        WarpkCfg<WM, KG, BK, ST, ALAY>::TN, ALAY, kFeedTMA,                                      \
+        WarpkCfg<WM, KG, BK, ST, ALAY>::kThreads, WarpkCfg<WM, KG, BK, ST, ALAY>::kSmemBytes,    \
+        &launch_warpk<WM, KG, BK, ST, ALAY>, PRE, nullptr                                        \
   }
 
-// Fields: name, warp rows WM (BM = 32 WM), k groups KG, BK, stages.  No
-// occupancy function: the host then gives these plans no split tail.
+// Fields: name, warp rows WM (BM = 32 WM), k groups KG, BK, stages, A's layout
+// in shared memory, what runs before the kernel (as for the FFMA plans: 0
+// nothing, 2 both operands packed aligned with A transposed, 3 B^T (and A)
+// transposed with 16-byte vectors).  No occupancy function: the host then
+// gives these plans no split tail.
+//   wk_   row-major A, k-chunked (aligned operands)
+//   wkT_  A stored K x M (op(A) = A^T, aligned operands)
+//   wkP_  any operands, packed first
+//   wkR_  op(B) = B^T on aligned operands, transposed first
 const Plan kPlansWarpk[] = {
-    B2G_WARPK_PLAN("wk_32x64x16_g8", 1, 8, 16, 16),
-    B2G_WARPK_PLAN("wk_64x64x16_g4", 2, 4, 16, 16),
+    B2G_WARPK_PLAN("wk_32x64x16_g8", 1, 8, 16, 16, kAKChunk, 0),
+    B2G_WARPK_PLAN("wk_64x64x16_g4", 2, 4, 16, 16, kAKChunk, 0),
+    B2G_WARPK_PLAN("wkT_32x64x16_g8", 1, 8, 16, 16, kAKMajor, 0),
+    B2G_WARPK_PLAN("wkT_64x64x16_g4", 2, 4, 16, 16, kAKMajor, 0),
+    B2G_WARPK_PLAN("wkP_32x64x16_g8", 1, 8, 16, 16, kAKMajor, 2),
+    B2G_WARPK_PLAN("wkP_64x64x16_g4", 2, 4, 16, 16, kAKMajor, 2),
+    B2G_WARPK_PLAN("wkR_32x64x16_g8", 1, 8, 16, 16, kAKMajor, 3),
+    B2G_WARPK_PLAN("wkR_64x64x16_g4", 2, 4, 16, 16, kAKMajor, 3),
 };
 const int kNumPlansWarpk = sizeof(kPlansWarpk) / sizeof(kPlansWarpk[0]);
 

@@ -116,21 +116,27 @@ def test_tune_table_classes(b2g):
     assert _plan(b2g, 0, 0, 768, 768, 768, 1.0, FAKE, 768, FAKE, 768, FAKE, 768) == "wk_64x64x16_g4"
     assert _plan(b2g, 0, 0, 128, 128, 32768, 1.0, FAKE, 32768, FAKE, 128, FAKE, 128).startswith("tma_")
     # odd leading dimension -> operands packed into the workspace first
-    assert _plan(b2g, 0, 0, 1000, 1025, 777, 0.75, FAKE, 777, FAKE, 1025, FAKE, 1025).startswith("pack_")
-    # misaligned base pointer -> packed
-    assert _plan(b2g, 0, 0, 512, 512, 512, 1.0, FAKE + 4, 512, FAKE, 512, FAKE, 512).startswith("pack_")
+    assert _plan(b2g, 0, 0, 1000, 1025, 777, 0.75, FAKE, 777, FAKE, 1025, FAKE, 1025).startswith(
+        ("pack_", "wkP_"))
+    # misaligned base pointer -> packed (small: then the one-launch wk kernel)
+    assert _plan(b2g, 0, 0, 512, 512, 512, 1.0, FAKE + 4, 512, FAKE, 512, FAKE, 512) == "wkP_32x64x16_g8"
+    assert _plan(b2g, 0, 0, 2048, 2048, 2048, 1.0, FAKE + 4, 2048, FAKE, 2048, FAKE, 2048).startswith("pack_")
     # K not a multiple of 4 -> packed
-    assert _plan(b2g, 0, 0, 512, 512, 510, 1.0, FAKE, 512, FAKE, 512, FAKE, 512).startswith("pack_")
+    assert _plan(b2g, 0, 0, 512, 512, 510, 1.0, FAKE, 512, FAKE, 512, FAKE, 512).startswith("wkP_")
     # small general problems -> 4-byte feed (no workspace)
     assert _plan(b2g, 0, 0, 64, 64, 63, 1.0, FAKE, 64, FAKE, 64, FAKE, 64).startswith("gen_")
     # op(A) = A^T aligned -> transposed-layout bulk-tensor plan; op(B) = B^T
     # aligned -> B^T (and A) transposed with 16-byte vectors, then that plan
-    assert _plan(b2g, 1, 0, 512, 512, 512, 1.0, FAKE, 512, FAKE, 512, FAKE, 512).startswith("tmaT_")
-    assert _plan(b2g, 0, 1, 512, 512, 512, 1.0, FAKE, 512, FAKE, 512, FAKE, 512).startswith("pret_")
-    assert _plan(b2g, 1, 1, 512, 512, 512, 1.0, FAKE, 512, FAKE, 512, FAKE, 512).startswith("pret_")
+    # (small products of each class on the one-launch wk kernel)
+    assert _plan(b2g, 1, 0, 512, 512, 512, 1.0, FAKE, 512, FAKE, 512, FAKE, 512) == "wkT_32x64x16_g8"
+    assert _plan(b2g, 1, 0, 4096, 4096, 4096, 1.0, FAKE, 4096, FAKE, 4096, FAKE, 4096).startswith("tmaT_")
+    assert _plan(b2g, 0, 1, 512, 512, 512, 1.0, FAKE, 512, FAKE, 512, FAKE, 512) == "wkR_32x64x16_g8"
+    assert _plan(b2g, 1, 1, 512, 512, 512, 1.0, FAKE, 512, FAKE, 512, FAKE, 512) == "wkR_32x64x16_g8"
+    assert _plan(b2g, 0, 1, 4096, 4096, 4096, 1.0, FAKE, 4096, FAKE, 4096, FAKE, 4096).startswith("pret_")
     # op(B) = B^T with K % 4 != 0 or an odd leading dimension -> packed
-    assert _plan(b2g, 0, 1, 512, 512, 510, 1.0, FAKE, 512, FAKE, 510, FAKE, 512).startswith("pack_")
-    assert _plan(b2g, 0, 1, 512, 512, 512, 1.0, FAKE, 512, FAKE, 513, FAKE, 512).startswith("pack_")
+    assert _plan(b2g, 0, 1, 512, 512, 510, 1.0, FAKE, 512, FAKE, 510, FAKE, 512).startswith("wkP_")
+    assert _plan(b2g, 0, 1, 512, 512, 512, 1.0, FAKE, 512, FAKE, 513, FAKE, 512).startswith("wkP_")
+    assert _plan(b2g, 0, 1, 2048, 2048, 2048, 1.0, FAKE, 2048, FAKE, 2049, FAKE, 2048).startswith("pack_")
     # small op(B) = B^T calls -> 4-byte feed
     assert _plan(b2g, 0, 1, 64, 64, 64, 1.0, FAKE, 64, FAKE, 64, FAKE, 64).startswith("gen_")
 
@@ -199,11 +205,16 @@ def test_workspace_size_query(b2g):
     assert rc == 0 and n > 0 and n % (16 * 1024 * 4) == 0
     rc, n = b2g.b2g_sgemm_workspace_size(0, 0, 64, 64, 64, 1.0, FAKE, 63, FAKE, 64, FAKE, 64)
     assert rc == -2
-    # packing: A^T (K x round_up(M, 4)) and B (K x round_up(N, 4)), then the tail
+    # packing: A^T (K x round_up(M, 4)) and B (K x round_up(N, 4)), then the
+    # tail (none for the one-launch wk plans)
     BM, BN = plan_tile(b2g, 1000, 1025, 777, 777, 1025, 1025)
     rc, n = b2g.b2g_sgemm_workspace_size(0, 0, 1000, 1025, 777, 1.0, FAKE, 777, FAKE, 1025,
                                          FAKE, 1025)
-    assert rc == 0 and n == want_bytes(777 * (1000 + 1028) * 4, 1000, 1025, 777, BM, BN)
+    name = b2g.b2g_plan_name(b2g.b2g_sgemm_select_plan(0, 0, 1000, 1025, 777, 1.0, FAKE, 777,
+                                                        FAKE, 1025, FAKE, 1025))
+    base = 777 * (1000 + 1028) * 4
+    assert rc == 0 and n == (base if name.startswith("wk") else
+                             want_bytes(base, 1000, 1025, 777, BM, BN))
     assert b2g.b2g_release_workspaces() == 0  # nothing allocated yet: no CUDA call needed
 
 
@@ -222,6 +233,7 @@ def test_launch_count_query(b2g):
     assert count(16, 4096, 4096) == 1                # skinny, split-K summed in clusters
     assert count(16, 1024, 8192) == 2                # skinny split-K and its reduction
     assert count(1000, 1025, 777, lda=777) == 3      # one packing launch, GEMM, tail
+    assert count(512, 512, 510, lda=510) == 2        # one packing launch, one-launch wk GEMM
     rc, _ = b2g.b2g_sgemm_launch_count(0, 0, 64, 64, 64, 1.0, FAKE, 63, FAKE, 64, FAKE, 64)
     assert rc == -2
     # op(B) = B^T at 4096^3: transposes of A and of B^T, GEMM, tail reduction;

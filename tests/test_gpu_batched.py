@@ -53,7 +53,7 @@ CASES = [
     (16, 512, 256, 5, False, False, 0),     # skinny split-K
     (1024, 1024, 2048, 2, False, False, 0),  # pre-transposed A (workspace x batch)
     (1000, 1025, 777, 2, False, False, 0),   # packed operands
-    (400, 384, 512, 3, False, True, 0),      # op(B) = B^T: B^T and A transposed first (pret_)
+    (400, 384, 512, 3, False, True, 0),      # op(B) = B^T: B^T and A transposed first
     (400, 384, 512, 3, True, True, 4),       # the same with A stored K x M, padded strides
     (64, 64, 64, 1, False, False, 0),
 ]

@@ -52,7 +52,9 @@ def _kernel_nodes(cu, stream_handle, fn):
 
 @pytest.mark.parametrize("M,N,K,lda,alpha,beta", [
     (2048, 2048, 2048, 2048, 1.0, 0.5),   # transpose-first, split tail
+    (2000, 2000, 2001, 2001, 1.0, 0.5),   # packed operands (K % 4 != 0), split tail
     (1000, 1025, 777, 777, 0.75, -1.25),  # packed operands (odd lda), split tail
+    (512, 512, 510, 510, 1.0, 0.5),       # packed operands (K % 4 != 0), one-launch wk GEMM
     (16, 4096, 4096, 4096, 1.0, 1.0),     # skinny, k slabs summed in the cluster
     (16, 1024, 8192, 8192, 1.0, 1.0),     # skinny, streaming kernel + split-K reduction
     (256, 256, 64, 64, 1.0, 0.0),         # one kernel, no split (64 k)

@@ -252,11 +252,13 @@ def test_square4096_transposed_operands_full(tb, trans):
     check(dC.cpu().numpy(), ref, bound, f"square4096 trans {trans}")
 
 
-@pytest.mark.parametrize("shape", [(600, 520, 1024), (1000, 1028, 776), (64, 4096, 512)])
+@pytest.mark.parametrize("shape", [(600, 520, 1024), (1000, 1028, 776), (64, 4096, 512),
+                                   (1100, 1028, 1024)])
 @pytest.mark.parametrize("transA", [False, True])
 def test_transposed_b_plans(tb, shape, transA):
-    """op(B) = B^T on aligned operands above 5e7 multiply-adds: the pret_
-    plans (both tile shapes), split tail included."""
+    """op(B) = B^T on aligned operands above 5e7 multiply-adds: B^T (and A)
+    transposed first, then the one-launch wkR_ plans below about 1e9
+    multiply-adds or the pret_ plans (both tile shapes, split tail included)."""
     torch, b2g = tb
     M, N, K = shape
     rng = np.random.default_rng(M + N + K + transA)
@@ -266,7 +268,7 @@ def test_transposed_b_plans(tb, shape, transA):
     ref, bound, _ = oracle.sgemm(A, B, C, 0.5, 1.5, transA=transA, transB=True)
     plan = b2g.b2g_plan_name(b2g.b2g_sgemm_select_plan(int(transA), 1, M, N, K, 0.5, 1 << 20,
                                                         A.shape[1], 1 << 20, K, 1 << 20, N))
-    assert plan.startswith("pret_"), plan
+    assert plan.startswith("pret_" if M * N * K >= 1.0e9 else ("pret_", "wkR_")), plan
     got, rc, guard = gemm(b2g, torch, A, B, C, 0.5, 1.5, transA, True)
     assert rc == 0 and guard
     check(got, ref, bound, f"{shape} transA={transA} {plan}")
