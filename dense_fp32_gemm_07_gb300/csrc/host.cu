@@ -347,7 +347,8 @@ int select_plan(const Call& c, int* fallback = nullptr) {
   // The work of the whole call: a batch of products amortises a
   // transpose-first plan like one large product (one launch each for all),
   // once each product has ~5e7 multiply-adds (measured: 32 x 512^3 171.6 us
-  // against 203.1 on the small-problem plan; 64 x 256^3 66.7 against 60.1).
+  // against 203.1 on the k-chunked split-tail plan; 64 x 256^3 66.7 against
+  // 60.1).
   const double per = (double)c.M * c.N * c.K;
   const double mnk = c.batch > 1 && per >= 5.0e7 ? per * c.batch : per;
   for (const TuneRule& r : kTuneTable) {

@@ -3,7 +3,7 @@
 // thread-block cluster, their sums added through distributed shared memory
 // in slice order (one launch, no workspace, no reduction kernel).  The
 // kernel is the 64 x 128 tile, 16-k stage, k-chunked-A kernel of the
-// small-problem plan (tma_64x128x16_s6_o2) in that form, compiled in its own
+// tma_64x128x16_s6_o2 plan in that form, compiled in its own
 // translation unit; the plans differ only in the most k slices per tile
 // (2, 4, 8 -- the portable cluster size -- or 16).  Fields as in plans_tma.cu, then the
 // largest cluster.

@@ -1,7 +1,8 @@
-// plans_tma_o5.cu -- the small-problem kernel (64 x 128 tiles, 16-k stages,
-// 6 stages, A k-chunked by a 3-D bulk-tensor view: no transpose before it)
-// with packed two-lane FP32 FMAs instead of scalar ones, in its own
-// translation unit.  Fields as in plans_tma.cu.
+// plans_tma_o5.cu -- the split-tail kernel for products below about 1e9
+// multiply-adds that the one-launch wk_ plans leave to it (64 x 128 tiles,
+// 16-k stages, 6 stages, A k-chunked by a 3-D bulk-tensor view: no transpose
+// before it) with packed two-lane FP32 FMAs instead of scalar ones, in its
+// own translation unit.  Fields as in plans_tma.cu.
 #include "plan_registry.h"
 #include "sgemm_ffma.cuh"
 
