@@ -326,7 +326,7 @@ int warpk_choice(const Call& c, const char* rule_plan) {
   int pick = -1;
   const char* us = std::strchr(rule_plan, '_');
   const size_t fam = us ? (size_t)(us - rule_plan) : 0;
-  for (const char* tile : {"_32x64x16_g8", "_64x64x16_g4"}) {
+  for (const char* tile : {"_32x64x16_g8", "_64x64x16_g4", "_64x128x16_g2"}) {
     char name[32];
     if (fam == 0 || fam + std::strlen(tile) >= sizeof(name)) break;
     std::memcpy(name, rule_plan, fam);

@@ -6,8 +6,9 @@
 // into slices that write partial sums to a workspace and add them in a
 // second kernel: two launches, the partial sums' round trip through L2 and a
 // dependency between them, about 8 us a call even at 128^3.  Here one CTA
-// takes one small output tile (BM x 64, BM = 32 * WM) and KG groups of WM
-// consumer warps take its k tiles in turn (k tile t goes to group t % KG),
+// takes one small output tile (BM x BN = 32 WM x 64 WN) and KG groups of
+// WM x WN consumer warps take its k tiles in turn (k tile t goes to group
+// t % KG),
 // each warp with the 8 x 8 register outer product of the FFMA plans (packed
 // two-lane FMAs, B row-major; A either row-major, k-chunked by a 3-D
 // bulk-tensor view, or stored K x M, landing transposed).  When
@@ -26,10 +27,11 @@
 
 namespace b2g {
 
-template <int WM, int KG, int BK, int STAGES, int ALAY>
+template <int WM, int WN, int KG, int BK, int STAGES, int ALAY>
 struct WarpkCfg {
-  static constexpr int BM = 32 * WM, BN = 64, TN = 8;
-  static constexpr int kConsumerWarps = WM * KG;
+  static constexpr int BM = 32 * WM, BN = 64 * WN, TN = 8;
+  static constexpr int kGroupWarps = WM * WN;  // the warps of one k group
+  static constexpr int kConsumerWarps = kGroupWarps * KG;
   static constexpr int kConsumers = kConsumerWarps * 32;
   static constexpr int kThreads = kConsumers + 32;
   static constexpr int kAStage = BM * BK, kBStage = BK * BN;  // floats
@@ -42,12 +44,12 @@ struct WarpkCfg {
   static_assert(ALAY == kAKChunk || ALAY == kAKMajor, "A's shared-memory layout");
 };
 
-template <int WM, int KG, int BK, int STAGES, int ALAY>
-__global__ void __launch_bounds__(WarpkCfg<WM, KG, BK, STAGES, ALAY>::kThreads, 1)
+template <int WM, int WN, int KG, int BK, int STAGES, int ALAY>
+__global__ void __launch_bounds__(WarpkCfg<WM, WN, KG, BK, STAGES, ALAY>::kThreads, 1)
     sgemm_warpk_kernel(const __grid_constant__ SgemmParams p,
                        const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB) {
-  using Cfg = WarpkCfg<WM, KG, BK, STAGES, ALAY>;
+  using Cfg = WarpkCfg<WM, WN, KG, BK, STAGES, ALAY>;
   constexpr int BM = Cfg::BM, BN = Cfg::BN, TN = Cfg::TN;
   extern __shared__ __align__(1024) unsigned char smem[];
   float* sA = reinterpret_cast<float*>(smem);          // [STAGES][BK/4][BM][4] or [STAGES][BK][BM]
@@ -62,7 +64,7 @@ __global__ void __launch_bounds__(WarpkCfg<WM, KG, BK, STAGES, ALAY>::kThreads, 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, WM);
+      mbar_init(empty0 + 8 * s, Cfg::kGroupWarps);
     }
     *failed = 0;
     fence_mbar_init();
@@ -109,14 +111,15 @@ __global__ void __launch_bounds__(WarpkCfg<WM, KG, BK, STAGES, ALAY>::kThreads, 
 
   // --------------------------------------------------------------- consumers
   const int cw = warp - 1;
-  const int g = cw / WM, wm = cw % WM;  // k group, warp row
+  const int g = cw / Cfg::kGroupWarps;  // k group
+  const int wm = cw % Cfg::kGroupWarps % WM, wn = cw % Cfg::kGroupWarps / WM;  // warp tile
   const int tr = lane >> 3, tc = lane & 7;
   // Thread rows: wm*32 + tr + 4i with A k-chunked (the 4 thread rows of a
   // warp read 4 consecutive 16-byte vectors), wm*32 + 4tr + (i & 3) + 16(i >> 2)
   // with A transposed (one 16-byte load gives 4 rows at one k).  Thread
   // columns 4tc + 32(j >> 2) + (j & 3).
   const int a_off = ALAY == kAKChunk ? (wm * 32 + tr) * 4 : wm * 32 + 4 * tr;
-  const int b_off = 4 * tc;
+  const int b_off = wn * 64 + 4 * tc;
   float acc[8][TN];
 #pragma unroll
   for (int i = 0; i < 8; ++i)
@@ -244,11 +247,11 @@ __global__ void __launch_bounds__(WarpkCfg<WM, KG, BK, STAGES, ALAY>::kThreads, 
 }
 
 // One CTA per output tile (of every problem of a batch).
-template <int WM, int KG, int BK, int STAGES, int ALAY>
+template <int WM, int WN, int KG, int BK, int STAGES, int ALAY>
 cudaError_t launch_warpk(const SgemmParams& p, const CUtensorMap* tmA, const CUtensorMap* tmB,
                          int /*num_sms*/, cudaStream_t stream) {
-  using Cfg = WarpkCfg<WM, KG, BK, STAGES, ALAY>;
-  auto kern = sgemm_warpk_kernel<WM, KG, BK, STAGES, ALAY>;
+  using Cfg = WarpkCfg<WM, WN, KG, BK, STAGES, ALAY>;
+  auto kern = sgemm_warpk_kernel<WM, WN, KG, BK, STAGES, ALAY>;
   static std::atomic<int> opted[kMaxDevices];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
@@ -268,15 +271,17 @@ cudaError_t launch_warpk(const SgemmParams& p, const CUtensorMap* tmA, const CUt
                     dim3(Cfg::kThreads), args, Cfg::kSmemBytes, stream);
 }
 
-#define B2G_WARPK_PLAN(NAME, WM, KG, BK, ST, ALAY, PRE)                                         \
+#define B2G_WARPK_PLAN(NAME, WM, WN, KG, BK, ST, ALAY, PRE)                                     \
   Plan {                                                                                         \
-    NAME, WarpkCfg<WM, KG, BK, ST, ALAY>::BM, WarpkCfg<WM, KG, BK, ST, ALAY>::BN, BK, ST,        \
-        WarpkCfg<WM, KG, BK, ST, ALAY>::TN, ALAY, kFeedTMA,                                      \
-        WarpkCfg<WM, KG, BK, ST, ALAY>::kThreads, WarpkCfg<WM, KG, BK, ST, ALAY>::kSmemBytes,    \
-        &launch_warpk<WM, KG, BK, ST, ALAY>, PRE, nullptr                                        \
+    NAME, WarpkCfg<WM, WN, KG, BK, ST, ALAY>::BM, WarpkCfg<WM, WN, KG, BK, ST, ALAY>::BN, BK,    \
+        ST, WarpkCfg<WM, WN, KG, BK, ST, ALAY>::TN, ALAY, kFeedTMA,                              \
+        WarpkCfg<WM, WN, KG, BK, ST, ALAY>::kThreads,                                            \
+        WarpkCfg<WM, WN, KG, BK, ST, ALAY>::kSmemBytes, &launch_warpk<WM, WN, KG, BK, ST, ALAY>, \
+        PRE, nullptr                                                                             \
   }
 
-// Fields: name, warp rows WM (BM = 32 WM), k groups KG, BK, stages, A's layout
+// Fields: name, warp tiles WM x WN (BM = 32 WM, BN = 64 WN), k groups KG, BK,
+// stages, A's layout
 // in shared memory, what runs before the kernel (as for the FFMA plans: 0
 // nothing, 2 both operands packed aligned with A transposed, 3 B^T (and A)
 // transposed with 16-byte vectors).  No occupancy function: the host then
@@ -286,14 +291,18 @@ cudaError_t launch_warpk(const SgemmParams& p, const CUtensorMap* tmA, const CUt
 //   wkP_  any operands, packed first
 //   wkR_  op(B) = B^T on aligned operands, transposed first
 const Plan kPlansWarpk[] = {
-    B2G_WARPK_PLAN("wk_32x64x16_g8", 1, 8, 16, 16, kAKChunk, 0),
-    B2G_WARPK_PLAN("wk_64x64x16_g4", 2, 4, 16, 16, kAKChunk, 0),
-    B2G_WARPK_PLAN("wkT_32x64x16_g8", 1, 8, 16, 16, kAKMajor, 0),
-    B2G_WARPK_PLAN("wkT_64x64x16_g4", 2, 4, 16, 16, kAKMajor, 0),
-    B2G_WARPK_PLAN("wkP_32x64x16_g8", 1, 8, 16, 16, kAKMajor, 2),
-    B2G_WARPK_PLAN("wkP_64x64x16_g4", 2, 4, 16, 16, kAKMajor, 2),
-    B2G_WARPK_PLAN("wkR_32x64x16_g8", 1, 8, 16, 16, kAKMajor, 3),
-    B2G_WARPK_PLAN("wkR_64x64x16_g4", 2, 4, 16, 16, kAKMajor, 3),
+    B2G_WARPK_PLAN("wk_32x64x16_g8", 1, 1, 8, 16, 16, kAKChunk, 0),
+    B2G_WARPK_PLAN("wk_64x64x16_g4", 2, 1, 4, 16, 16, kAKChunk, 0),
+    B2G_WARPK_PLAN("wk_64x128x16_g2", 2, 2, 2, 16, 16, kAKChunk, 0),
+    B2G_WARPK_PLAN("wkT_32x64x16_g8", 1, 1, 8, 16, 16, kAKMajor, 0),
+    B2G_WARPK_PLAN("wkT_64x64x16_g4", 2, 1, 4, 16, 16, kAKMajor, 0),
+    B2G_WARPK_PLAN("wkT_64x128x16_g2", 2, 2, 2, 16, 16, kAKMajor, 0),
+    B2G_WARPK_PLAN("wkP_32x64x16_g8", 1, 1, 8, 16, 16, kAKMajor, 2),
+    B2G_WARPK_PLAN("wkP_64x64x16_g4", 2, 1, 4, 16, 16, kAKMajor, 2),
+    B2G_WARPK_PLAN("wkP_64x128x16_g2", 2, 2, 2, 16, 16, kAKMajor, 2),
+    B2G_WARPK_PLAN("wkR_32x64x16_g8", 1, 1, 8, 16, 16, kAKMajor, 3),
+    B2G_WARPK_PLAN("wkR_64x64x16_g4", 2, 1, 4, 16, 16, kAKMajor, 3),
+    B2G_WARPK_PLAN("wkR_64x128x16_g2", 2, 2, 2, 16, 16, kAKMajor, 3),
 };
 const int kNumPlansWarpk = sizeof(kPlansWarpk) / sizeof(kPlansWarpk[0]);
 

@@ -232,8 +232,8 @@ def test_launch_count_query(b2g):
     assert count(4096, 4096, 4096) == 3              # transpose, GEMM, tail reduction
     assert count(16, 4096, 4096) == 1                # skinny, split-K summed in clusters
     assert count(16, 1024, 8192) == 2                # skinny split-K and its reduction
-    assert count(1000, 1025, 777, lda=777) == 3      # one packing launch, GEMM, tail
-    assert count(512, 512, 510, lda=510) == 2        # one packing launch, one-launch wk GEMM
+    assert count(1000, 1025, 777, lda=777) == 2      # one packing launch, one-launch wk GEMM
+    assert count(4096, 4096, 4095, lda=4095) == 3    # one packing launch, GEMM, tail
     rc, _ = b2g.b2g_sgemm_launch_count(0, 0, 64, 64, 64, 1.0, FAKE, 63, FAKE, 64, FAKE, 64)
     assert rc == -2
     # op(B) = B^T at 4096^3: transposes of A and of B^T, GEMM, tail reduction;
