@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <cmath>
@@ -422,6 +423,55 @@ int skinny_splits(const Plan& pl, const Call& c, int* kc) {
 // 128-k slices; 32 k gained nothing more (17.25)
 constexpr int kMinSliceK = 64;
 
+// Estimated time (us) of a persistent FFMA grid whose work units are
+// `first` whole tiles and then (tiles - first) tiles cut into S k slices,
+// unit u going to CTA u mod G and CTA b to SM b mod sms (so SM 0 carries the
+// most).  An SM's CTAs run side by side until the shortest is done; each
+// phase runs at the FP32 pipe efficiency of the consumer warps still active
+// (12 or more 0.88, 8 0.85, 4 0.40) and every unit pays one k tile of
+// overhead (its fill and epilogue).  A split adds its reduction: the slices
+// written and read back, C read and written, at 5.5 TB/s, plus 2 us.
+// Fitted to 20 GB300 timings of square products from 1152^3 to 4096^3 with
+// chosen splits (3% root-mean-square error).
+double tail_time_us(const Plan& pl, long long tiles, long long kt, int sms, int occ,
+                    long long first, long long S, bool read_c) {
+  const long long G = (long long)sms * occ;
+  const long long f = S > 1 ? first : tiles;
+  const long long ns = S > 1 ? (tiles - first) * S : 0;
+  const long long slice = (kt + S - 1) / S;
+  double loads[8];
+  const int n = occ < 8 ? occ : 8;
+  for (int i = 0; i < n; ++i) {
+    const long long b = (long long)i * sms;
+    const long long whole = b < f ? (f - b + G - 1) / G : 0;
+    const long long sl = b < ns ? (ns - b + G - 1) / G : 0;
+    loads[i] = (double)(whole * (kt + 1) + sl * (slice + 1));
+  }
+  std::sort(loads, loads + n);
+  const int cw = pl.threads / 32 - 1;  // consumer warps per CTA
+  double t = 0.0, prev = 0.0;
+  for (int i = 0; i < n; ++i) {
+    const int active = n - i, w = active * cw;
+    const double e = w >= 12 ? 0.88 : w >= 8 ? 0.85 : w >= 4 ? 0.40 : 0.20;
+    t += active * (loads[i] - prev) / e;
+    prev = loads[i];
+  }
+  t *= (double)pl.BM * pl.BN * pl.BK / (128.0 * 2070.0);
+  if (S > 1)
+    t += (double)(tiles - first) * pl.BM * pl.BN * 4.0 * (2.0 * S + 1.0 + (read_c ? 1.0 : 0.0)) /
+             5.5e6 +
+         2.0;
+  return t;
+}
+
+// The split: the rule above, unless the balance model expects another split
+// (all of the last two or three rounds' tiles cut, or more slices) to be at
+// least 3% faster.  Measured (us, rule -> chosen): 1152^3 70.8 -> 63.1 (all
+// 162 tiles in 4 slices), 1664^3 178.7 -> 157.8 (338 tiles in 4 slices, no
+// split before: 34 SMs ran three tiles, the rest two), 2560^3 546.8 -> 513.7
+// (the 344 tiles after the first round in 2 slices); 1408^3 and 3072^3, where
+// the model's alternatives measured slower (116.1 and 876.3 against 104.7
+// and 863.0), keep the rule's choice.
 int tail_split(const Plan& pl, const Call& c, int* first) {
   *first = 0;
   if (is_skinny(pl) || !pl.occupancy || pl.cluster_max) return 1;
@@ -433,11 +483,25 @@ int tail_split(const Plan& pl, const Call& c, int* first) {
   if (tiles <= 0 || G <= 0) return 1;
   const long long q = tiles / G, r = tiles - q * G;
   if (r == 0) return 1;
-  long long S = G / r;
   const long long smax = c.K / kMinSliceK;
+  long long S = G / r;
   if (S > smax) S = smax;
+  long long f = q * G;
+  if (S < 2) S = 1, f = 0;
+  const long long kt = (c.K + pl.BK - 1) / pl.BK;
+  const bool read_c = c.beta != 0.f;
+  const double rule = tail_time_us(pl, tiles, kt, sms, occ, f, S, read_c);
+  double best = 0.97 * rule;
+  for (long long qq = q >= 2 ? q - 2 : 0; qq <= q; ++qq) {
+    if (qq * G >= tiles) continue;
+    for (long long s = 1; s <= smax && s <= 16; ++s) {
+      if (s == 1 && qq != q) continue;  // no split: one candidate
+      const double t = tail_time_us(pl, tiles, kt, sms, occ, qq * G, s, read_c);
+      if (t < best) best = t, S = s, f = s > 1 ? qq * G : 0;
+    }
+  }
   if (S < 2) return 1;
-  *first = (int)(q * G);
+  *first = (int)f;
   return (int)S;
 }
 

@@ -145,15 +145,57 @@ def test_tune_table_classes(b2g):
 NO_DEVICE_SLOTS = 152 * 4
 
 
-def split_tail(M, N, K, BM, BN, slots=NO_DEVICE_SLOTS):
+def _tail_time(tiles, kt, sms, occ, first, S, BM, BN, BK, cw, read_c):
+    """The host's estimate of a persistent grid's time (us) for a split."""
+    G = sms * occ
+    f = first if S > 1 else tiles
+    ns = (tiles - first) * S if S > 1 else 0
+    sl = -(-kt // S)
+    loads = []
+    for i in range(min(occ, 8)):
+        b = i * sms
+        whole = (f - b + G - 1) // G if b < f else 0
+        nsl = (ns - b + G - 1) // G if b < ns else 0
+        loads.append(float(whole * (kt + 1) + nsl * (sl + 1)))
+    loads.sort()
+    t, prev, n = 0.0, 0.0, len(loads)
+    for i, L in enumerate(loads):
+        w = (n - i) * cw
+        e = 0.88 if w >= 12 else 0.85 if w >= 8 else 0.40 if w >= 4 else 0.20
+        t += (n - i) * (L - prev) / e
+        prev = L
+    t *= BM * BN * BK / (128.0 * 2070.0)
+    if S > 1:
+        t += (tiles - first) * BM * BN * 4.0 * (2.0 * S + 1.0 + (1.0 if read_c else 0.0)) / 5.5e6 + 2.0
+    return t
+
+
+def split_tail(M, N, K, BM, BN, slots=NO_DEVICE_SLOTS, BK=32, cw=4, read_c=True, sms=152):
     """(first split tile, slices) of the split-tail rule: T tiles over G slots,
-    T = q*G + r; the last r tiles get S = G // r slices of at least 64 k."""
+    T = q*G + r; the last r tiles get S = G // r slices of at least 64 k, unless
+    the balance model finds a split at least 3% faster."""
     T = -(-M // BM) * -(-N // BN)
     q, r = divmod(T, slots)
     if r == 0:
         return 0, 1
-    S = min(slots // r, K // 64)
-    return (q * slots, S) if S >= 2 else (0, 1)
+    occ = slots // sms
+    smax = K // 64
+    S = min(slots // r, smax)
+    f = q * slots
+    if S < 2:
+        S, f = 1, 0
+    kt = -(-K // BK)
+    best = 0.97 * _tail_time(T, kt, sms, occ, f, S, BM, BN, BK, cw, read_c)
+    for qq in range(max(0, q - 2), q + 1):
+        if qq * slots >= T:
+            continue
+        for s in range(1, min(smax, 16) + 1):
+            if s == 1 and qq != q:
+                continue
+            t = _tail_time(T, kt, sms, occ, qq * slots, s, BM, BN, BK, cw, read_c)
+            if t < best:
+                best, S, f = t, s, (qq * slots if s > 1 else 0)
+    return (f, S) if S >= 2 else (0, 1)
 
 
 def want_bytes(base, M, N, K, BM, BN):
@@ -176,10 +218,21 @@ def test_split_tail_rule_examples():
     assert split_tail(4096, 4096, 4096, 128, 64, slots=456) == (1824, 2)
     # 2048^3 on 64 x 128 tiles over 456 slots: 512 = 456 + 56 -> 8 slices
     assert split_tail(2048, 2048, 2048, 64, 128, slots=456) == (456, 8)
-    # whole waves, too little k, or r too large for 2 slices: no split
+    # whole waves or too little k: no split
     assert split_tail(64 * 608, 128, 4096, 64, 128) == (0, 1)
     assert split_tail(4096, 4096, 127, 128, 64) == (0, 1)
-    assert split_tail(4096, 640, 4096, 128, 64) == (0, 1)  # 320 tiles > 608 / 2
+    # too many tiles left for 2 slices each, but SMs unevenly loaded (320
+    # tiles: some SMs run 3, the others 2): the balance model cuts every tile
+    assert split_tail(4096, 640, 4096, 128, 64) == (0, 5)
+    assert split_tail(4096, 640, 4096, 128, 64, slots=456) == (0, 4)
+    # measured on GB300 (456 slots): 1664^3 178.7 -> 157.8 us with every tile in
+    # 4 slices, 2560^3 546.8 -> 513.7 with the tiles after the first round in
+    # 2; 1408^3 and 3072^3 (alternatives measured slower) keep no split
+    assert split_tail(1664, 1664, 1664, 128, 64, slots=456) == (0, 4)
+    assert split_tail(2560, 2560, 2560, 128, 64, slots=456) == (456, 2)
+    assert split_tail(1408, 1408, 1408, 128, 64, slots=456) == (0, 1)
+    assert split_tail(3072, 3072, 3072, 128, 64, slots=456) == (0, 1)
+    assert split_tail(8192, 11008, 4096, 128, 64, slots=456) == (10944, 7)
 
 
 def test_workspace_size_query(b2g):
