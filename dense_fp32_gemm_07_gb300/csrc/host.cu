@@ -1088,8 +1088,8 @@ int run_tf32x3(const Call& c, void* stream, int variant) {
   float* Bhi = Alo + (size_t)c.M * c.K;
   float* Blo = Bhi + (size_t)c.N * c.K;
   if (tail_bytes) p.work = ws + split_bytes / sizeof(float);
-  cudaError_t e = launch_split_a(c.A, c.M, c.K, c.lda, Ahi, Alo, d->sms, st);
-  if (e == cudaSuccess) e = launch_split_bt(c.B, c.K, c.N, c.ldb, Bhi, Blo, st);
+  cudaError_t e =
+      launch_split_ab(c.A, c.M, c.K, c.lda, Ahi, Alo, c.B, c.N, c.ldb, Bhi, Blo, d->sms, st);
   CUtensorMap maps[4];
   if (e == cudaSuccess) {
     rc = encode_2d_sw128(&maps[0], Ahi, c.K, c.M, c.K, kTcBM);

@@ -12,8 +12,9 @@
 // |a||b| per product), accumulated in FP32 in tensor memory.
 //
 // Stages:
-//  1. split kernels (HBM bound): A -> A_hi, A_lo (M x K, row-major = K-major);
-//     B -> B_hi^T, B_lo^T (N x K, transposed so that B is K-major too);
+//  1. one split kernel (HBM bound): A -> A_hi, A_lo (M x K, row-major =
+//     K-major) and B -> B_hi^T, B_lo^T (N x K, transposed so that B is
+//     K-major too);
 //  2. a persistent tcgen05 kernel: one lane issues bulk-tensor copies of the
 //     four 128 x 32 tiles per stage (128-byte swizzle), one lane issues the
 //     three tcgen05.mma kind::tf32 per K step into a double-buffered 128 x 128
@@ -53,15 +54,15 @@ __device__ __forceinline__ void tf32_split(float x, float& hi, float& lo) {
 }
 
 // A (M x K, lda) -> Ahi, Alo (M x K, leading dimension K).  16-byte vectors:
-// A 16-byte aligned, lda and K multiples of 4.
-__global__ void __launch_bounds__(256) split_a_kernel(const float* __restrict__ A, int M, int K,
-                                                      long long lda, float* __restrict__ Ahi,
-                                                      float* __restrict__ Alo) {
-  pdl_wait();
+// A 16-byte aligned, lda and K multiples of 4.  Block `blk` of `nblk` takes
+// every nblk-th group of 256 vectors.
+__device__ __forceinline__ void split_a_part(const float* __restrict__ A, int M, int K,
+                                             long long lda, float* __restrict__ Ahi,
+                                             float* __restrict__ Alo, int blk, int nblk) {
   const long long kv = K / 4;
   const long long total = (long long)M * kv;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-       i += (long long)gridDim.x * blockDim.x) {
+  for (long long i = (long long)blk * blockDim.x + threadIdx.x; i < total;
+       i += (long long)nblk * blockDim.x) {
     const long long r = i / kv, c = (i - r * kv) * 4;
     const float4 v = *reinterpret_cast<const float4*>(A + r * lda + c);
     float4 h, l;
@@ -72,20 +73,19 @@ __global__ void __launch_bounds__(256) split_a_kernel(const float* __restrict__ 
     *reinterpret_cast<float4*>(Ahi + r * K + c) = h;
     *reinterpret_cast<float4*>(Alo + r * K + c) = l;
   }
-  pdl_launch_dependents();  // after the work, as in the transpose kernel
 }
 
 // B (K x N, ldb) -> Bhi^T, Blo^T (N x K, leading dimension K) in 64 x 64
 // tiles: coalesced reads of B rows, 16-byte writes of the transposed rows.  The
 // scalar shared-memory writes of the [n][k] tile (rows padded to 68 floats so
 // the 16-byte reads stay aligned) are 4-way bank conflicted, which the
-// HBM-bound kernel does not notice.  K % 4 == 0; N arbitrary.
-__global__ void __launch_bounds__(256) split_bt_kernel(const float* __restrict__ B, int K, int N,
-                                                       long long ldb, float* __restrict__ Bhi,
-                                                       float* __restrict__ Blo) {
-  __shared__ __align__(16) float tile[64][68];  // [n][k], rows padded to keep 16-byte reads aligned
-  pdl_wait();
-  const int k0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+// HBM-bound kernel does not notice.  K % 4 == 0; N arbitrary.  This block
+// takes the tile of columns 64 bx and rows 64 by.
+__device__ __forceinline__ void split_bt_part(const float* __restrict__ B, int K, int N,
+                                              long long ldb, float* __restrict__ Bhi,
+                                              float* __restrict__ Blo, int bx, int by,
+                                              float (&tile)[64][68]) {
+  const int k0 = by * 64, n0 = bx * 64;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   // load: warp w takes rows k = k0 + w + 8j; lanes take 32 consecutive n (twice)
 #pragma unroll
@@ -114,6 +114,24 @@ __global__ void __launch_bounds__(256) split_bt_kernel(const float* __restrict__
       *reinterpret_cast<float4*>(Blo + (long long)n * K + k) = l;
     }
   }
+}
+
+// Both splits in one launch: blocks 0 .. na-1 split A, the rest take B's 64 x
+// 64 tiles (a block's part is uniform across its threads, so the barrier in
+// B's part is reached by all of them).
+__global__ void __launch_bounds__(256) split_ab_kernel(const float* __restrict__ A, int M, int K,
+                                                       long long lda, float* __restrict__ Ahi,
+                                                       float* __restrict__ Alo, int na,
+                                                       const float* __restrict__ B, int N,
+                                                       long long ldb, float* __restrict__ Bhi,
+                                                       float* __restrict__ Blo, int tiles_x) {
+  __shared__ __align__(16) float tile[64][68];  // [n][k], rows padded to keep 16-byte reads aligned
+  pdl_wait();
+  const int b = (int)blockIdx.x;
+  if (b < na)
+    split_a_part(A, M, K, lda, Ahi, Alo, b, na);
+  else
+    split_bt_part(B, K, N, ldb, Bhi, Blo, (b - na) % tiles_x, (b - na) / tiles_x, tile);
   pdl_launch_dependents();  // after the work, as in the transpose kernel
 }
 
@@ -602,24 +620,23 @@ __global__ void __launch_bounds__(kTpThreads, 1)
 
 // ------------------------------------------------------------------- launchers
 
-cudaError_t launch_split_a(const float* A, int M, int K, long long lda, float* Ahi, float* Alo,
-                           int num_sms, cudaStream_t stream) {
+cudaError_t launch_split_ab(const float* A, int M, int K, long long lda, float* Ahi, float* Alo,
+                            const float* B, int N, long long ldb, float* Bhi, float* Blo,
+                            int num_sms, cudaStream_t stream) {
   const long long total = (long long)M * (K / 4);
-  long long blocks = (total + 255) / 256;
+  long long na = (total + 255) / 256;
   const long long cap = (long long)num_sms * 8;
-  if (blocks > cap) blocks = cap;
-  if (blocks < 1) blocks = 1;
-  void* args[] = {(void*)&A, (void*)&M, (void*)&K, (void*)&lda, (void*)&Ahi, (void*)&Alo};
-  return launch_pdl(reinterpret_cast<const void*>(&split_a_kernel), dim3((unsigned)blocks),
+  if (na > cap) na = cap;
+  if (na < 1) na = 1;
+  const long long tx = (N + 63) / 64, ty = (K + 63) / 64;
+  const long long blocks = na + tx * ty;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  int na_i = (int)na, tx_i = (int)tx;
+  void* args[] = {(void*)&A,   (void*)&M,   (void*)&K,   (void*)&lda, (void*)&Ahi, (void*)&Alo,
+                  (void*)&na_i, (void*)&B,  (void*)&N,   (void*)&ldb, (void*)&Bhi, (void*)&Blo,
+                  (void*)&tx_i};
+  return launch_pdl(reinterpret_cast<const void*>(&split_ab_kernel), dim3((unsigned)blocks),
                     dim3(256), args, 0, stream);
-}
-
-cudaError_t launch_split_bt(const float* B, int K, int N, long long ldb, float* Bhi, float* Blo,
-                            cudaStream_t stream) {
-  const dim3 grid((unsigned)((N + 63) / 64), (unsigned)((K + 63) / 64));
-  void* args[] = {(void*)&B, (void*)&K, (void*)&N, (void*)&ldb, (void*)&Bhi, (void*)&Blo};
-  return launch_pdl(reinterpret_cast<const void*>(&split_bt_kernel), grid, dim3(256), args, 0,
-                    stream);
 }
 
 cudaError_t launch_tf32x3(const Tf32x3Params& p, const CUtensorMap* maps, int num_sms,

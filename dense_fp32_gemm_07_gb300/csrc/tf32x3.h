@@ -26,12 +26,12 @@ struct Tf32x3Params {
 // Tile shape of the tensor-core kernel.
 constexpr int kTcBM = 128, kTcBN = 128, kTcBK = 32, kTcStages = 3;
 
-// A -> Ahi, Alo (M x K, ld K); B -> Bhi^T, Blo^T (N x K, ld K).  A, B 16-byte
-// aligned, lda % 4 == 0, K % 4 == 0.
-cudaError_t launch_split_a(const float* A, int M, int K, long long lda, float* Ahi, float* Alo,
-                           int num_sms, cudaStream_t stream);
-cudaError_t launch_split_bt(const float* B, int K, int N, long long ldb, float* Bhi, float* Blo,
-                            cudaStream_t stream);
+// A -> Ahi, Alo (M x K, ld K) and B -> Bhi^T, Blo^T (N x K, ld K), in one
+// launch.  A 16-byte aligned, lda % 4 == 0, K % 4 == 0; B read element by
+// element.
+cudaError_t launch_split_ab(const float* A, int M, int K, long long lda, float* Ahi, float* Alo,
+                            const float* B, int N, long long ldb, float* Bhi, float* Blo,
+                            int num_sms, cudaStream_t stream);
 
 // The GEMM on the split operands.  maps: Ahi, Alo, Bhi^T, Blo^T as 2-D tensors
 // {K, rows} with 128-byte swizzle and boxes {32, 128}.  tiles_m counts
