@@ -305,7 +305,7 @@ const char* const kTileTwins[][2] = {
 // plan is taken when its estimate is 3% lower (near a tie the wk plan's
 // second wave made it the slower one with operands out of L2: the ragged
 // 1000 x 1025 x 777, packed first, 50.9 us against 47.4).  Measured (us; split tail /
-// wk_32x64x16_g8 / wk_64x64x16_g4): 128^3 10.4 / 8.4 / 7.2, 256^3 10.2 / 7.2
+// 32 x 64 / 64 x 64 tiles, 16-k stages): 128^3 10.4 / 8.4 / 7.2, 256^3 10.2 / 7.2
 // / 8.1, 384^3 9.9 / 7.9 / 10.5, 512^3 12.4 / 9.2 / 13.2, 768^3 23.7 / 24.0 /
 // 18.6, 1024^3 47.6 / 59.2 / 47.0; strided batches (split tail / the wk plan
 // the model picks): 128 x 128^3 14.6 / 27.2, 64 x 256^3 48.4 / 53.2,
@@ -327,7 +327,7 @@ int warpk_choice(const Call& c, const char* rule_plan) {
   int pick = -1;
   const char* us = std::strchr(rule_plan, '_');
   const size_t fam = us ? (size_t)(us - rule_plan) : 0;
-  for (const char* tile : {"_32x64x16_g8", "_64x64x16_g4", "_64x128x16_g2"}) {
+  for (const char* tile : {"_32x64x32_g8", "_64x64x32_g4", "_64x128x32_g2"}) {
     char name[32];
     if (fam == 0 || fam + std::strlen(tile) >= sizeof(name)) break;
     std::memcpy(name, rule_plan, fam);

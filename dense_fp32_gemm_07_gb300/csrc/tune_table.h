@@ -51,7 +51,7 @@ const TuneRule kTuneTable[] = {
     // 64 x 128 tiles, whichever a wave model expects faster), unless the
     // split-tail plan of a later rule is expected faster (few tiles over a
     // long k range, or many waves)
-    {kClassFast, 0, kInf, 0, kInf, 0, "wk_32x64x16_g8", nullptr, 1.5e9},
+    {kClassFast, 0, kInf, 0, kInf, 0, "wk_32x64x32_g8", nullptr, 1.5e9},
     // the transpose costs about what it saves here; the packed-FMA form of
     // the k-chunked kernel (two CTAs per SM) beats the scalar one by 0.35-0.9
     // us a call (128^3 8.52 -> 7.71 us, 512^3 13.66 -> 13.31, 1000 x 1024 x
@@ -62,21 +62,21 @@ const TuneRule kTuneTable[] = {
     {kClassFast, 0, kInf, 0, kInf, 1.0e9, "pre_128x64x32_s3_o5", "tmaX_128x128x16_s6_o2"},
     // op(A) = A^T: small products in one launch (the wk kernel reading A
     // stored K x M), larger ones on the transposed-layout kernel
-    {kClassFastTransA, 0, kInf, 0, kInf, 0, "wkT_32x64x16_g8", nullptr, 1.5e9},
+    {kClassFastTransA, 0, kInf, 0, kInf, 0, "wkT_32x64x32_g8", nullptr, 1.5e9},
     {kClassFastTransA, 0, kInf, 0, kInf, 0, "tmaT_128x64x32_s3_o5", nullptr},
     // op(B) = B^T on aligned operands: B^T (and A, unless it comes stored
     // K x M) transposed into the workspace by the 16-byte-vector transpose,
     // then the wk kernel (one launch) or the transposed-layout kernel
     // (4096^3: packing both operands with 4-byte moves cost 3.5% of the
     // call); small calls take the 4-byte feed
-    {kClassFastTransB, 0, kInf, 0, kInf, 5.0e7, "wkR_32x64x16_g8", "gen_64x64x16_s4", 1.5e9},
+    {kClassFastTransB, 0, kInf, 0, kInf, 5.0e7, "wkR_32x64x32_g8", "gen_64x64x16_s4", 1.5e9},
     {kClassFastTransB, 0, kInf, 0, kInf, 5.0e7, "pret_128x64x32_s3_o5", "gen_64x64x16_s4"},
     {kClassFastTransB, 0, kInf, 0, kInf, 0, "gen_64x64x16_s4", nullptr},
     // anything else (misaligned pointers, odd leading dimensions, K % 4 != 0,
     // op(B) = B^T): pack A^T and B aligned into the workspace, then the wk
     // kernel (one launch) or the transposed-layout kernel; the 4-byte feed
     // needs no workspace
-    {kClassGeneral, 0, kInf, 0, kInf, 5.0e7, "wkP_32x64x16_g8", "gen_64x64x16_s4", 1.5e9},
+    {kClassGeneral, 0, kInf, 0, kInf, 5.0e7, "wkP_32x64x32_g8", "gen_64x64x16_s4", 1.5e9},
     {kClassGeneral, 0, kInf, 0, kInf, 5.0e7, "pack_128x64x32_s3_o5", "gen_64x64x16_s4"},
     {kClassGeneral, 0, kInf, 0, kInf, 0, "gen_64x64x16_s4", nullptr},
 };

@@ -111,15 +111,15 @@ def test_tune_table_classes(b2g):
     assert _plan(b2g, 0, 0, 16, 4095, 4096, 1.0, FAKE, 4096, FAKE, 4096, FAKE, 4096).startswith("tma_")
     # small products: one launch, the k range split between a CTA's warps;
     # few tiles over a long k range keep the split-tail plan
-    assert _plan(b2g, 0, 0, 64, 64, 64, 1.0, FAKE, 64, FAKE, 64, FAKE, 64) == "wk_32x64x16_g8"
-    assert _plan(b2g, 0, 0, 512, 512, 512, 1.0, FAKE, 512, FAKE, 512, FAKE, 512) == "wk_32x64x16_g8"
-    assert _plan(b2g, 0, 0, 768, 768, 768, 1.0, FAKE, 768, FAKE, 768, FAKE, 768) == "wk_64x64x16_g4"
+    assert _plan(b2g, 0, 0, 64, 64, 64, 1.0, FAKE, 64, FAKE, 64, FAKE, 64) == "wk_32x64x32_g8"
+    assert _plan(b2g, 0, 0, 512, 512, 512, 1.0, FAKE, 512, FAKE, 512, FAKE, 512) == "wk_32x64x32_g8"
+    assert _plan(b2g, 0, 0, 768, 768, 768, 1.0, FAKE, 768, FAKE, 768, FAKE, 768) == "wk_64x64x32_g4"
     assert _plan(b2g, 0, 0, 128, 128, 32768, 1.0, FAKE, 32768, FAKE, 128, FAKE, 128).startswith("tma_")
     # odd leading dimension -> operands packed into the workspace first
     assert _plan(b2g, 0, 0, 1000, 1025, 777, 0.75, FAKE, 777, FAKE, 1025, FAKE, 1025).startswith(
         ("pack_", "wkP_"))
     # misaligned base pointer -> packed (small: then the one-launch wk kernel)
-    assert _plan(b2g, 0, 0, 512, 512, 512, 1.0, FAKE + 4, 512, FAKE, 512, FAKE, 512) == "wkP_32x64x16_g8"
+    assert _plan(b2g, 0, 0, 512, 512, 512, 1.0, FAKE + 4, 512, FAKE, 512, FAKE, 512) == "wkP_32x64x32_g8"
     assert _plan(b2g, 0, 0, 2048, 2048, 2048, 1.0, FAKE + 4, 2048, FAKE, 2048, FAKE, 2048).startswith("pack_")
     # K not a multiple of 4 -> packed
     assert _plan(b2g, 0, 0, 512, 512, 510, 1.0, FAKE, 512, FAKE, 512, FAKE, 512).startswith("wkP_")
@@ -128,10 +128,10 @@ def test_tune_table_classes(b2g):
     # op(A) = A^T aligned -> transposed-layout bulk-tensor plan; op(B) = B^T
     # aligned -> B^T (and A) transposed with 16-byte vectors, then that plan
     # (small products of each class on the one-launch wk kernel)
-    assert _plan(b2g, 1, 0, 512, 512, 512, 1.0, FAKE, 512, FAKE, 512, FAKE, 512) == "wkT_32x64x16_g8"
+    assert _plan(b2g, 1, 0, 512, 512, 512, 1.0, FAKE, 512, FAKE, 512, FAKE, 512) == "wkT_32x64x32_g8"
     assert _plan(b2g, 1, 0, 4096, 4096, 4096, 1.0, FAKE, 4096, FAKE, 4096, FAKE, 4096).startswith("tmaT_")
-    assert _plan(b2g, 0, 1, 512, 512, 512, 1.0, FAKE, 512, FAKE, 512, FAKE, 512) == "wkR_32x64x16_g8"
-    assert _plan(b2g, 1, 1, 512, 512, 512, 1.0, FAKE, 512, FAKE, 512, FAKE, 512) == "wkR_32x64x16_g8"
+    assert _plan(b2g, 0, 1, 512, 512, 512, 1.0, FAKE, 512, FAKE, 512, FAKE, 512) == "wkR_32x64x32_g8"
+    assert _plan(b2g, 1, 1, 512, 512, 512, 1.0, FAKE, 512, FAKE, 512, FAKE, 512) == "wkR_32x64x32_g8"
     assert _plan(b2g, 0, 1, 4096, 4096, 4096, 1.0, FAKE, 4096, FAKE, 4096, FAKE, 4096).startswith("pret_")
     # op(B) = B^T with K % 4 != 0 or an odd leading dimension -> packed
     assert _plan(b2g, 0, 1, 512, 512, 510, 1.0, FAKE, 512, FAKE, 510, FAKE, 512).startswith("wkP_")

@@ -19,8 +19,8 @@ def tb():
 @pytest.mark.parametrize("plan_name,M,N,K", [
     ("tma_64x128x16_s6_o2", 64, 64, 64),
     ("tma_64x128x16_s6_o5", 64, 64, 64),      # packed, k-chunked A
-    ("wk_32x64x16_g8", 64, 64, 64),           # the small-problem plans: k split between warps
-    ("wk_64x64x16_g4", 64, 64, 64),
+    ("wk_32x64x32_g8", 64, 64, 64),           # the small-problem plans: k split between warps
+    ("wk_64x64x32_g4", 64, 64, 64),
     ("tmaX_64x128x16_s6_o1", 64, 64, 64),
     ("gen_64x64x16_s4", 64, 64, 64),
     ("pre_128x64x32_s3_o5", 64, 64, 128),   # packed kernels, both tile shapes
