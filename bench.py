@@ -615,7 +615,7 @@ def run_ours(args, w):
         raise RuntimeError(f"kernel status word {flags:#x}")
 
     # every configuration of the workload list, each with the oracle beside it
-    configs = {}
+    per_workload = {}
     if not args.no_configs:
         for name, cw in workloads.WORKLOADS.items():
             entry, (cA, cB, cC) = time_config(torch, b2g, cw, dev, stream, peak, hpeak,
@@ -624,7 +624,7 @@ def run_ours(args, w):
                 entry["oracle"] = oracle_rate(cw, cA, cB, cC, args.oracle_seconds)
                 entry["gpu_over_oracle"] = round(entry["tflops"] * 1e3
                                                  / entry["oracle"]["gflops"], 1)
-            configs[name] = entry
+            per_workload[name] = entry
             del cA, cB, cC
         rc, flags = b2g.b2g_status(stream.cuda_stream)
         if rc or flags:
@@ -684,8 +684,8 @@ def run_ours(args, w):
                          "frac": sk_gbs / hpeak, "algorithmic_bytes": sk.min_bytes(),
                          "peak_basis": hbasis},
         }
-        if configs:
-            line["configs"] = configs
+        if per_workload:
+            line["configs"] = per_workload
             line["configs_note"] = (
                 "per workload: us_per_call = back-to-back calls through the C ABI (CUDA events "
                 "on the launching stream); graph_us_per_call = the same calls replayed from a "

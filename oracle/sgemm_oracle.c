@@ -14,7 +14,7 @@
  * Choices (readings of points the pages leave open):
  *  - Every product and sum is taken in double (the pages' own CPU reference
  *    accumulates in float; double makes the oracle far more accurate than any
- *    FP32 result it judges).
+ *    FP32 result it checks).
  *  - Loop order is i-k-j with a per-row accumulator, the order of the
  *    handbook's CPU reference (section 完整代码, gemm_cpu); rows are independent,
  *    so OpenMP splits them across cores without changing any sum.
@@ -26,7 +26,7 @@
  *
  * Besides the result it returns, per element, the elementwise error budget
  *     bound_ij = 2*K*2^-24 * (|alpha| * sum_k |a_ik||b_kj| + |beta * c_ij|) + 1e-6
- * used to judge an FP32 result, and the number of multiply-adds it performed.
+ * used to check an FP32 result, and the number of multiply-adds it performed.
  */
 #include <math.h>
 #include <stdint.h>
