@@ -200,8 +200,7 @@ __global__ void __launch_bounds__(WarpkCfg<WM, WN, KG, BK, STAGES, ALAY>::kThrea
   // Sum the groups' partial tiles in group order and write C: each thread takes
   // float4 positions e = t, t + kConsumers, ... of the tile (row e / (BN/4)).
   constexpr int kPos = BM * BN / 4;
-  constexpr int kPer = kPos / Cfg::kConsumers;
-  static_assert(kPos % Cfg::kConsumers == 0, "whole float4 positions per thread");
+  constexpr int kPer = (kPos + Cfg::kConsumers - 1) / Cfg::kConsumers;
   const int t = threadIdx.x - 32;
   float* Cb = p.C + (long long)bt * p.strideC;
   const float alpha = p.alpha, beta = p.beta;
@@ -211,7 +210,7 @@ __global__ void __launch_bounds__(WarpkCfg<WM, WN, KG, BK, STAGES, ALAY>::kThrea
     for (int u = 0; u < kPer; ++u) {
       const int e = t + u * Cfg::kConsumers;
       const int gr = m0 + e / (BN / 4), gc = n0 + 4 * (e % (BN / 4));
-      if (gr < p.M && gc + 3 < p.N)
+      if (e < kPos && gr < p.M && gc + 3 < p.N)
         cv[u] = *reinterpret_cast<const float4*>(Cb + (long long)gr * p.ldc + gc);
     }
   }
@@ -219,7 +218,7 @@ __global__ void __launch_bounds__(WarpkCfg<WM, WN, KG, BK, STAGES, ALAY>::kThrea
   for (int u = 0; u < kPer; ++u) {
     const int e = t + u * Cfg::kConsumers;
     const int gr = m0 + e / (BN / 4), gc = n0 + 4 * (e % (BN / 4));
-    if (gr >= p.M || gc >= p.N) continue;
+    if (e >= kPos || gr >= p.M || gc >= p.N) continue;
     float4 s = *reinterpret_cast<const float4*>(part + 4 * e);
 #pragma unroll
     for (int q = 1; q < KG; ++q) {
