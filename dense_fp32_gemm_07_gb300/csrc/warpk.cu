@@ -6,24 +6,22 @@
 // into slices that write partial sums to a workspace and add them in a
 // second kernel: two launches, the partial sums' round trip through L2 and a
 // dependency between them, about 8 us a call even at 128^3.  Here one CTA
-// takes one small output tile (BM x BN = 32 WM x 64 WN) and KG groups of
+// takes one small output tile (BM x BN = 32 WM x 64 WN), and KG groups of
 // WM x WN consumer warps take its k tiles in turn (k tile t goes to group
-// t % KG),
-// each warp with the 8 x 8 register outer product of the FFMA plans (packed
-// two-lane FMAs, B row-major; A either row-major, k-chunked by a 3-D
-// bulk-tensor view, or stored K x M, landing transposed).  When
-// the groups are done, their partial tiles meet in the drained shared-memory
-// ring and are added in group order, then C = alpha * sum + beta * C is
-// written: one launch, no workspace.  Every output element is a fixed-order
-// sum (k order inside a group, group order across them), so the results are
-// bitwise reproducible run to run.
+// t % KG).  Each warp keeps the 8 x 8 register outer product of the FFMA
+// plans (packed two-lane FMAs; B row-major; A either row-major, k-chunked by
+// a 3-D bulk-tensor view, or stored K x M, landing transposed).  When the
+// groups are done, their partial tiles meet in the drained shared-memory ring
+// and are added in group order, then C = alpha * sum + beta * C is written:
+// one launch, no workspace.  Every output element is a fixed-order sum (k
+// order inside a group, group order across them), so the results are bitwise
+// reproducible run to run.
 //
-// One elected producer thread fills an S-stage ring of 32-k stages (16-k
-// stages measured 4-11% slower from 384^3 to 1024^3: twice the barrier round
-// trips) with bulk-tensor copies
-// (full/empty mbarriers, S a multiple of KG so that a slot always serves the
-// same group); every wait is bounded and a timeout leaves C untouched, with
-// the reason in the status word.
+// One elected producer thread fills an S-stage ring of 32-k stages with
+// bulk-tensor copies (full/empty mbarriers; S a multiple of KG, so that a
+// slot always serves the same group).  16-k stages measured 4-11% slower from
+// 384^3 to 1024^3 (twice the barrier round trips).  Every wait is bounded and
+// a timeout leaves C untouched, with the reason in the status word.
 #include "plan_registry.h"
 #include "sgemm_ffma.cuh"
 
@@ -282,11 +280,10 @@ cudaError_t launch_warpk(const SgemmParams& p, const CUtensorMap* tmA, const CUt
   }
 
 // Fields: name, warp tiles WM x WN (BM = 32 WM, BN = 64 WN), k groups KG, BK,
-// stages, A's layout
-// in shared memory, what runs before the kernel (as for the FFMA plans: 0
-// nothing, 2 both operands packed aligned with A transposed, 3 B^T (and A)
-// transposed with 16-byte vectors).  No occupancy function: the host then
-// gives these plans no split tail.
+// stages, A's layout in shared memory, what runs before the kernel (as for
+// the FFMA plans: 0 nothing, 2 both operands packed aligned with A
+// transposed, 3 B^T (and A) transposed with 16-byte vectors).  No occupancy
+// function: the host then gives these plans no split tail.
 //   wk_   row-major A, k-chunked (aligned operands)
 //   wkT_  A stored K x M (op(A) = A^T, aligned operands)
 //   wkP_  any operands, packed first
