@@ -104,3 +104,16 @@ def test_k_chunked_schedule(tb, shape, beta):
     hA, hB, hC = (torch.from_numpy(x).pin_memory() for x in (A, B, C))
     b2g.sgemm_host(hA, hB, hC, 0.75, beta)
     check(hC.numpy(), ref, bound, f"host chunked {shape} beta={beta}")
+
+
+def test_k_chunked_beta_zero_does_not_read_c(tb):
+    """K >= 2048 with beta = 0: the chunks' products and the panel kernel
+    never read C, so NaN in C does not reach the result."""
+    torch, b2g = tb
+    M, N, K = 1300, 516, 2048
+    A, B, _ = _inputs(12, M, N, K)
+    C = np.full((M, N), np.nan, np.float32)
+    ref, bound, _ = oracle.sgemm(A, B, None, -0.5, 0.0)
+    hA, hB, hC = (torch.from_numpy(x).pin_memory() for x in (A, B, C))
+    b2g.sgemm_host(hA, hB, hC, -0.5, 0.0)
+    check(hC.numpy(), ref, bound, "host chunked beta 0, NaN C")
