@@ -71,12 +71,18 @@ const TuneRule kTuneTable[] = {
     // call); small calls take the 4-byte feed
     {kClassFastTransB, 0, kInf, 0, kInf, 5.0e7, "wkR_32x64x32_g8", "gen_64x64x16_s4", 1.5e9},
     {kClassFastTransB, 0, kInf, 0, kInf, 5.0e7, "pret_128x64x32_s3_o5", "gen_64x64x16_s4"},
+    // below 5e7 multiply-adds one packing launch for both operands beats the
+    // two transposes, and either beats the 4-byte feed 2-4x (128^3 6.9 / 8.5 /
+    // 14.6 us, 300^3 8.3 / 9.2 / 19.0), which stays the fallback without a
+    // workspace
+    {kClassFastTransB, 0, kInf, 0, kInf, 0, "wkP_32x64x32_g8", "gen_64x64x16_s4", 5.0e7},
     {kClassFastTransB, 0, kInf, 0, kInf, 0, "gen_64x64x16_s4", nullptr},
     // anything else (misaligned pointers, odd leading dimensions, K % 4 != 0,
     // op(B) = B^T): pack A^T and B aligned into the workspace, then the wk
     // kernel (one launch) or the transposed-layout kernel; the 4-byte feed
-    // needs no workspace
-    {kClassGeneral, 0, kInf, 0, kInf, 5.0e7, "wkP_32x64x32_g8", "gen_64x64x16_s4", 1.5e9},
+    // needs no workspace and is the fallback (128 x 128 x 127: packed + wk
+    // 7.5 us, 4-byte feed 33.2; 300 x 300 x 301: 9.8 against 19.5)
+    {kClassGeneral, 0, kInf, 0, kInf, 0, "wkP_32x64x32_g8", "gen_64x64x16_s4", 1.5e9},
     {kClassGeneral, 0, kInf, 0, kInf, 5.0e7, "pack_128x64x32_s3_o5", "gen_64x64x16_s4"},
     {kClassGeneral, 0, kInf, 0, kInf, 0, "gen_64x64x16_s4", nullptr},
 };

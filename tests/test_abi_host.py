@@ -123,8 +123,9 @@ def test_tune_table_classes(b2g):
     assert _plan(b2g, 0, 0, 2048, 2048, 2048, 1.0, FAKE + 4, 2048, FAKE, 2048, FAKE, 2048).startswith("pack_")
     # K not a multiple of 4 -> packed
     assert _plan(b2g, 0, 0, 512, 512, 510, 1.0, FAKE, 512, FAKE, 512, FAKE, 512).startswith("wkP_")
-    # small general problems -> 4-byte feed (no workspace)
-    assert _plan(b2g, 0, 0, 64, 64, 63, 1.0, FAKE, 64, FAKE, 64, FAKE, 64).startswith("gen_")
+    # small general problems -> packed, then the one-launch wk kernel (the
+    # 4-byte feed is the fallback without a workspace)
+    assert _plan(b2g, 0, 0, 64, 64, 63, 1.0, FAKE, 64, FAKE, 64, FAKE, 64).startswith("wkP_")
     # op(A) = A^T aligned -> transposed-layout bulk-tensor plan; op(B) = B^T
     # aligned -> B^T (and A) transposed with 16-byte vectors, then that plan
     # (small products of each class on the one-launch wk kernel)
@@ -137,8 +138,8 @@ def test_tune_table_classes(b2g):
     assert _plan(b2g, 0, 1, 512, 512, 510, 1.0, FAKE, 512, FAKE, 510, FAKE, 512).startswith("wkP_")
     assert _plan(b2g, 0, 1, 512, 512, 512, 1.0, FAKE, 512, FAKE, 513, FAKE, 512).startswith("wkP_")
     assert _plan(b2g, 0, 1, 2048, 2048, 2048, 1.0, FAKE, 2048, FAKE, 2049, FAKE, 2048).startswith("pack_")
-    # small op(B) = B^T calls -> 4-byte feed
-    assert _plan(b2g, 0, 1, 64, 64, 64, 1.0, FAKE, 64, FAKE, 64, FAKE, 64).startswith("gen_")
+    # small op(B) = B^T calls -> one packing launch, then the wk kernel
+    assert _plan(b2g, 0, 1, 64, 64, 64, 1.0, FAKE, 64, FAKE, 64, FAKE, 64).startswith("wkP_")
 
 
 # With no device answering, the host sizes splits for 152 SMs x 4 resident CTAs.
