@@ -299,8 +299,9 @@ const char* const kTileTwins[][2] = {
 // The one-launch small-problem plans (wk_*: one CTA per output tile, its k
 // range split between the CTA's warps) against the split-tail plan that the
 // next rule names, by a model fitted to GB300 timings of back-to-back calls:
-// a wk call takes 2.0 + waves x (2.4 + BM x BN x K x 4.6e-6) us (waves of one
-// CTA per SM; each wave pays its CTAs' start, first copies and reduction),
+// a wk call takes 2.0 + waves x (2.4 + BM x BN x K x 4.6e-6 x (1 + 0.1 x
+// log2(K / 1024) above K = 1024)) us (waves of one CTA per SM; each wave pays
+// its CTAs' start, first copies and reduction),
 // the split-tail plan 7.4 + (M N K of the whole call) x 3.7e-8 us, and a wk
 // plan is taken when its estimate is 3% lower (near a tie the wk plan's
 // second wave made it the slower one with operands out of L2: the ragged
@@ -325,6 +326,9 @@ int warpk_choice(const Call& c, const char* rule_plan) {
   const double b = c.batch > 0 ? c.batch : 1;
   double best = 0.97 * (7.4 + (double)c.M * c.N * (double)c.K * b * 3.7e-8);
   int pick = -1;
+  // a CTA's FP32 pipe keeps less busy over a long k range (1-wave timings:
+  // 4.6e-6 us per multiply-add of a CTA up to K = 1024, 5.5e-6 at K = 4096)
+  const double long_k = c.K > 1024 ? 1.0 + 0.1 * std::log2((double)c.K / 1024.0) : 1.0;
   const char* us = std::strchr(rule_plan, '_');
   const size_t fam = us ? (size_t)(us - rule_plan) : 0;
   for (const char* tile : {"_32x64x32_g8", "_64x64x32_g4", "_64x128x32_g2"}) {
@@ -337,7 +341,7 @@ int warpk_choice(const Call& c, const char* rule_plan) {
     const Plan& pl = *plan_at(i);
     const double tiles = (double)((c.M + pl.BM - 1) / pl.BM) * ((c.N + pl.BN - 1) / pl.BN) * b;
     const double waves = std::ceil(tiles / sms);
-    const double t = 2.0 + waves * (2.4 + pl.BM * pl.BN * (double)c.K * 4.6e-6);
+    const double t = 2.0 + waves * (2.4 + pl.BM * pl.BN * (double)c.K * 4.6e-6 * long_k);
     if (t <= best) best = t, pick = i;
   }
   return pick;
