@@ -19,9 +19,10 @@
 //
 // One elected producer thread fills an S-stage ring of 32-k stages with
 // bulk-tensor copies (full/empty mbarriers; S a multiple of KG, so that a
-// slot always serves the same group; two slots a group for the 8-group
-// tile: with one, a group waits for its slot's refill after every stage, and
-// 64 x 4096 x 4096 took 50.5 us against 47.4).  16-k stages measured 4-11% slower from
+// slot always serves the same group).  With one slot a group (the 8-group
+// tile) a group waits for its slot's refill after every stage: two slots
+// took 64 x 4096 x 4096 from 50.5 to 47.4 us but 512^3 from 8.42 to 8.58, and
+// the table sends long k ranges to the split-tail plans anyway.  16-k stages measured 4-11% slower from
 // 384^3 to 1024^3 (twice the barrier round trips).  Every wait is bounded and
 // a timeout leaves C untouched, with the reason in the status word.
 #include "plan_registry.h"
@@ -291,16 +292,16 @@ cudaError_t launch_warpk(const SgemmParams& p, const CUtensorMap* tmA, const CUt
 //   wkP_  any operands, packed first
 //   wkR_  op(B) = B^T on aligned operands, transposed first
 const Plan kPlansWarpk[] = {
-    B2G_WARPK_PLAN("wk_32x64x32_g8", 1, 1, 8, 32, 16, kAKChunk, 0),
+    B2G_WARPK_PLAN("wk_32x64x32_g8", 1, 1, 8, 32, 8, kAKChunk, 0),
     B2G_WARPK_PLAN("wk_64x64x32_g4", 2, 1, 4, 32, 8, kAKChunk, 0),
     B2G_WARPK_PLAN("wk_64x128x32_g2", 2, 2, 2, 32, 8, kAKChunk, 0),
-    B2G_WARPK_PLAN("wkT_32x64x32_g8", 1, 1, 8, 32, 16, kAKMajor, 0),
+    B2G_WARPK_PLAN("wkT_32x64x32_g8", 1, 1, 8, 32, 8, kAKMajor, 0),
     B2G_WARPK_PLAN("wkT_64x64x32_g4", 2, 1, 4, 32, 8, kAKMajor, 0),
     B2G_WARPK_PLAN("wkT_64x128x32_g2", 2, 2, 2, 32, 8, kAKMajor, 0),
-    B2G_WARPK_PLAN("wkP_32x64x32_g8", 1, 1, 8, 32, 16, kAKMajor, 2),
+    B2G_WARPK_PLAN("wkP_32x64x32_g8", 1, 1, 8, 32, 8, kAKMajor, 2),
     B2G_WARPK_PLAN("wkP_64x64x32_g4", 2, 1, 4, 32, 8, kAKMajor, 2),
     B2G_WARPK_PLAN("wkP_64x128x32_g2", 2, 2, 2, 32, 8, kAKMajor, 2),
-    B2G_WARPK_PLAN("wkR_32x64x32_g8", 1, 1, 8, 32, 16, kAKMajor, 3),
+    B2G_WARPK_PLAN("wkR_32x64x32_g8", 1, 1, 8, 32, 8, kAKMajor, 3),
     B2G_WARPK_PLAN("wkR_64x64x32_g4", 2, 1, 4, 32, 8, kAKMajor, 3),
     B2G_WARPK_PLAN("wkR_64x128x32_g2", 2, 2, 2, 32, 8, kAKMajor, 3),
 };
