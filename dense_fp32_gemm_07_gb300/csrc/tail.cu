@@ -2,10 +2,12 @@
 //
 // A persistent grid of G CTAs that runs T output tiles finishes when its
 // busiest SM does: with T = q*G + r (0 < r < G) the last round keeps only r
-// CTAs busy.  The host therefore cuts each of the last r tiles into S k slices
-// (S = G / r, at least 64 k per slice), so every CTA gets q whole tiles plus
-// at most one slice.  The GEMM kernel writes each slice's raw BM x BN sums to
-// the workspace; this kernel adds a tile's S slices in slice order (a fixed
+// CTAs busy.  The host therefore cuts the tiles from tail_first on into S k
+// slices of at least 64 k: by default the last r tiles with S = G / r, so
+// every CTA gets q whole tiles plus at most one slice, or, where a per-SM
+// balance model expects it to be faster, the tiles of the last rounds into
+// more slices.  The GEMM kernel writes each slice's raw BM x BN sums to the
+// workspace; this kernel adds a tile's S slices in slice order (a fixed
 // order: results are reproducible run to run) and applies the same epilogue
 // as the GEMM kernel, C = alpha * sum + beta * C, reading C only when
 // beta != 0.
