@@ -171,9 +171,10 @@ int b2g_sgemm_host(int M, int N, int K, float alpha, const float* A, int lda, co
 /*
  * Workspace bytes the tune table's plan wants for these arguments (0 when it
  * needs none), stored in *bytes: A^T or the packed operands when the plan
- * writes them, then (256-byte aligned) the split tail's partial sums, at most
- * SMs x resident CTAs x BM x BN floats.  The split depends on the current
- * device's SM count and occupancy.  Returns 0, a B2G_ERR_* code for invalid
+ * writes them, then (256-byte aligned) the split tail's partial sums, one
+ * BM x BN block of floats per k slice of every split tile (at most 16 slices
+ * a tile; 224 tiles x 2 slices at 4096^3, 338 x 4 at 1664^3).  The split
+ * depends on the current device's SM count and occupancy.  Returns 0, a B2G_ERR_* code for invalid
  * arguments, or B2G_ERR_NULL when bytes is NULL.  Launches nothing.
  */
 int b2g_sgemm_workspace_size(int transA, int transB, int M, int N, int K, float alpha,
